@@ -1,0 +1,17 @@
+"""GB300-native (sm_103a) dynamic sparse 3D attention for video DiT training (DSV).
+
+The compute path is a C-ABI CUDA library (``libdsv.so``, entry points declared in
+``include/dsv.h``); :mod:`.binding` is a thin ctypes layer over it that passes
+device pointers, sizes and the current CUDA stream.  Importing this package does not
+load the library; the first call does, and fails loudly if it has not been built.
+"""
+from .binding import (  # noqa: F401
+    DSVError,
+    dsv_estimate_topk,
+    dsv_estimate_topk_workspace,
+    dsv_sparse_attn_bwd,
+    dsv_sparse_attn_bwd_workspace,
+    dsv_sparse_attn_fwd,
+    library_path,
+    load_library,
+)

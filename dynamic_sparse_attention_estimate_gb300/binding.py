@@ -1,0 +1,187 @@
+"""ctypes binding of libdsv.so (the C ABI declared in include/dsv.h).
+
+Argument marshalling only: each function checks dtypes/shapes of the torch tensors it
+is given, allocates outputs with torch on the input's device, and passes raw device
+pointers, sizes and the current CUDA stream to the library.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libdsv.so"
+_lib = None
+
+DSV_OK = 0
+STATUS_NAMES = {0: "DSV_OK", 1: "DSV_ERR_INVALID_ARG", 2: "DSV_ERR_UNSUPPORTED", 3: "DSV_ERR_WORKSPACE",
+                4: "DSV_ERR_CUDA", 5: "DSV_ERR_DEVICE_CHECK"}
+
+EXPORTED = (
+    "dsv_estimate_topk_workspace", "dsv_estimate_topk", "dsv_sparse_attn_fwd",
+    "dsv_sparse_attn_bwd_workspace", "dsv_sparse_attn_bwd_workspace_min", "dsv_sparse_attn_bwd",
+    "dsv_status_string", "dsv_last_error_message", "dsv_last_device_status",
+)
+
+
+class DSVError(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("d", ctypes.c_int64), ("r", ctypes.c_int64), ("block", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("scale", ctypes.c_float)]
+
+
+def library_path() -> str:
+    return os.environ.get("DSV_LIBRARY", os.path.join(_HERE, _LIB_NAME))
+
+
+def load_library(path: Optional[str] = None):
+    """Load libdsv.so (once).  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} not found: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    dp = ctypes.POINTER(Dims)
+    lib.dsv_estimate_topk_workspace.argtypes = [dp]
+    lib.dsv_estimate_topk_workspace.restype = sz
+    lib.dsv_estimate_topk.argtypes = [dp, vp, vp, vp, vp, sz, vp]
+    lib.dsv_estimate_topk.restype = st
+    lib.dsv_sparse_attn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
+    lib.dsv_sparse_attn_fwd.restype = st
+    lib.dsv_sparse_attn_bwd_workspace.argtypes = [dp]
+    lib.dsv_sparse_attn_bwd_workspace.restype = sz
+    lib.dsv_sparse_attn_bwd_workspace_min.argtypes = [dp]
+    lib.dsv_sparse_attn_bwd_workspace_min.restype = sz
+    lib.dsv_sparse_attn_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.dsv_sparse_attn_bwd.restype = st
+    lib.dsv_status_string.argtypes = [st]
+    lib.dsv_status_string.restype = ctypes.c_char_p
+    lib.dsv_last_error_message.argtypes = []
+    lib.dsv_last_error_message.restype = ctypes.c_char_p
+    lib.dsv_last_device_status.argtypes = [vp]
+    lib.dsv_last_device_status.restype = st
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def make_dims(B, H, N, d, r, k, block=64, scale: Optional[float] = None) -> Dims:
+    return Dims(int(B), int(H), int(N), int(d), int(r), int(block), int(k),
+                float(scale) if scale is not None else 0.0)
+
+
+def _check(status: int, what: str):
+    if status != DSV_OK:
+        lib = load_library()
+        msg = lib.dsv_last_error_message()
+        raise DSVError(status, what, msg.decode() if msg else "")
+
+
+def _stream_ptr(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: need a contiguous CUDA {dtype} tensor with {ndim} dims, got "
+                         f"{t.dtype} {tuple(t.shape)} contiguous={t.is_contiguous()} device={t.device}")
+
+
+# ---------------------------------------------------------------- entry points (same names as the C ABI)
+
+def dsv_estimate_topk_workspace(dims: Dims) -> int:
+    return int(load_library().dsv_estimate_topk_workspace(ctypes.byref(dims)))
+
+
+def dsv_estimate_topk(q_lr: torch.Tensor, k_lr: torch.Tensor, k: int, block: int = 64,
+                      idx: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """idx [B, H, N/block, k] int32 of the top-k keys per query block (ascending)."""
+    _need(q_lr, "q_lr", torch.bfloat16, 4)
+    _need(k_lr, "k_lr", torch.bfloat16, 4)
+    B, H, N, r = q_lr.shape
+    if k_lr.shape != q_lr.shape:
+        raise ValueError("q_lr and k_lr must have the same shape")
+    dims = make_dims(B, H, N, 0, r, k, block)
+    if idx is None:
+        idx = torch.empty((B, H, max(N // block, 0), int(k)), dtype=torch.int32, device=q_lr.device)
+    lib = load_library()
+    ws_bytes = int(lib.dsv_estimate_topk_workspace(ctypes.byref(dims)))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q_lr.device) if ws_bytes else None
+    _check(lib.dsv_estimate_topk(ctypes.byref(dims), _ptr(q_lr), _ptr(k_lr), _ptr(idx), _ptr(ws), ws_bytes,
+                                 _stream_ptr(q_lr)), "dsv_estimate_topk")
+    return idx
+
+
+def dsv_sparse_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, block: int = 64,
+                        scale: Optional[float] = None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """(O bf16 [B,H,N,d], LSE fp32 [B,H,N]) of softmax attention over the selected keys."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(idx, "idx", torch.int32, 4)
+    B, H, N, d = q.shape
+    kk = idx.shape[3]
+    dims = make_dims(B, H, N, d, 0, kk, block, scale)
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    lib = load_library()
+    _check(lib.dsv_sparse_attn_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
+                                   _stream_ptr(q)), "dsv_sparse_attn_fwd")
+    return o, lse
+
+
+def dsv_sparse_attn_bwd_workspace(dims: Dims, minimum: bool = False) -> int:
+    lib = load_library()
+    f = lib.dsv_sparse_attn_bwd_workspace_min if minimum else lib.dsv_sparse_attn_bwd_workspace
+    return int(f(ctypes.byref(dims)))
+
+
+def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                        lse: torch.Tensor, idx: torch.Tensor, block: int = 64, scale: Optional[float] = None,
+                        workspace: Optional[torch.Tensor] = None, out=None):
+    """(dQ, dK, dV) bf16 [B,H,N,d]; dK/dV reduced deterministically per key."""
+    for t, n in ((do, "do"), (q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    _need(idx, "idx", torch.int32, 4)
+    B, H, N, d = q.shape
+    kk = idx.shape[3]
+    dims = make_dims(B, H, N, d, 0, kk, block, scale)
+    lib = load_library()
+    if workspace is None:
+        nbytes = int(lib.dsv_sparse_attn_bwd_workspace(ctypes.byref(dims)))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    _check(lib.dsv_sparse_attn_bwd(ctypes.byref(dims), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                   _ptr(idx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                                   _stream_ptr(q)), "dsv_sparse_attn_bwd")
+    return dq, dk, dv
+
+
+def dsv_last_device_status(device: Optional[torch.device] = None) -> int:
+    stream = torch.cuda.current_stream(device).cuda_stream
+    return int(load_library().dsv_last_device_status(stream))

@@ -1,0 +1,129 @@
+/*
+ * dsv.h -- C ABI of libdsv.so: DSV's dynamic sparse 3D attention on one GB300 (sm_103a).
+ *
+ * Source of the method: "DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale
+ * Video DiT Training" (German and Spanish technical summaries).  Per attention head
+ * a low-rank pair (Q_lr, K_lr) estimates Q K^T (section 2A); one fused kernel forms
+ * that estimate and selects the top-k keys without materialising the N x N scores
+ * (section 2B, "Fused MM & Top-K"), once per group of 3D-neighbouring queries
+ * (section 2B, "Query Grouping"); softmax attention forward and backward then run
+ * over the selected keys only (Spanish summary section 3, custom fused kernels for
+ * estimation and sparse attention; training needs the backward).
+ *
+ * Conventions shared by every call
+ *   - Layout: contiguous [B][H][N][d] (bf16) for Q, K, V, dO, O, dQ, dK, dV;
+ *     [B][H][N][r] (bf16) for Q_lr, K_lr; [B][H][N] fp32 for LSE;
+ *     [B][H][N/block][k] int32 for idx.  Tokens are in block-major order: query
+ *     block b of a head is rows [block*b, block*b + block).  The caller permutes
+ *     tokens (3D cubes of neighbours) before the call; the kernels do not care how.
+ *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned.  The
+ *     library allocates nothing and frees nothing; it keeps no state between calls
+ *     except the device status word read by dsv_last_device_status().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls enqueue work and return at once; none synchronises except
+ *     dsv_last_device_status().
+ *   - Arguments are validated on the host before anything is launched; an invalid
+ *     call returns an error code, launches nothing and writes nothing.
+ *     dsv_last_error_message() then holds a one-line reason (per host thread).
+ *   - Identical inputs give bitwise-identical outputs (no floating-point atomics).
+ */
+#ifndef DSV_H
+#define DSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSV_OK = 0,
+    DSV_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer */
+    DSV_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. d not in {64,128}) */
+    DSV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    DSV_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, attribute) */
+    DSV_ERR_DEVICE_CHECK = 5   /* a kernel found an out-of-range key index */
+} dsv_status;
+
+/* Problem sizes.  block must be 64; N % block == 0; 1 <= k <= N;
+ * d in {64, 128}; r in {16, 32, 48, 64} (only the estimate reads r);
+ * scale <= 0 selects 1/sqrt(d) (the usual softmax scale; the pages give none). */
+typedef struct {
+    int64_t B, H, N;
+    int64_t d, r;
+    int64_t block;
+    int64_t k;
+    float scale;
+} dsv_dims;
+
+/* Bytes of device workspace dsv_estimate_topk needs (0: it needs none). */
+size_t dsv_estimate_topk_workspace(const dsv_dims* dims);
+
+/*
+ * Low-rank estimate + top-k per query block (DSV section 2A/2B: fused MM & top-k
+ * with query grouping).
+ *   q_hat[b]  = sum of Q_lr over the `block` tokens of query block b;
+ *   s[b, j]   = q_hat[b] . K_lr[j]   for every key j of the same head (never stored);
+ *   idx[b, :] = the k keys of largest s[b, j], ties to the lower j, ascending order.
+ * q_lr, k_lr: bf16 [B][H][N][r].  idx: int32 [B][H][N/block][k] (output).
+ * Scores are formed in fp32 from q_hat held as an exact two-term bf16 sum; with
+ * integer-valued factors (|q_hat| < 2^16, |s| < 2^24) every score is exact, so the
+ * selection equals the exact-arithmetic one.  ws may be NULL when the workspace
+ * size is 0.
+ */
+dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void* k_lr,
+                             int32_t* idx, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Sparse attention forward over the selected keys (DSV Spanish summary section 3:
+ * sparse attention kernels; page 1 section 2A: only the critical KV pairs are used).
+ * For query i of block b:  l_ij = scale * Q_i . K_j for j in idx[b];
+ *   LSE_i = max_j l_ij + ln sum_j exp(l_ij - max_j l_ij);  O_i = sum_j exp(l_ij - LSE_i) V_j.
+ * q, k, v: bf16 [B][H][N][d].  idx: int32 [B][H][N/block][k], entries in [0, N)
+ * (need not be sorted here).  o: bf16 [B][H][N][d] (output).  lse: fp32 [B][H][N]
+ * (output, natural log).  Accumulation in fp32.
+ */
+dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v,
+                               const int32_t* idx, void* o, float* lse, void* stream);
+
+/* Recommended / minimum device workspace for dsv_sparse_attn_bwd.  With more
+ * workspace the backward processes more query blocks per wave (fewer launches). */
+size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims);
+size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims);
+
+/*
+ * Sparse attention backward (needed for training, DSV page 1 section 2A stage 2).
+ * Recomputes P_ij = exp(scale Q_i.K_j - LSE_i) from the stored LSE, then
+ *   D_i = dO_i . O_i;  dS_ij = P_ij (dO_i . V_j - D_i);
+ *   dQ_i = scale sum_j dS_ij K_j;
+ *   dK_j = scale sum_{i: j in idx[block(i)]} dS_ij Q_i;  dV_j = sum_{same i} P_ij dO_i.
+ * Keys no block selected get dK = dV = 0.  No gradient flows to Q_lr / K_lr.
+ * idx rows MUST be strictly ascending (as dsv_estimate_topk writes them).
+ * dK/dV are reduced per key in ascending query-block order from per-(block, key)
+ * partial rows held in the workspace: deterministic, no float atomics.
+ * d_o, q, k, v, o: bf16 [B][H][N][d]; lse fp32 [B][H][N]; idx int32 [B][H][N/block][k];
+ * dq, dk, dv: bf16 [B][H][N][d] (outputs).  ws: device workspace of ws_bytes >=
+ * dsv_sparse_attn_bwd_workspace_min(dims), 256-byte aligned.
+ */
+dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void* q, const void* k,
+                               const void* v, const void* o, const float* lse, const int32_t* idx,
+                               void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* dsv_status_string(dsv_status status);
+
+/* One-line reason for the last non-OK status returned on this host thread. */
+const char* dsv_last_error_message(void);
+
+/* Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns DSV_ERR_DEVICE_CHECK if a kernel met a key index outside [0, N) since the
+ * last read (the offending entry is skipped, never dereferenced), DSV_ERR_CUDA if
+ * the synchronisation failed, DSV_OK otherwise. */
+dsv_status dsv_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSV_H */

@@ -1,0 +1,26 @@
+"""CPU oracle for DSV's dynamic sparse attention -- TEST INFRASTRUCTURE, not product code.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU-baseline leg and
+its ``--impl reference`` arm) may import, call or execute anything here.  The product
+path (the CUDA library and its Python binding) never does, and this package never
+imports the product.
+
+Pins (what ties each function to something other than itself) live in ``tests/``:
+  estimate / top-k : brute force over all subsets on tiny inputs, a hand-worked
+                     fixture in tests/golden/, linearity of the block estimate;
+  forward          : torch fp64 scaled_dot_product_attention at density 100 % and
+                     with a -inf mask outside the selected set;
+  backward         : torch fp64 autograd of the masked dense form, central finite
+                     differences, closed forms (sum dV = sum dO, sum dK = 0,
+                     unselected keys get zero gradient).
+"""
+from .dsv_oracle import (  # noqa: F401
+    block_representatives,
+    block_scores,
+    default_scale,
+    estimate_topk,
+    run_heads,
+    sparse_attn_bwd,
+    sparse_attn_fwd,
+    topk_select,
+)

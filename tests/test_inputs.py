@@ -1,0 +1,68 @@
+"""Host-side input generation: token layout and seeded draws (CPU only)."""
+import numpy as np
+import torch
+
+from dynamic_sparse_attention_estimate_gb300.inputs import (
+    BLOCK, WORKLOADS, block_major_permutation, make_head, make_inputs, sample_blocks)
+
+
+def _coords(latent, raster_idx):
+    T, Hh, W = latent
+    return np.stack([raster_idx // (Hh * W), (raster_idx // W) % Hh, raster_idx % W], axis=1)
+
+
+def test_every_permutation_is_a_bijection():
+    for wl in WORKLOADS.values():
+        perm = block_major_permutation(wl.latent, wl.block_shape)
+        assert perm.size == wl.N
+        assert np.array_equal(np.sort(perm), np.arange(wl.N))
+
+
+def test_cube_blocks_are_4x4x4_neighbourhoods():
+    wl = WORKLOADS["short"]
+    perm = block_major_permutation(wl.latent, wl.block_shape)
+    c = _coords(wl.latent, perm).reshape(wl.NB, BLOCK, 3)
+    extent = c.max(axis=1) - c.min(axis=1)
+    assert np.all(extent == 3)
+
+
+def test_long_workload_tail_frames_use_1x8x8_tiles():
+    wl = WORKLOADS["long"]
+    perm = block_major_permutation(wl.latent, wl.block_shape)
+    c = _coords(wl.latent, perm).reshape(wl.NB, BLOCK, 3)
+    extent = c.max(axis=1) - c.min(axis=1)
+    n_cube_blocks = (124 // 4) * (64 // 4) * (64 // 4)
+    assert np.all(extent[:n_cube_blocks] == 3)
+    assert np.all(extent[n_cube_blocks:] == np.array([0, 7, 7]))
+    assert wl.NB == 8128
+
+
+def test_tiny_uses_consecutive_raster_blocks():
+    wl = WORKLOADS["tiny"]
+    assert np.array_equal(block_major_permutation(wl.latent, wl.block_shape), np.arange(wl.N))
+
+
+def test_draws_are_seeded_shaped_and_integer_factors_in_range():
+    wl = WORKLOADS["tiny"]
+    a = make_inputs(wl)
+    b = make_inputs(wl)
+    for key in a:
+        assert torch.equal(a[key], b[key])
+        assert a[key].dtype == torch.bfloat16
+    assert a["q"].shape == (1, 2, 1024, 64) and a["q_lr"].shape == (1, 2, 1024, 16)
+    lr = a["q_lr"].float()
+    assert torch.equal(lr, lr.round()) and lr.abs().max() <= 4
+    # heads are independent streams: generating head 1 alone gives the same slice
+    alone = make_head(wl, 0, 1)
+    assert torch.equal(alone["k"], a["k"][0, 1])
+
+
+def test_k_from_density_is_floor():
+    wl = WORKLOADS["sweep"]
+    assert [wl.with_density(x).k for x in (0.05, 0.10, 0.20, 1.0)] == [6553, 13107, 26214, 131072]
+    assert WORKLOADS["short"].k == 1638 and WORKLOADS["long"].k == 52019
+
+
+def test_sample_blocks_sorted_distinct():
+    s = sample_blocks(8128, 64)
+    assert s.size == 64 and np.all(np.diff(s) > 0) and s.max() < 8128
