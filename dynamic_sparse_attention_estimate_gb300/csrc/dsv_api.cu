@@ -1,0 +1,319 @@
+// C ABI of libdsv.so (declared in include/dsv.h): host-side validation, workspace
+// planning and launches.  Nothing here allocates device memory.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/dsv.h"
+#include "dsv_internal.h"
+
+// Device status word: kernels OR in kStatusBadIndex when they meet a key index outside
+// [0, N) or a repeated key in one idx row.  Read and cleared by dsv_last_device_status.
+__device__ unsigned int g_dsv_status;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+dsv_status fail(dsv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+dsv_status ok() {
+  g_msg[0] = '\0';
+  return DSV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
+
+dsv_status status_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSV_ERR_CUDA, "device ordinal %d out of range", dev);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dsv_status);
+    if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return DSV_OK;
+}
+
+dsv_status check_dims(const dsv_dims* d, bool need_d, bool need_r) {
+  if (!d) return fail(DSV_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->H < 1 || d->N < 1) return fail(DSV_ERR_INVALID_ARG, "B, H, N must be >= 1");
+  if (d->block != 64) return fail(DSV_ERR_UNSUPPORTED, "block must be 64 (got %lld)", (long long)d->block);
+  if (d->N % d->block) return fail(DSV_ERR_INVALID_ARG, "N (%lld) must be a multiple of block", (long long)d->N);
+  if (d->N > 0x7fffffffLL) return fail(DSV_ERR_INVALID_ARG, "N must fit int32 key indices");
+  if (d->k < 1 || d->k > d->N) return fail(DSV_ERR_INVALID_ARG, "need 1 <= k <= N (k=%lld)", (long long)d->k);
+  if (d->B * d->H > (1LL << 31) - 1) return fail(DSV_ERR_INVALID_ARG, "B*H too large");
+  if (need_d && d->d != 64 && d->d != 128)
+    return fail(DSV_ERR_UNSUPPORTED, "head dim d must be 64 or 128 (got %lld)", (long long)d->d);
+  if (need_r && (d->r < 16 || d->r > 64 || d->r % 16))
+    return fail(DSV_ERR_UNSUPPORTED, "low-rank dim r must be 16, 32, 48 or 64 (got %lld)", (long long)d->r);
+  if (!(d->scale == d->scale)) return fail(DSV_ERR_INVALID_ARG, "scale is NaN");
+  return DSV_OK;
+}
+
+#define DSV_NEED_PTR(p)                                                                \
+  do {                                                                                 \
+    if (!(p)) return fail(DSV_ERR_INVALID_ARG, "%s is NULL", #p);                     \
+    if (!aligned16(p)) return fail(DSV_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+float eff_scale(const dsv_dims* d) { return d->scale > 0.f ? d->scale : 1.0f / sqrtf(static_cast<float>(d->d)); }
+
+// ---------------------------------------------------------------- backward workspace planning
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WavePlan {
+  int64_t nh = 0, nblk = 0;  // heads per wave (whole-head waves) or blocks per wave (sub-head)
+  bool sub = false;
+};
+
+struct Carve {
+  size_t colbits, colpre, count, offsets, partial, acc, total;
+};
+
+Carve carve(const dsv_dims* d, int64_t nh, int64_t nblk, bool sub) {
+  const int64_t W32 = (nblk + 31) / 32;
+  Carve c;
+  size_t o = 0;
+  c.colbits = o; o += up(sizeof(uint32_t) * nh * W32 * d->N);
+  c.colpre = o;  o += up(sizeof(uint32_t) * nh * W32 * d->N);
+  c.count = o;   o += up(sizeof(uint32_t) * nh * d->N);
+  c.offsets = o; o += up(sizeof(int64_t) * nh * d->N);
+  c.partial = o; o += up(sizeof(float) * 2 * d->d * nh * nblk * d->k);
+  c.acc = o;     o += sub ? up(sizeof(float) * 2 * d->d * d->N) : 0;
+  c.total = o;
+  return c;
+}
+
+size_t plan_bytes(const dsv_dims* d, const WavePlan& w) { return carve(d, w.nh, w.nblk, w.sub).total; }
+
+// Largest plan that fits `budget` bytes (whole heads first, then blocks of one head).
+bool plan_for(const dsv_dims* d, size_t budget, WavePlan* out) {
+  const int64_t BH = d->B * d->H, NB = d->N / 64;
+  for (int64_t nh = BH; nh >= 1; nh = (nh == 1 ? 0 : (nh + 1) / 2)) {
+    WavePlan w{nh, NB, false};
+    if (plan_bytes(d, w) <= budget) {
+      // grow back towards BH while it still fits (the halving may undershoot)
+      while (w.nh < BH) {
+        WavePlan w2{w.nh + 1, NB, false};
+        if (plan_bytes(d, w2) > budget) break;
+        w = w2;
+      }
+      *out = w;
+      return true;
+    }
+    if (nh == 1) break;
+  }
+  for (int64_t s = 2; s <= NB; s = (s < 64 ? s + 1 : s + s / 8)) {
+    const int64_t nblk = (NB + s - 1) / s;
+    WavePlan w{1, nblk, true};
+    if (plan_bytes(d, w) <= budget) { *out = w; return true; }
+  }
+  WavePlan w{1, 1, NB > 1};
+  if (plan_bytes(d, w) <= budget) { *out = w; return true; }
+  return false;
+}
+
+constexpr size_t kRecommendedPartialBytes = size_t(16) << 30;
+
+}  // namespace
+
+extern "C" {
+
+const char* dsv_status_string(dsv_status s) {
+  switch (s) {
+    case DSV_OK: return "DSV_OK";
+    case DSV_ERR_INVALID_ARG: return "DSV_ERR_INVALID_ARG";
+    case DSV_ERR_UNSUPPORTED: return "DSV_ERR_UNSUPPORTED";
+    case DSV_ERR_WORKSPACE: return "DSV_ERR_WORKSPACE";
+    case DSV_ERR_CUDA: return "DSV_ERR_CUDA";
+    case DSV_ERR_DEVICE_CHECK: return "DSV_ERR_DEVICE_CHECK";
+  }
+  return "DSV_ERR_UNKNOWN";
+}
+
+const char* dsv_last_error_message(void) { return g_msg; }
+
+size_t dsv_estimate_topk_workspace(const dsv_dims* dims) {
+  (void)dims;
+  return 0;
+}
+
+dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void* k_lr, int32_t* idx, void* ws,
+                             size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  dsv_status s = check_dims(dims, false, true);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(q_lr);
+  DSV_NEED_PTR(k_lr);
+  DSV_NEED_PTR(idx);
+  unsigned int* status = nullptr;
+  if ((s = status_word(&status)) != DSV_OK) return s;
+  dsv::EstimateParams p;
+  p.q_lr = static_cast<const dsv::bf16*>(q_lr);
+  p.k_lr = static_cast<const dsv::bf16*>(k_lr);
+  p.idx = idx;
+  p.BH = dims->B * dims->H;
+  p.N = dims->N;
+  p.NB = dims->N / dims->block;
+  p.topk = dims->k;
+  p.r = static_cast<int>(dims->r);
+  p.status = status;
+  cudaError_t e = dsv::launch_estimate_topk(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "estimate launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
+                               void* o, float* lse, void* stream) {
+  dsv_status s = check_dims(dims, true, false);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(q);
+  DSV_NEED_PTR(k);
+  DSV_NEED_PTR(v);
+  DSV_NEED_PTR(idx);
+  DSV_NEED_PTR(o);
+  DSV_NEED_PTR(lse);
+  unsigned int* status = nullptr;
+  if ((s = status_word(&status)) != DSV_OK) return s;
+  dsv::FwdParams p;
+  p.q = static_cast<const dsv::bf16*>(q);
+  p.k = static_cast<const dsv::bf16*>(k);
+  p.v = static_cast<const dsv::bf16*>(v);
+  p.idx = idx;
+  p.o = static_cast<dsv::bf16*>(o);
+  p.lse = lse;
+  p.BH = dims->B * dims->H;
+  p.N = dims->N;
+  p.NB = dims->N / dims->block;
+  p.topk = dims->k;
+  p.d = static_cast<int>(dims->d);
+  p.scale = eff_scale(dims);
+  p.status = status;
+  cudaError_t e = dsv::launch_sparse_fwd(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims) {
+  if (check_dims(dims, true, false) != DSV_OK) return 0;
+  WavePlan w{1, 1, dims->N / 64 > 1};
+  return plan_bytes(dims, w);
+}
+
+size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims) {
+  if (check_dims(dims, true, false) != DSV_OK) return 0;
+  // the largest plan whose partial rows stay within the recommended budget
+  const size_t per_block = sizeof(float) * 2 * dims->d * dims->k;
+  const int64_t BH = dims->B * dims->H, NB = dims->N / 64;
+  const int64_t blocks = static_cast<int64_t>(kRecommendedPartialBytes / (per_block ? per_block : 1));
+  WavePlan w;
+  if (blocks >= BH * NB) w = WavePlan{BH, NB, false};
+  else if (blocks >= NB) w = WavePlan{blocks / NB, NB, false};
+  else {
+    const int64_t nblk = blocks < 1 ? 1 : blocks;
+    const int64_t s = (NB + nblk - 1) / nblk;
+    w = WavePlan{1, (NB + s - 1) / s, true};
+  }
+  return plan_bytes(dims, w);
+}
+
+dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
+                               const void* o, const float* lse, const int32_t* idx, void* dq, void* dk, void* dv,
+                               void* ws, size_t ws_bytes, void* stream) {
+  dsv_status s = check_dims(dims, true, false);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(d_o);
+  DSV_NEED_PTR(q);
+  DSV_NEED_PTR(k);
+  DSV_NEED_PTR(v);
+  DSV_NEED_PTR(o);
+  DSV_NEED_PTR(lse);
+  DSV_NEED_PTR(idx);
+  DSV_NEED_PTR(dq);
+  DSV_NEED_PTR(dk);
+  DSV_NEED_PTR(dv);
+  if (!ws) return fail(DSV_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  WavePlan plan;
+  if (!plan_for(dims, ws_bytes, &plan))
+    return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the minimum %zu", ws_bytes,
+                dsv_sparse_attn_bwd_workspace_min(dims));
+  unsigned int* status = nullptr;
+  if ((s = status_word(&status)) != DSV_OK) return s;
+
+  const Carve c = carve(dims, plan.nh, plan.nblk, plan.sub);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  dsv::BwdParams p;
+  p.d_o = static_cast<const dsv::bf16*>(d_o);
+  p.q = static_cast<const dsv::bf16*>(q);
+  p.k = static_cast<const dsv::bf16*>(k);
+  p.v = static_cast<const dsv::bf16*>(v);
+  p.o = static_cast<const dsv::bf16*>(o);
+  p.lse = lse;
+  p.idx = idx;
+  p.dq = static_cast<dsv::bf16*>(dq);
+  p.dk = static_cast<dsv::bf16*>(dk);
+  p.dv = static_cast<dsv::bf16*>(dv);
+  p.BH = dims->B * dims->H;
+  p.N = dims->N;
+  p.NB = dims->N / dims->block;
+  p.topk = dims->k;
+  p.d = static_cast<int>(dims->d);
+  p.scale = eff_scale(dims);
+  p.status = status;
+  p.colbits = reinterpret_cast<uint32_t*>(base + c.colbits);
+  p.colpre = reinterpret_cast<uint32_t*>(base + c.colpre);
+  p.count = reinterpret_cast<uint32_t*>(base + c.count);
+  p.offsets = reinterpret_cast<int64_t*>(base + c.offsets);
+  p.partial = reinterpret_cast<float*>(base + c.partial);
+  p.acc = plan.sub ? reinterpret_cast<float*>(base + c.acc) : nullptr;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!plan.sub) {
+    for (int64_t bh0 = 0; bh0 < p.BH; bh0 += plan.nh) {
+      dsv::BwdWave w{bh0, plan.nh < p.BH - bh0 ? plan.nh : p.BH - bh0, 0, p.NB, true, true};
+      cudaError_t e = dsv::launch_bwd_wave(p, w, st);
+      if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+    }
+  } else {
+    for (int64_t bh = 0; bh < p.BH; ++bh) {
+      for (int64_t b0 = 0; b0 < p.NB; b0 += plan.nblk) {
+        const int64_t n = plan.nblk < p.NB - b0 ? plan.nblk : p.NB - b0;
+        dsv::BwdWave w{bh, 1, b0, n, b0 == 0, b0 + n == p.NB};
+        cudaError_t e = dsv::launch_bwd_wave(p, w, st);
+        if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+      }
+    }
+  }
+  return ok();
+}
+
+dsv_status dsv_last_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  unsigned int v = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&v, g_dsv_status, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_dsv_status, &zero, sizeof(zero));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+  if (v) return fail(DSV_ERR_DEVICE_CHECK, "a kernel met an out-of-range or repeated key index (status 0x%x)", v);
+  return ok();
+}
+
+}  // extern "C"

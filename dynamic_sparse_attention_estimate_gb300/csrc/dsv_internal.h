@@ -1,0 +1,61 @@
+// Host-side launch interface between the C ABI (dsv_api.cu) and the kernel files.
+// Everything here is validated by the caller before a launch happens.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsv {
+
+using bf16 = __nv_bfloat16;
+
+struct EstimateParams {
+  const bf16* q_lr;   // [BH][N][r]
+  const bf16* k_lr;   // [BH][N][r]
+  int32_t* idx;       // [BH][NB][k]
+  int64_t BH, N, NB, topk;
+  int r;
+  unsigned int* status;
+};
+cudaError_t launch_estimate_topk(const EstimateParams& p, cudaStream_t stream);
+
+struct FwdParams {
+  const bf16 *q, *k, *v;  // [BH][N][d]
+  const int32_t* idx;     // [BH][NB][k]
+  bf16* o;                // [BH][N][d]
+  float* lse;             // [BH][N]
+  int64_t BH, N, NB, topk;
+  int d;
+  float scale;
+  unsigned int* status;
+};
+cudaError_t launch_sparse_fwd(const FwdParams& p, cudaStream_t stream);
+
+// One wave of the backward: either whole heads [bh0, bh0 + nh) (blk0 = 0, nblk = NB)
+// or the query blocks [blk0, blk0 + nblk) of the single head bh0 (nh = 1).
+struct BwdWave {
+  int64_t bh0, nh, blk0, nblk;
+  bool first_of_head, last_of_head;  // for sub-head waves
+};
+
+struct BwdParams {
+  const bf16 *d_o, *q, *k, *v, *o;
+  const float* lse;
+  const int32_t* idx;
+  bf16 *dq, *dk, *dv;
+  int64_t BH, N, NB, topk;
+  int d;
+  float scale;
+  unsigned int* status;
+  // workspace carve-out for one wave (sized for the largest wave)
+  uint32_t* colbits;   // [nh][W32][N]   bit lb of word (lb / 32): block lb selected key j
+  uint32_t* colpre;    // [nh][W32][N]   popcount of the words before
+  uint32_t* count;     // [nh][N]
+  int64_t* offsets;    // [nh][N]        first partial row of key j (absolute within the wave)
+  float* partial;      // [pairs][2 d]   dK part, then dV part
+  float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
+};
+cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream);
+
+}  // namespace dsv

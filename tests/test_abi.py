@@ -1,0 +1,85 @@
+"""C-ABI library: builds, loads, exports every symbol include/dsv.h declares, and rejects
+invalid calls on the host before launching anything (CPU only: no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dynamic_sparse_attention_estimate_gb300 as pkg
+from dynamic_sparse_attention_estimate_gb300.binding import EXPORTED, make_dims
+
+REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(REPO, "include", "dsv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dynamic_sparse_attention_estimate_gb300.build import build
+    build()
+    return pkg.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.dsv_status_string(0) == b"DSV_OK"
+    assert lib.dsv_status_string(5) == b"DSV_ERR_DEVICE_CHECK"
+
+
+def _call_fwd(lib, dims, ptr=0x1000):
+    p = ctypes.c_void_p(ptr)
+    return lib.dsv_sparse_attn_fwd(ctypes.byref(dims), p, p, p, p, p, p, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("block", 32, 2), ("N", 1000, 1), ("k", 0, 1), ("k", 1025, 1), ("d", 96, 2), ("B", 0, 1),
+])
+def test_invalid_dims_rejected_before_launch(lib, field, value, status):
+    dims = make_dims(1, 2, 1024, 64, 16, 128)
+    setattr(dims, field, value)
+    assert _call_fwd(lib, dims) == status
+    assert lib.dsv_last_error_message()
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    dims = make_dims(1, 2, 1024, 64, 16, 128)
+    assert lib.dsv_sparse_attn_fwd(ctypes.byref(dims), None, None, None, None, None, None, None) == 1
+    assert b"NULL" in lib.dsv_last_error_message()
+    assert _call_fwd(lib, dims, 0x1004) == 1
+    assert b"aligned" in lib.dsv_last_error_message()
+    p = ctypes.c_void_p(0x1000)
+    bad_r = make_dims(1, 2, 1024, 64, 24, 128)
+    assert lib.dsv_estimate_topk(ctypes.byref(bad_r), p, p, p, None, 0, None) == 2
+
+
+def test_backward_workspace_checks(lib):
+    dims = make_dims(1, 12, 16384, 64, 16, 1638)
+    rec = lib.dsv_sparse_attn_bwd_workspace(ctypes.byref(dims))
+    mn = lib.dsv_sparse_attn_bwd_workspace_min(ctypes.byref(dims))
+    assert 0 < mn < rec
+    # partial rows: 12 heads x 256 blocks x 1638 keys x 2 x 64 fp32
+    assert rec >= 12 * 256 * 1638 * 2 * 64 * 4
+    p = ctypes.c_void_p(0x1000)
+    args = [ctypes.byref(dims)] + [p] * 10
+    assert lib.dsv_sparse_attn_bwd(*args, None, 0, None) == 3            # no workspace
+    assert lib.dsv_sparse_attn_bwd(*args, ctypes.c_void_p(0x1000), mn - 256, None) == 3   # too small
+    assert lib.dsv_sparse_attn_bwd(*args, ctypes.c_void_p(0x1010), rec, None) == 3        # misaligned
+
+
+def test_estimate_needs_no_workspace(lib):
+    dims = make_dims(1, 2, 1024, 64, 16, 128)
+    assert lib.dsv_estimate_topk_workspace(ctypes.byref(dims)) == 0

@@ -1,0 +1,195 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Selection must be bit-exact; O, dQ, dK, dV (bf16) within max-abs 2e-2 and rel-L2 1e-2
+of the oracle; LSE within 1e-2.  Small workloads are compared element by element;
+the short-clip workload (the one the benchmark times) is compared on every head for
+the selection, on whole heads for the forward, on sampled blocks for the backward
+(dO zeroed outside them), and through closed-form invariants on every head.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dynamic_sparse_attention_estimate_gb300 import dsv_estimate_topk, dsv_sparse_attn_bwd, dsv_sparse_attn_fwd
+from dynamic_sparse_attention_estimate_gb300.binding import dsv_last_device_status, dsv_sparse_attn_bwd_workspace, \
+    make_dims
+from dynamic_sparse_attention_estimate_gb300.inputs import WORKLOADS, Workload, make_inputs, sample_blocks
+
+from gpu_helpers import EDGE_REL_ELEM, LSE_MAX_ABS, assert_close, check_idx_invariants, need_gpu, np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _to(dev, x):
+    return {k: v.to(dev) for k, v in x.items()}
+
+
+def _run(g, k, workspace=None):
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], k)
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+    dq, dk, dv = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=workspace)
+    torch.cuda.synchronize()
+    assert dsv_last_device_status() == 0
+    return idx, o, lse, dq, dk, dv
+
+
+def _full_check(x, out, k, heads=None, rel_elem=0.0):
+    idx, o, lse, dq, dk, dv = out
+    B, H = x["q"].shape[:2]
+    for h in (range(H) if heads is None else heads):
+        c = {key: val[0, h] for key, val in x.items()}
+        want = oracle.estimate_topk(c["q_lr"], c["k_lr"], 64, k)
+        got = idx[0, h].cpu().numpy()
+        assert np.array_equal(got, want), f"head {h}: selection differs in {(got != want).any(axis=1).sum()} blocks"
+        ro, rl = oracle.sparse_attn_fwd(c["q"], c["k"], c["v"], want, 64)
+        rdq, rdk, rdv = oracle.sparse_attn_bwd(c["do"], c["q"], c["k"], c["v"], want, 64, o=ro, lse=rl)
+        assert_close(f"O[h{h}]", o[0, h], ro, rel_elem=rel_elem)
+        assert_close(f"LSE[h{h}]", lse[0, h], rl, max_abs=LSE_MAX_ABS)
+        assert_close(f"dQ[h{h}]", dq[0, h], rdq, rel_elem=rel_elem)
+        assert_close(f"dK[h{h}]", dk[0, h], rdk, rel_elem=rel_elem)
+        assert_close(f"dV[h{h}]", dv[0, h], rdv, rel_elem=rel_elem)
+
+
+def test_tiny_workload_full():
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"]
+    x = make_inputs(wl)
+    out = _run(_to(dev, x), wl.k)
+    _full_check(x, out, wl.k)
+
+
+def test_ragged_d128_r32_nb_not_multiple_of_16():
+    """N = 1280 (20 blocks), d = 128, r = 32, k = 100 (a ragged last chunk), factors in [-8, 8]."""
+    dev = need_gpu()
+    wl = Workload("ragged", 1, 2, (5, 16, 16), 128, 32, 100, None, lr_max=8)
+    x = make_inputs(wl)
+    out = _run(_to(dev, x), wl.k)
+    _full_check(x, out, wl.k)
+
+
+@pytest.mark.parametrize("k", [1, 63, 65, 1024])
+def test_edge_k_values(k):
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(1)
+    x = make_inputs(wl)
+    out = _run(_to(dev, x), k)
+    _full_check(x, out, k, rel_elem=EDGE_REL_ELEM)
+    if k == wl.N:
+        assert torch.equal(out[0][0, 0].cpu(), torch.arange(wl.N, dtype=torch.int32).expand(wl.NB, wl.N))
+
+
+def test_full_density_equals_dense_attention():
+    """k = N: the sparse path is dense bidirectional attention (checked against SDPA too)."""
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(2)
+    x = make_inputs(wl)
+    g = _to(dev, x)
+    idx, o, lse, dq, dk, dv = _run(g, wl.N)
+    ref = torch.nn.functional.scaled_dot_product_attention(g["q"].float(), g["k"].float(), g["v"].float())
+    assert_close("O vs SDPA", o, np64(ref))
+
+
+def test_ties_go_to_the_lower_key_index():
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(2)
+    x = make_inputs(wl)
+    x["k_lr"][0, 0].zero_()                      # every score 0: first k keys
+    x["k_lr"][0, 1] = x["k_lr"][0, 1].clamp(-1, 1)  # few distinct scores: many ties
+    out = _run(_to(dev, x), 200)
+    assert torch.equal(out[0][0, 0].cpu(), torch.arange(200, dtype=torch.int32).expand(wl.NB, 200))
+    _full_check(x, out, 200)
+
+
+def test_short_clip_selection_every_head_bit_exact():
+    dev = need_gpu()
+    wl = WORKLOADS["short"]
+    x = make_inputs(wl)
+    g = _to(dev, x)
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    torch.cuda.synchronize()
+    check_idx_invariants(idx, wl.N)
+    for h in range(wl.H):
+        want = oracle.estimate_topk(x["q_lr"][0, h], x["k_lr"][0, h], 64, wl.k)
+        assert np.array_equal(idx[0, h].cpu().numpy(), want), f"head {h}"
+
+
+def test_short_clip_attention():
+    dev = need_gpu()
+    wl = WORKLOADS["short"]
+    x = make_inputs(wl)
+    g = _to(dev, x)
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+    dq, dk, dv = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx)
+    torch.cuda.synchronize()
+    assert dsv_last_device_status() == 0
+    idx_np = idx.cpu().numpy()
+    # forward on two whole heads
+    for h in (0, wl.H - 1):
+        ro, rl = oracle.sparse_attn_fwd(x["q"][0, h], x["k"][0, h], x["v"][0, h], idx_np[0, h], 64)
+        assert_close(f"O[h{h}]", o[0, h], ro)
+        assert_close(f"LSE[h{h}]", lse[0, h], rl, max_abs=LSE_MAX_ABS)
+    # closed forms on every head of the unmasked backward
+    for h in range(wl.H):
+        sdo = np64(g["do"][0, h]).sum(0)
+        assert_close(f"sum dV[h{h}] = sum dO", np64(dv[0, h]).sum(0), sdo, max_abs=0.5, rel_l2=1e-2)
+        sel = np.zeros(wl.N, bool)
+        sel[np.unique(idx_np[0, h])] = True
+        assert not np64(dk[0, h])[~sel].any() and not np64(dv[0, h])[~sel].any()
+        assert np.abs(np64(dk[0, h]).sum(0)).max() < 0.5
+    # backward on sampled blocks: dO zeroed outside them, every head
+    blocks = sample_blocks(wl.NB, 16)
+    mask = torch.zeros(wl.N, dtype=torch.bool)
+    for b in blocks:
+        mask[b * 64:(b + 1) * 64] = True
+    do_m = g["do"] * mask.to(dev)[None, None, :, None]
+    dq2, dk2, dv2 = dsv_sparse_attn_bwd(do_m, g["q"], g["k"], g["v"], o, lse, idx)
+    torch.cuda.synchronize()
+    rows = mask.numpy()
+    for h in range(wl.H):
+        c = {key: val[0, h] for key, val in x.items()}
+        rdq, rdk, rdv = oracle.sparse_attn_bwd(c["do"], c["q"], c["k"], c["v"], idx_np[0, h], 64, blocks=blocks)
+        assert_close(f"dQ[h{h}] sampled", np64(dq2[0, h])[rows], rdq[rows])
+        assert_close(f"dK[h{h}] sampled", dk2[0, h], rdk)
+        assert_close(f"dV[h{h}] sampled", dv2[0, h], rdv)
+
+
+def test_backward_is_deterministic_and_wave_independent():
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(2)
+    x = make_inputs(wl)
+    g = _to(dev, x)
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+    ref = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx)
+    again = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx)
+    dims = make_dims(1, 2, wl.N, wl.d, wl.r, wl.k)
+    small = dsv_sparse_attn_bwd_workspace(dims, minimum=True)
+    for nbytes in (small, small * 3, small * 12):   # sub-head waves of one or a few blocks
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        other = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws)
+        for a, b in zip(ref, other):
+            assert torch.equal(a, b)
+    for a, b in zip(ref, again):
+        assert torch.equal(a, b)
+    assert dsv_last_device_status() == 0
+
+
+def test_out_of_range_and_repeated_indices_set_the_device_status():
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(1)
+    g = _to(dev, make_inputs(wl))
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    torch.cuda.synchronize()
+    assert dsv_last_device_status() == 0
+    bad = idx.clone()
+    bad[0, 0, 3, 5] = wl.N + 7          # out of range: skipped, flagged
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], bad)
+    assert dsv_last_device_status() == 5
+    assert dsv_last_device_status() == 0  # read clears it
+    dup = idx.clone()
+    dup[0, 0, 2, 1] = dup[0, 0, 2, 0]    # repeated key in one row
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+    dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, dup)
+    assert dsv_last_device_status() == 5
