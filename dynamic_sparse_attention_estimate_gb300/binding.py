@@ -25,6 +25,7 @@ EXPORTED = (
     "dsv_estimate_topk_workspace", "dsv_estimate_topk", "dsv_sparse_attn_fwd",
     "dsv_sparse_attn_bwd_workspace", "dsv_sparse_attn_bwd_workspace_min", "dsv_sparse_attn_bwd",
     "dsv_status_string", "dsv_last_error_message", "dsv_last_device_status",
+    "dsv_profile_enable", "dsv_profile_read",
 )
 
 
@@ -73,6 +74,10 @@ def load_library(path: Optional[str] = None):
     lib.dsv_last_error_message.restype = ctypes.c_char_p
     lib.dsv_last_device_status.argtypes = [vp]
     lib.dsv_last_device_status.restype = st
+    lib.dsv_profile_enable.argtypes = [st]
+    lib.dsv_profile_enable.restype = st
+    lib.dsv_profile_read.argtypes = [ctypes.c_char_p, sz]
+    lib.dsv_profile_read.restype = sz
     if path is None:
         _lib = lib
     return lib
@@ -185,3 +190,20 @@ def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: t
 def dsv_last_device_status(device: Optional[torch.device] = None) -> int:
     stream = torch.cuda.current_stream(device).cuda_stream
     return int(load_library().dsv_last_device_status(stream))
+
+
+def dsv_profile_enable(on: bool = True) -> None:
+    _check(load_library().dsv_profile_enable(1 if on else 0), "dsv_profile_enable")
+
+
+def dsv_profile_read() -> dict:
+    """{kernel name: (launches, total device ms)} since the previous read."""
+    lib = load_library()
+    need = int(lib.dsv_profile_read(None, 0))
+    buf = ctypes.create_string_buffer(max(need, 1) + 4096)
+    lib.dsv_profile_read(buf, len(buf))
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, n, ms = line.split()
+        out[name] = (int(n), float(ms))
+    return out

@@ -5,6 +5,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
+#include <string>
+#include <vector>
+
 #include "../../include/dsv.h"
 #include "dsv_internal.h"
 
@@ -131,7 +135,33 @@ bool plan_for(const dsv_dims* d, size_t budget, WavePlan* out) {
 
 constexpr size_t kRecommendedPartialBytes = size_t(16) << 30;
 
+// ---------------------------------------------------------------- optional per-kernel timing
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t begin, end;
+};
+constexpr int kProfPool = 16384;
+bool g_prof_on = false;
+std::vector<cudaEvent_t> g_prof_events;   // 2 * kProfPool, created at enable time
+std::vector<ProfRecord> g_prof_records;
+size_t g_prof_dropped = 0;
+
 }  // namespace
+
+namespace dsv {
+ProfScope::ProfScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
+  if (!g_prof_on) return;
+  const size_t n = g_prof_records.size();
+  if (n >= static_cast<size_t>(kProfPool)) { ++g_prof_dropped; return; }
+  ProfRecord r{name, g_prof_events[2 * n], g_prof_events[2 * n + 1]};
+  if (cudaEventRecord(r.begin, s) != cudaSuccess) return;
+  g_prof_records.push_back(r);
+  slot = static_cast<int>(n);
+}
+ProfScope::~ProfScope() {
+  if (slot >= 0) cudaEventRecord(g_prof_records[slot].end, stream);
+}
+}  // namespace dsv
 
 extern "C" {
 
@@ -303,6 +333,57 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
     }
   }
   return ok();
+}
+
+dsv_status dsv_profile_enable(int on) {
+  if (on && !g_prof_on) {
+    if (g_prof_events.empty()) {
+      g_prof_events.resize(2 * kProfPool);
+      for (auto& e : g_prof_events) {
+        cudaError_t err = cudaEventCreate(&e);
+        if (err != cudaSuccess) {
+          g_prof_events.clear();
+          return fail(DSV_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(err));
+        }
+      }
+    }
+    g_prof_records.clear();
+    g_prof_dropped = 0;
+  }
+  if (!on) g_prof_records.clear();
+  g_prof_on = on != 0;
+  return ok();
+}
+
+size_t dsv_profile_read(char* buf, size_t buf_bytes) {
+  std::map<std::string, std::pair<long long, double>> agg;
+  for (const auto& r : g_prof_records) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.end) == cudaSuccess && cudaEventElapsedTime(&ms, r.begin, r.end) == cudaSuccess) {
+      auto& a = agg[r.name];
+      a.first += 1;
+      a.second += ms;
+    }
+  }
+  const bool consume = buf != nullptr && buf_bytes > 0;   // a size query keeps the records
+  if (consume) g_prof_records.clear();
+  std::string out;
+  char line[256];
+  for (const auto& kv : agg) {
+    snprintf(line, sizeof(line), "%s %lld %.6f\n", kv.first.c_str(), kv.second.first, kv.second.second);
+    out += line;
+  }
+  if (g_prof_dropped) {
+    snprintf(line, sizeof(line), "dropped %zu 0\n", g_prof_dropped);
+    out += line;
+    if (consume) g_prof_dropped = 0;
+  }
+  if (consume) {
+    const size_t n = out.size() < buf_bytes - 1 ? out.size() : buf_bytes - 1;
+    memcpy(buf, out.data(), n);
+    buf[n] = '\0';
+  }
+  return out.size() + 1;
 }
 
 dsv_status dsv_last_device_status(void* stream) {

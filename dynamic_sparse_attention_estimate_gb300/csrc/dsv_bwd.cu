@@ -375,22 +375,27 @@ cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t str
   cudaError_t e = cudaMemsetAsync(p.colbits, 0, sizeof(uint32_t) * w.nh * W32 * N, stream);
   if (e != cudaSuccess) return e;
   const int64_t pairs = w.nh * w.nblk * p.topk;
+  { ProfScope prof("bwd_set_bits", stream);
   set_bits_kernel<<<grid_for(pairs, 256), 256, 0, stream>>>(p.idx, p.colbits, N, p.NB, p.topk, w.bh0, w.blk0, w.nblk,
-                                                             W32, pairs, p.status);
-  colpre_kernel<<<grid_for(w.nh * N, 256), 256, 0, stream>>>(p.colbits, p.colpre, p.count, N, W32, w.nh);
-  scan_kernel<<<static_cast<unsigned>(w.nh), kScanThreads, 0, stream>>>(p.count, p.offsets, N, w.nblk * p.topk);
+                                                             W32, pairs, p.status); }
+  { ProfScope prof("bwd_colpre", stream);
+  colpre_kernel<<<grid_for(w.nh * N, 256), 256, 0, stream>>>(p.colbits, p.colpre, p.count, N, W32, w.nh); }
+  { ProfScope prof("bwd_scan", stream);
+  scan_kernel<<<static_cast<unsigned>(w.nh), kScanThreads, 0, stream>>>(p.count, p.offsets, N, w.nblk * p.topk); }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const int smem = BwdSmem<D>::TOTAL;
   e = cudaFuncSetAttribute(sparse_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  { ProfScope prof("bwd_main", stream);
   sparse_bwd_main_kernel<D><<<static_cast<unsigned>(w.nh * w.nblk), kThreads, smem, stream>>>(
-      p, w.bh0, w.blk0, w.nblk, W32, p.scale * kLog2e);
+      p, w.bh0, w.blk0, w.nblk, W32, p.scale * kLog2e); }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   int mode = 0;
   if (w.nblk != p.NB) mode = w.first_of_head ? (w.last_of_head ? 0 : 1) : (w.last_of_head ? 3 : 2);
-  reduce_kernel<D><<<grid_for(w.nh * N * 32, 256, 152 * 64), 256, 0, stream>>>(p, w.bh0, w.nh, mode);
+  { ProfScope prof("bwd_reduce", stream);
+  reduce_kernel<D><<<grid_for(w.nh * N * 32, 256, 152 * 64), 256, 0, stream>>>(p, w.bh0, w.nh, mode); }
   return cudaGetLastError();
 }
 

@@ -192,6 +192,7 @@ cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(sparse_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
+  ProfScope prof("sparse_fwd", stream);
   sparse_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.o, p.lse, p.N, p.NB, p.topk,
                                                           p.scale * kLog2e, p.status);
   return cudaGetLastError();

@@ -10,6 +10,15 @@ namespace dsv {
 
 using bf16 = __nv_bfloat16;
 
+// Brackets one kernel launch with CUDA events when per-kernel timing is enabled
+// (dsv_profile_enable); a no-op otherwise.
+struct ProfScope {
+  int slot;
+  cudaStream_t stream;
+  ProfScope(const char* name, cudaStream_t s);
+  ~ProfScope();
+};
+
 struct EstimateParams {
   const bf16* q_lr;   // [BH][N][r]
   const bf16* k_lr;   // [BH][N][r]

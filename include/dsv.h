@@ -99,7 +99,8 @@ size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims);
  *   dQ_i = scale sum_j dS_ij K_j;
  *   dK_j = scale sum_{i: j in idx[block(i)]} dS_ij Q_i;  dV_j = sum_{same i} P_ij dO_i.
  * Keys no block selected get dK = dV = 0.  No gradient flows to Q_lr / K_lr.
- * idx rows MUST be strictly ascending (as dsv_estimate_topk writes them).
+ * The entries of one idx row must be distinct (dsv_estimate_topk writes them strictly
+ * ascending); a repeated or out-of-range entry sets the device status word.
  * dK/dV are reduced per key in ascending query-block order from per-(block, key)
  * partial rows held in the workspace: deterministic, no float atomics.
  * d_o, q, k, v, o: bf16 [B][H][N][d]; lse fp32 [B][H][N]; idx int32 [B][H][N/block][k];
@@ -121,6 +122,19 @@ const char* dsv_last_error_message(void);
  * last read (the offending entry is skipped, never dereferenced), DSV_ERR_CUDA if
  * the synchronisation failed, DSV_OK otherwise. */
 dsv_status dsv_last_device_status(void* stream);
+
+/*
+ * Optional per-kernel device timing, for measurement tools (not needed for use).
+ * While enabled, every kernel launch the library makes is bracketed by two CUDA events
+ * recorded on the launch's own stream (events come from a pool created at enable time;
+ * no device memory is allocated).  dsv_profile_read() waits for the recorded events and
+ * writes one line per kernel, "name launches total_ms\n", summed since the previous read,
+ * into buf (NUL-terminated, truncated to buf_bytes); it returns the bytes needed.  With
+ * buf == NULL it only reports the size and keeps the records.  Disabling drops unread
+ * records.  Not thread-safe against concurrent launches from several host threads.
+ */
+dsv_status dsv_profile_enable(int on);
+size_t dsv_profile_read(char* buf, size_t buf_bytes);
 
 #ifdef __cplusplus
 }
