@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark one DSV sparse-attention layer step on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+low-rank estimate + top-k per query block -> sparse attention forward -> sparse
+attention backward (dQ, dK, dV), all through the C ABI (libdsv.so).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload short] [--impl dsv|reference]
+
+Prints ONE JSON line (rank 0).  `value` is the effective TFLOP/s of the whole job:
+14 * B * H * N * k * d flops per step (4 N k d forward + 10 N k d backward, only the
+selected query-key pairs counted) divided by the step time, which includes the
+estimate/top-k.  Inputs are resident in HBM when the timed region starts; a 512 MiB
+memset between timed steps flushes L2 (outside the timed events).  `e2e` is the same
+metric when every step also copies its inputs host->device from pinned memory and
+its outputs (O, LSE, dQ, dK, dV) back.  Under torchrun each rank runs an independent
+replica (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, REPO)
+
+METRIC = "sparse attn fwd+bwd effective TFLOP/s and tokens/s at 10% density; % of bf16 peak"
+CSRC = os.path.join(REPO, "dynamic_sparse_attention_estimate_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(REPO, "profiles", "kernel_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="short")
+    ap.add_argument("--density", type=float, default=None)
+    ap.add_argument("--impl", default="dsv", choices=["dsv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload(args):
+    from dynamic_sparse_attention_estimate_gb300.inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.density is not None:
+        wl = wl.with_density(args.density)
+    if wl.heads_per_call:
+        wl = wl.with_heads(wl.heads_per_call)   # the long clip runs 4 heads per call
+    return wl
+
+
+def config_of(wl):
+    t, h, w = wl.latent
+    return {"workload": f"{wl.name}: B={wl.B} H={wl.H} latent {t}x{h}x{w} -> N={wl.N}, d={wl.d}, r={wl.r}, "
+                        f"k={wl.k} ({100 * wl.density:.1f}% density), query blocks of 64",
+            "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "r": wl.r, "k": wl.k, "block": 64,
+            "density": round(wl.density, 4), "l2": "512 MiB memset between timed steps (outside the timed events)"}
+
+
+def flops_per_step(wl):
+    return 14.0 * wl.B * wl.H * wl.N * wl.k * wl.d
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
+
+def oracle_sample(wl, budget_s, cache={}):
+    """Run the fp64 oracle (estimate, forward, backward) on consecutive query blocks of
+    head 0 for about budget_s seconds.  Returns (effective flops done, seconds, blocks)."""
+    import numpy as np
+    import oracle
+    from dynamic_sparse_attention_estimate_gb300.inputs import make_head
+    key = (wl.name, wl.k, wl.N)
+    if key not in cache:
+        x = make_head(wl, 0, 0)
+        cache[key] = ({k: v.float().numpy().astype(np.float64) for k, v in x.items()}, [0])
+    f, nxt = cache[key]
+    t0 = time.perf_counter()
+    nblocks = 0
+    while nblocks == 0 or time.perf_counter() - t0 < budget_s:
+        b = nxt[0] % wl.NB
+        nxt[0] += 1
+        idx = oracle.estimate_topk(f["q_lr"], f["k_lr"], 64, wl.k, blocks=[b])
+        full_idx = np.zeros((wl.NB, wl.k), np.int32)
+        full_idx[b] = idx[0]
+        o, lse = oracle.sparse_attn_fwd(f["q"], f["k"], f["v"], full_idx, 64, blocks=[b])
+        oracle.sparse_attn_bwd(f["do"], f["q"], f["k"], f["v"], full_idx, 64, blocks=[b], o=o, lse=lse)
+        nblocks += 1
+    dt = time.perf_counter() - t0
+    return 14.0 * 64 * nblocks * wl.k * wl.d, dt, nblocks
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = workload(args)
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))   # whole run about two minutes
+    for _ in range(args.warmup):
+        oracle_sample(wl, per_step)
+    flops, secs, blocks = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        fl, dt, nb = oracle_sample(wl, per_step)
+        flops += fl
+        secs += dt
+        blocks += nb
+    value = flops / secs / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{blocks} query blocks of head 0 (estimate + forward + backward), "
+                                       f"~{per_step:.2f} s per step, numpy fp64"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "50"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start, t_end):
+        self.file.flush()
+        rows = []
+        try:
+            with open(self.file.name) as fh:
+                for line in fh:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9 or not parts[1].replace(".", "").isdigit():
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    if ts is None or t_start - 0.05 <= ts <= t_end + 0.05:
+                        rows.append(parts)
+        finally:
+            os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        powers = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(powers) if powers else None}
+
+
+# ---------------------------------------------------------------- roofline bookkeeping
+
+def measured_peaks():
+    p = os.path.join(REPO, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+KERNEL_FILES = {"estimate_topk": "dsv_estimate.cu", "estimate_arange": "dsv_estimate.cu", "sparse_fwd": "dsv_fwd.cu"}
+
+
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for f in (KERNEL_FILES.get(kernel, "dsv_bwd.cu"), "dsv_common.cuh"):
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic(kernel, wl, launches_per_step):
+    """(bound, amount per launch, unit) for a kernel of the step."""
+    BH = wl.B * wl.H
+    if kernel == "sparse_fwd":
+        return "tensor", 4.0 * BH * wl.N * wl.k * wl.d / launches_per_step, "flop"
+    if kernel == "bwd_main":
+        return "tensor", 10.0 * BH * wl.N * wl.k * wl.d / launches_per_step, "flop"
+    if kernel == "estimate_topk":
+        return "hbm", (2.0 * BH * wl.N * wl.r * 2 + 4.0 * BH * wl.NB * wl.k) / launches_per_step, "byte"
+    if kernel == "bwd_reduce":
+        pairs = BH * wl.NB * wl.k
+        return "hbm", (pairs * 2 * wl.d * 4 + 2.0 * BH * wl.N * wl.d * 2) / launches_per_step, "byte"
+    return None, None, None
+
+
+def roofline(prof, steps, wl):
+    hbm, bf16, src = measured_peaks()
+    kern = {k: v for k, v in prof.items() if k != "dropped"}
+    name, (launches, total_ms) = max(kern.items(), key=lambda kv: kv[1][1])
+    bound, amount, unit = algorithmic(name, wl, launches / steps)
+    avg_s = total_ms / launches / 1e3
+    out = {"kernel": name, "launches": launches, "avg_ms": total_ms / launches,
+           "share_of_kernel_time": total_ms / sum(v[1] for v in kern.values())}
+    if bound is None:
+        out.update({"bound": None, "achieved": None, "peak": None, "unit": None, "frac": None, "traffic": None})
+        return out
+    if bound == "tensor":
+        achieved = amount / avg_s / 1e12
+        out.update({"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                    "frac": achieved / bf16, "peak_source": f"bf16_tflops burst, of {src}"})
+    else:
+        achieved = amount / avg_s / 1e9
+        out.update({"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "peak_source": f"hbm_gbs, of {src}"})
+    out["algorithmic_per_launch"] = amount
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        t = json.load(open(TRAFFIC_FILE)).get(name)
+        if t and t.get("source_hash") == kernel_source_hash(name) and t.get("workload") == wl.name:
+            traffic = t["bytes_per_launch"]
+    out["traffic"] = traffic
+    return out
+
+
+# ---------------------------------------------------------------- the DSV arm
+
+def dsv_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_topk, dsv_sparse_attn_bwd,
+                                                         dsv_sparse_attn_fwd, load_library)
+    from dynamic_sparse_attention_estimate_gb300.binding import (dsv_last_device_status, dsv_profile_enable,
+                                                                 dsv_profile_read, dsv_sparse_attn_bwd_workspace,
+                                                                 make_dims)
+    from dynamic_sparse_attention_estimate_gb300.inputs import make_inputs
+    load_library()
+
+    wl = workload(args)
+    host = make_inputs(wl)
+    names = ("q", "k", "v", "do", "q_lr", "k_lr")
+    g = {n: host[n].to(dev) for n in names}
+    idx = torch.empty((wl.B, wl.H, wl.NB, wl.k), dtype=torch.int32, device=dev)
+    o = torch.empty_like(g["q"])
+    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
+    ws = torch.empty(dsv_sparse_attn_bwd_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, wl.k)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k, idx=idx)
+        dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx, out=(o, lse))
+        dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws, out=(dq, dk, dv))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dsv_last_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- timed region (device-resident inputs)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.time()
+        dsv_profile_enable(True)
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        prof = dsv_profile_read()
+        dsv_profile_enable(False)
+    clocks = clk.summary(t_wall0, t_wall1)
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    fl = flops_per_step(wl)
+    value = world * args.steps * fl / (total_ms / 1e3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # ---- stage breakdown (separately timed, same inputs)
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    n_stage = max(3, min(20, args.steps))
+    t_est = timed(lambda: dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k, idx=idx), n_stage)
+    t_fwd = timed(lambda: dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx, out=(o, lse)), n_stage)
+    t_bwd = timed(lambda: dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws,
+                                              out=(dq, dk, dv)), n_stage)
+    BH = wl.B * wl.H
+
+    # ---- e2e through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: host[n].pin_memory() for n in names}
+        outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        back = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in back.values())
+        n_e2e = max(3, min(args.steps, 50))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+        for i in range(n_e2e + 2):                 # two untimed passes first
+            a, b = ev[max(i - 2, 0)]
+            if i >= 2:
+                a.record()
+            for n in names:
+                g[n].copy_(pinned[n], non_blocking=True)
+            step()
+            for n, t in outs.items():
+                back[n].copy_(t, non_blocking=True)
+            if i >= 2:
+                b.record()
+            torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in ev)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * n_e2e * fl / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / n_e2e, "steps": n_e2e}
+
+    # ---- dense comparator (PyTorch SDPA fwd+bwd on the same shape)
+    dense = None
+    if not args.no_dense:
+        try:
+            qf, kf, vf = [g[n].detach().clone().requires_grad_(True) for n in ("q", "k", "v")]
+
+            def dense_step():
+                out = torch.nn.functional.scaled_dot_product_attention(qf, kf, vf)
+                out.backward(g["do"])
+            for _ in range(2):
+                dense_step()
+            t_dense = timed(dense_step, 5)
+            dense = {"ms": t_dense, "tflops": 14.0 * BH * wl.N * wl.N * wl.d / (t_dense / 1e3) / 1e12,
+                     "speedup_of_sparse_step": t_dense / ms_per_step, "impl": "torch SDPA (library)"}
+        except Exception as exc:  # a comparator only
+            dense = {"error": str(exc)[:200]}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        fl_s, dt, nb = oracle_sample(wl, 12.0)
+        cpu = {"value": fl_s / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{nb} of {BH * wl.NB} query blocks (head 0): estimate + forward + backward, numpy fp64, "
+                         f"{dt:.1f} s"}
+
+    rl = roofline(prof, args.steps, wl)
+    launches = sum(v[0] for k, v in prof.items() if k != "dropped")
+    hbm, bf16, src = measured_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the short-clip workload)",
+        "config": config_of(wl),
+        "tokens_per_s": world * wl.B * wl.N * args.steps / (total_ms / 1e3),
+        "pct_of_bf16_peak": 100.0 * value / world / bf16,
+        "stages_ms": {"estimate_topk": t_est, "sparse_fwd": t_fwd, "sparse_bwd": t_bwd},
+        "attn_only_tflops": 14.0 * BH * wl.N * wl.k * wl.d / ((t_fwd + t_bwd) / 1e3) / 1e12,
+        "kernel_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+        "roofline": rl, "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "dense_comparator": dense,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return dsv_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
