@@ -25,7 +25,7 @@ EXPORTED = (
     "dsv_estimate_topk_workspace", "dsv_estimate_topk", "dsv_sparse_attn_fwd",
     "dsv_sparse_attn_bwd_workspace", "dsv_sparse_attn_bwd_workspace_min", "dsv_sparse_attn_bwd",
     "dsv_status_string", "dsv_last_error_message", "dsv_last_device_status",
-    "dsv_profile_enable", "dsv_profile_read",
+    "dsv_profile_enable", "dsv_profile_read", "dsv_sparse_attn_bwd_noalloc",
 )
 
 
@@ -74,6 +74,8 @@ def load_library(path: Optional[str] = None):
     lib.dsv_last_error_message.restype = ctypes.c_char_p
     lib.dsv_last_device_status.argtypes = [vp]
     lib.dsv_last_device_status.restype = st
+    lib.dsv_sparse_attn_bwd_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.dsv_sparse_attn_bwd_noalloc.restype = st
     lib.dsv_profile_enable.argtypes = [st]
     lib.dsv_profile_enable.restype = st
     lib.dsv_profile_read.argtypes = [ctypes.c_char_p, sz]

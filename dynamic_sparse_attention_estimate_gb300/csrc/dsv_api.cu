@@ -397,4 +397,43 @@ dsv_status dsv_last_device_status(void* stream) {
   return ok();
 }
 
+// ---------------------------------------------------------------- backward with library-held scratch
+// For callers that cannot allocate device memory (see include/dsv.h).  The scratch is a
+// fixed device array; host code only ever uses the address looked up per device below.
+}  // extern "C"
+
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSV_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};   // per-device address of g_noalloc_scratch
+}  // namespace
+
+extern "C" {
+
+dsv_status dsv_sparse_attn_bwd_noalloc(const dsv_dims* dims, const void* d_o, const void* q, const void* k,
+                                       const void* v, const void* o, const float* lse, const int32_t* idx,
+                                       void* dq, void* dk, void* dv, void* stream) {
+  dsv_status s = check_dims(dims, true, false);
+  if (s != DSV_OK) return s;
+  const size_t need = dsv_sparse_attn_bwd_workspace_min(dims);
+  if (need > DSV_NOALLOC_SCRATCH_BYTES)
+    return fail(DSV_ERR_WORKSPACE,
+                "this backward needs at least %zu bytes of scratch but the no-allocation variant holds %zu; "
+                "call dsv_sparse_attn_bwd with a caller workspace instead",
+                need, static_cast<size_t>(DSV_NOALLOC_SCRATCH_BYTES));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSV_ERR_CUDA, "device ordinal %d out of range", dev);
+  if (!g_noalloc_ptr[dev]) {  // set-up, once per device, with that device current
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  // The backward clears its bitmaps at the start of every wave and writes every other
+  // scratch region before reading it, so what an earlier call left behind is never used.
+  return dsv_sparse_attn_bwd(dims, d_o, q, k, v, o, lse, idx, dq, dk, dv, g_noalloc_ptr[dev],
+                             DSV_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 }  // extern "C"

@@ -111,6 +111,31 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
                                const void* v, const void* o, const float* lse, const int32_t* idx,
                                void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Backward without a caller workspace.  Some callers cannot allocate device memory
+ * themselves: a host framework that owns every byte of the GPU through its own pool and
+ * forbids outside allocations during a step, a plug-in whose memory budget is fixed when
+ * its process starts, or a latency-critical loop where cudaMalloc/cudaFree would stall the
+ * device.  This entry point computes exactly what dsv_sparse_attn_bwd computes, with the
+ * library's own scratch: a fixed array of DSV_NOALLOC_SCRATCH_BYTES (32 MiB) in device
+ * memory, held by every GPU that loads the library until the process exits.  It allocates
+ * nothing.  (The DSV pages have no counterpart: this is a deployment convenience.)
+ *   - Problems whose smallest backward workspace (dsv_sparse_attn_bwd_workspace_min) is
+ *     above DSV_NOALLOC_SCRATCH_BYTES are rejected with DSV_ERR_WORKSPACE before anything
+ *     runs; larger problems that fit are processed in several waves.
+ *   - The first call on a device looks up that device's address of the array (with the
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the one array, which keeps whatever the last call left there (every
+ *     call rebuilds what it reads, so stale contents are never used); calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on it and must be
+ *     ordered by the caller.
+ * Arguments and outputs are those of dsv_sparse_attn_bwd without ws / ws_bytes.
+ */
+#define DSV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+dsv_status dsv_sparse_attn_bwd_noalloc(const dsv_dims* dims, const void* d_o, const void* q, const void* k,
+                                       const void* v, const void* o, const float* lse, const int32_t* idx,
+                                       void* dq, void* dk, void* dv, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* dsv_status_string(dsv_status status);
 
