@@ -236,7 +236,7 @@ dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* 
   p.d = static_cast<int>(dims->d);
   p.scale = eff_scale(dims);
   p.status = status;
-  cudaError_t e = dsv::launch_sparse_fwd(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = dsv::launch_sparse_fwd_tc(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -393,7 +393,10 @@ dsv_status dsv_last_device_status(void* stream) {
   e = cudaMemcpyFromSymbol(&v, g_dsv_status, sizeof(v));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_dsv_status, &zero, sizeof(zero));
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
-  if (v) return fail(DSV_ERR_DEVICE_CHECK, "a kernel met an out-of-range or repeated key index (status 0x%x)", v);
+  if (v)
+    return fail(DSV_ERR_DEVICE_CHECK, "device status 0x%x:%s%s", v,
+                (v & 1u) ? " an out-of-range or repeated key index" : "",
+                (v & 2u) ? " a kernel gave up waiting on its own barrier" : "");
   return ok();
 }
 

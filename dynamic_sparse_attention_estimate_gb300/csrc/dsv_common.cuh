@@ -11,6 +11,8 @@ namespace dsv {
 
 // Bit set in the device status word when a kernel meets a key index outside [0, N).
 constexpr unsigned int kStatusBadIndex = 1u;
+// Bit set when a kernel gave up waiting on one of its own mbarriers (bounded waits).
+constexpr unsigned int kStatusTimeout = 2u;
 
 // log2(e): softmax runs in base 2 with the scale folded in.
 constexpr float kLog2e = 1.4426950408889634f;

@@ -1,0 +1,415 @@
+// Sparse attention forward on the tcgen05 tensor cores (DSV, Spanish technical summary
+// section 3: custom fused kernels for sparse attention over the critical keys).
+//
+// One CTA = one query block (64 queries) of one head.  Its selected keys are processed in
+// chunks of 128 with keys on the MMA's M dimension (the "transposed" formulation):
+//     S^T[128 keys x 64 q]  = K_c . Q^T           (tcgen05, M=128, N=64, K=d)
+//     O^T[d x 64 q]        += V_c^T . P^T         (tcgen05, M=d,   N=64, K=128)
+// so both products keep M = 128 (M = 64 for d = 64), the MMA's efficient shape, even though
+// a query block has only 64 rows.  Roles (288 threads):
+//   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
+//              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16) to shared
+//              memory as the B operand of the next product;
+//   warps 4-7  producers: gather the chunk's K and V rows with cp.async into 128-byte-
+//              swizzled shared memory (two stages), then signal an mbarrier;
+//   warp 8     one thread issues every MMA and commits them to mbarriers.
+// The running max m_q is kept STALE: a chunk only triggers the cross-thread column max and
+// an O/L rescale when one of its logits exceeds m_q by more than 8 (in log2 units; the
+// first chunk always does).  Otherwise P <= 2^8, which bf16 and fp32 hold exactly enough,
+// and softmax is invariant to the subtracted constant.  Row sums are accumulated per key
+// lane in TMEM and reduced across lanes once, at the end.
+#include "dsv_common.cuh"
+#include "dsv_internal.h"
+#include "dsv_tc.cuh"
+
+#include <math_constants.h>
+
+namespace dsv {
+namespace {
+
+constexpr int kChunk = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 288;
+constexpr float kStaleLimit = 8.f;  // log2 units
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+// TMEM columns
+constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kColL = 192, kTmemCols = 256;
+
+template <int D>
+struct Smem {
+  static constexpr int BLK = D / 64;                 // 64-element column blocks
+  static constexpr int Q_BYTES = BLK * 64 * 128;
+  static constexpr int KV_BYTES = BLK * kChunk * 128;
+  static constexpr int P_BYTES = kChunk * 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + kStages * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + kStages * KV_BYTES;
+  static constexpr int TOTAL = OFF_P + 2 * P_BYTES;
+};
+
+struct Bars {
+  uint64_t full[kStages];   // producers -> MMA / softmax: K, V (and Q) of a stage landed
+  uint64_t empty[kStages];  // MMA commit: the PV product that last read a stage is done
+  uint64_t s_full[2];       // MMA commit: S^T in TMEM buffer b is ready
+  uint64_t s_empty[2];      // softmax: S^T buffer b has been read
+  uint64_t p_full[2];       // softmax: P^T tile b written
+  uint64_t pv_done[2];      // MMA commit: PV with P^T tile b done
+  uint64_t o_full;          // MMA commit: last PV done
+};
+
+DSV_DEVICE void named_sync_softmax() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// Barrier over the 128 softmax threads that also ORs a flag across them (uniform result).
+DSV_DEVICE bool named_sync_or(bool v) {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(v))
+               : "memory");
+  return r != 0;
+}
+
+// Column reduction over the 128 softmax threads of 64 per-thread values (v[c] is this
+// thread's value for column c).  Fixed order, so the result is deterministic.  Returns
+// through red[64] in shared memory (visible after the trailing barrier).
+template <bool MAX>
+DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* red, int warp, int lane) {
+  // butterfly halving: after the step with mask m each lane keeps half of its columns
+  float cur[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) cur[i] = v[i];
+  int n = 64;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+    n >>= 1;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < n) {
+        const float mine = upper ? cur[i + n] : cur[i];
+        const float other = upper ? cur[i] : cur[i + n];
+        const float recv = __shfl_xor_sync(0xffffffffu, other, m);
+        cur[i] = MAX ? fmaxf(mine, recv) : mine + recv;
+      }
+    }
+  }
+  // lane holds columns 2 lane, 2 lane + 1 (reduced over its warp)
+  red_w[warp * 64 + 2 * lane] = cur[0];
+  red_w[warp * 64 + 2 * lane + 1] = cur[1];
+  named_sync_softmax();
+  if (warp * 32 + lane < 64) {
+    const int q = warp * 32 + lane;
+    float r = red_w[q];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) r = MAX ? fmaxf(r, red_w[w * 64 + q]) : r + red_w[w * 64 + q];
+    red[q] = r;
+  }
+  named_sync_softmax();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+                     const int32_t* __restrict__ idx, bf16* __restrict__ o, float* __restrict__ lse, int64_t N,
+                     int64_t NB, int64_t kk, float scale_log2, unsigned int* status) {
+  using S = Smem<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ float m_s[64], alpha_s[64], red_w[4 * 64], red_s[64];
+  __shared__ uint8_t valid_s[kStages][kChunk];
+  __shared__ int flag_s[2];
+  __shared__ int fail_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bh = blockIdx.y, blk = blockIdx.x;
+  const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + S::OFF_Q, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V, sP = sbase + S::OFF_P;
+  auto bar = [](uint64_t& b) { return smem_u32(&b); };
+
+  if (warp == 0) {
+    tc::tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar(bars.full[s]), 128);
+      tc::mbar_init(bar(bars.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(bar(bars.s_full[b]), 1);
+      tc::mbar_init(bar(bars.s_empty[b]), 128);
+      tc::mbar_init(bar(bars.p_full[b]), 128);
+      tc::mbar_init(bar(bars.pv_done[b]), 1);
+    }
+    tc::mbar_init(bar(bars.o_full), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    flag_s[0] = flag_s[1] = 0;
+    fail_s = 0;
+  }
+  if (tid < 64) m_s[tid] = -CUDART_INF_F;
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp >= 4 && warp < 8) {
+    // ================================================================ producers
+    const int t = tid - 128;
+    const bf16* qb = q + (bh * N + blk * 64) * D;
+    const bf16* kh = k + bh * N * D;
+    const bf16* vh = v + bh * N * D;
+    const int32_t* ib = idx + (bh * NB + blk) * kk;
+    for (int i = t; i < 64 * (D / 8); i += 128) {
+      const int row = i / (D / 8), e = (i % (D / 8)) * 8;
+      cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
+    }
+    bool ok_run = true;
+    for (int c = 0; c < nchunks && ok_run; ++c) {
+      const int st = c % kStages;
+      if (c >= kStages && !tc::mbar_wait(bar(bars.empty[st]), ((c / kStages) - 1) & 1, kWaitLimit)) {
+        ok_run = false;
+        break;
+      }
+      const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
+      for (int i = t; i < kChunk * (D / 8); i += 128) {
+        const int row = i / (D / 8), e = (i % (D / 8)) * 8;
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + row;
+        const int64_t j = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
+        const bool ok = j >= 0 && j < N;
+        if (e == 0) {
+          valid_s[st][row] = ok;
+          if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
+        }
+        const int64_t src = ok ? j : 0;
+        const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
+        cp_async_16(dK + off, kh + src * D + e, ok);
+        cp_async_16(dV + off, vh + src * D + e, ok);
+      }
+      cp_async_commit();
+      if (c >= 1) {
+        cp_async_wait<1>();
+        tc::fence_async_shared();
+        tc::mbar_arrive(bar(bars.full[(c - 1) % kStages]));
+      }
+    }
+    cp_async_wait<0>();
+    tc::fence_async_shared();
+    if (ok_run) tc::mbar_arrive(bar(bars.full[(nchunks - 1) % kStages]));
+    else atomicOr(&fail_s, 1);
+  } else if (warp == 8) {
+    // ================================================================ MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idO = tc::idesc_bf16(D, 64, 1, 1);
+      bool ok_run = true;
+      for (int c = 0; c <= nchunks && ok_run; ++c) {
+        if (c < nchunks) {
+          const int st = c % kStages, b = c & 1;
+          ok_run = tc::mbar_wait(bar(bars.full[st]), (c / kStages) & 1, kWaitLimit);
+          if (ok_run && c >= 2) ok_run = tc::mbar_wait(bar(bars.s_empty[b]), ((c - 2) >> 1) & 1, kWaitLimit);
+          if (!ok_run) break;
+          tc::tc_fence_after();
+          const uint32_t aK = sK + st * S::KV_BYTES;
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
+            const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
+            tc::mma_ss(tmem + (b ? kColS1 : kColS0), tc::smem_desc(aK + off_a, 16, 1024),
+                       tc::smem_desc(sQ + off_b, 16, 1024), idS, j > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bars.s_full[b]));
+        }
+        if (c >= 1) {
+          const int cp = c - 1, st = cp % kStages, b = cp & 1;
+          ok_run = tc::mbar_wait(bar(bars.p_full[b]), (cp >> 1) & 1, kWaitLimit);
+          if (!ok_run) break;
+          tc::tc_fence_after();
+          const uint32_t aV = sV + st * S::KV_BYTES, bP = sP + b * S::P_BYTES;
+#pragma unroll
+          for (int j = 0; j < kChunk / 16; ++j)
+            tc::mma_ss(tmem + kColO, tc::smem_desc(aV + j * 2048, kChunk * 128, 1024),
+                       tc::smem_desc(bP + j * 2048, 8192, 1024), idO, (cp > 0 || j > 0) ? 1u : 0u);
+          tc::mma_commit(bar(bars.pv_done[b]));
+          tc::mma_commit(bar(bars.empty[st]));
+          if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
+        }
+      }
+      if (!ok_run) atomicOr(&fail_s, 1);
+    }
+  } else {
+    // ================================================================ softmax (threads 0..127)
+    const int t = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Every softmax thread runs every iteration and reaches every named barrier, also after
+    // a timed-out wait (later waits are then skipped and the results are discarded).
+    bool ok_run = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages, b = c & 1;
+      ok_run = ok_run && tc::mbar_wait(bar(bars.s_full[b]), (c >> 1) & 1, kWaitLimit);
+      ok_run = ok_run && tc::mbar_wait(bar(bars.full[st]), (c / kStages) & 1, kWaitLimit);
+      tc::tc_fence_after();
+      float x[64];
+      {
+        uint32_t r[16];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          tc::tmem_ld16(tmem + lane_base + (b ? kColS1 : kColS0) + h * 16, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[h * 16 + i] = __uint_as_float(r[i]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(bars.s_empty[b]));
+      const bool valid = (static_cast<int64_t>(c) * kChunk + t < kk) && valid_s[st][t];
+      bool over = false;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        x[i] = valid ? x[i] * scale_log2 : -CUDART_INF_F;
+        over |= x[i] - m_s[i] > kStaleLimit;
+      }
+      if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(&flag_s[c & 1], 1);
+      if (t == 0) flag_s[(c + 1) & 1] = 0;
+      named_sync_softmax();
+      if (flag_s[c & 1]) {
+        // ---- new running max for this chunk; rescale O and L
+        column_reduce<true>(x, red_w, red_s, warp, lane);
+        if (t < 64) {
+          const float mo = m_s[t];
+          const float mn = fmaxf(mo, red_s[t]);
+          alpha_s[t] = mn == -CUDART_INF_F ? 1.f : fast_exp2(mo - mn);
+          m_s[t] = mn;
+        }
+        named_sync_softmax();
+        if (c > 0) {
+          ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[(c - 1) & 1]), ((c - 1) >> 1) & 1, kWaitLimit);
+          tc::tc_fence_after();
+#pragma unroll
+          for (int col = 0; col < 2; ++col) {  // O^T (lanes = d) then L (lanes = keys)
+            const uint32_t base = tmem + lane_base + (col ? kColL : kColO);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              uint32_t r[16];
+              tc::tmem_ld16(base + h * 16, r);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_s[h * 16 + i]);
+              tc::tmem_st16(base + h * 16, r);
+            }
+          }
+          tc::tmem_wait_st();
+        }
+      }
+      // ---- P^T row of this key: exp2(x - m), into the B tile (64 queries = one 128-byte row)
+      if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[b]), ((c - 2) >> 1) & 1, kWaitLimit);
+      float p[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) p[i] = x[i] == -CUDART_INF_F ? 0.f : fast_exp2(x[i] - m_s[i]);
+      const uint32_t prow = sP + b * S::P_BYTES + t * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t w0 = pack_bf16x2(p[ch * 8 + 0], p[ch * 8 + 1]), w1 = pack_bf16x2(p[ch * 8 + 2], p[ch * 8 + 3]);
+        const uint32_t w2 = pack_bf16x2(p[ch * 8 + 4], p[ch * 8 + 5]), w3 = pack_bf16x2(p[ch * 8 + 6], p[ch * 8 + 7]);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + (((ch ^ t) & 7) << 4)), "r"(w0), "r"(w1),
+                     "r"(w2), "r"(w3));
+      }
+      // ---- row sums of this key lane, accumulated in TMEM
+      {
+        const uint32_t base = tmem + lane_base + kColL;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t r[16];
+          if (c > 0) {
+            tc::tmem_ld16(base + h * 16, r);
+            tc::tmem_wait_ld();
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint((c > 0 ? __uint_as_float(r[i]) : 0.f) + p[h * 16 + i]);
+          tc::tmem_st16(base + h * 16, r);
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_async_shared();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(bars.p_full[b]));
+    }
+    // ---- epilogue: l = column sums of L, O = O^T / l, LSE = (m + log2 l) ln 2
+    ok_run = ok_run && tc::mbar_wait(bar(bars.o_full), 0, kWaitLimit);
+    if (!ok_run) atomicOr(&fail_s, 1);
+    const bool failed = named_sync_or(!ok_run);
+    if (!failed) {
+      tc::tc_fence_after();
+      float lsum[64];
+      {
+        uint32_t r[16];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          tc::tmem_ld16(tmem + lane_base + kColL + h * 16, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lsum[h * 16 + i] = __uint_as_float(r[i]);
+        }
+      }
+      column_reduce<false>(lsum, red_w, red_s, warp, lane);
+      // O^T lane -> head dim: identity for d = 128; for d = 64 (M = 64) rows sit 16 per lane quadrant
+      const int dim = D == 128 ? t : ((lane < 16) ? warp * 16 + lane : -1);
+      bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D], K stage 0 is free now
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + lane_base + kColO + h * 16, r);  // whole warp, converged
+        tc::tmem_wait_ld();
+        if (dim >= 0) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int qq = h * 16 + i;
+            const float l = red_s[qq];
+            stage[qq * D + dim] = __float2bfloat16_rn(l > 0.f ? __uint_as_float(r[i]) / l : 0.f);
+          }
+        }
+      }
+      named_sync_softmax();
+      bf16* ob = o + (bh * N + blk * 64) * D;
+      for (int i = t; i < 64 * D / 8; i += 128)
+        reinterpret_cast<uint4*>(ob)[i] = reinterpret_cast<const uint4*>(stage)[i];
+      if (t < 64) {
+        const float l = red_s[t];
+        lse[bh * N + blk * 64 + t] = l > 0.f ? (m_s[t] + __log2f(l)) * kLn2 : -CUDART_INF_F;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (fail_s && tid == 0) flag_status(status, kStatusTimeout);
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
+  const int smem = Smem<D>::TOTAL;
+  cudaError_t e = cudaFuncSetAttribute(sparse_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
+  ProfScope prof("sparse_fwd", stream);
+  sparse_fwd_tc_kernel<D><<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.o, p.lse, p.N, p.NB, p.topk,
+                                                             p.scale * kLog2e, p.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_fwd_tc(const FwdParams& p, cudaStream_t stream) {
+  switch (p.d) {
+    case 64: return launch_d<64>(p, stream);
+    case 128: return launch_d<128>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsv

@@ -40,6 +40,7 @@ struct FwdParams {
   unsigned int* status;
 };
 cudaError_t launch_sparse_fwd(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_sparse_fwd_tc(const FwdParams& p, cudaStream_t stream);
 
 // One wave of the backward: either whole heads [bh0, bh0 + nh) (blk0 = 0, nblk = NB)
 // or the query blocks [blk0, blk0 + nblk) of the single head bh0 (nh = 1).
