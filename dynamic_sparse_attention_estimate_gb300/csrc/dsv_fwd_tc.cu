@@ -10,8 +10,9 @@
 //   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
 //              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16) to shared
 //              memory as the B operand of the next product;
-//   warps 4-7  producers: gather the chunk's K and V rows with cp.async into 128-byte-
-//              swizzled shared memory (two stages), then signal an mbarrier;
+//   warps 4-7  producers, two groups of 64 threads, one per stage: gather a chunk's K and
+//              V rows with cp.async into 128-byte-swizzled shared memory, wait for their
+//              own copies, then signal the stage's mbarrier;
 //   warp 8     one thread issues every MMA and commits them to mbarriers.
 // The running max m_q is kept STALE: a chunk only triggers the cross-thread column max and
 // an O/L rescale when one of its logits exceeds m_q by more than 8 (in log2 units; the
@@ -135,7 +136,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(bar(bars.full[s]), 128);
+      tc::mbar_init(bar(bars.full[s]), 64);
       tc::mbar_init(bar(bars.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -157,24 +158,29 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 
   if (warp >= 4 && warp < 8) {
     // ================================================================ producers
-    const int t = tid - 128;
+    // Two groups of 64 threads; group g owns stage g and the chunks c with c % 2 == g, so
+    // each group can block on its own copies while the other group's are in flight.
+    const int grp = (warp - 4) >> 1;
+    const int t = tid - 128 - grp * 64;
     const bf16* qb = q + (bh * N + blk * 64) * D;
     const bf16* kh = k + bh * N * D;
     const bf16* vh = v + bh * N * D;
     const int32_t* ib = idx + (bh * NB + blk) * kk;
-    for (int i = t; i < 64 * (D / 8); i += 128) {
-      const int row = i / (D / 8), e = (i % (D / 8)) * 8;
-      cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
+    if (grp == 0) {
+      for (int i = t; i < 64 * (D / 8); i += 64) {
+        const int row = i / (D / 8), e = (i % (D / 8)) * 8;
+        cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
+      }
     }
     bool ok_run = true;
-    for (int c = 0; c < nchunks && ok_run; ++c) {
-      const int st = c % kStages;
+    for (int c = grp; c < nchunks; c += kStages) {
+      const int st = grp;
       if (c >= kStages && !tc::mbar_wait(bar(bars.empty[st]), ((c / kStages) - 1) & 1, kWaitLimit)) {
         ok_run = false;
         break;
       }
       const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
-      for (int i = t; i < kChunk * (D / 8); i += 128) {
+      for (int i = t; i < kChunk * (D / 8); i += 64) {
         const int row = i / (D / 8), e = (i % (D / 8)) * 8;
         const int64_t slot = static_cast<int64_t>(c) * kChunk + row;
         const int64_t j = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
@@ -189,16 +195,12 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         cp_async_16(dV + off, vh + src * D + e, ok);
       }
       cp_async_commit();
-      if (c >= 1) {
-        cp_async_wait<1>();
-        tc::fence_async_shared();
-        tc::mbar_arrive(bar(bars.full[(c - 1) % kStages]));
-      }
+      cp_async_wait<0>();
+      tc::fence_async_shared();
+      tc::mbar_arrive(bar(bars.full[st]));
     }
     cp_async_wait<0>();
-    tc::fence_async_shared();
-    if (ok_run) tc::mbar_arrive(bar(bars.full[(nchunks - 1) % kStages]));
-    else atomicOr(&fail_s, 1);
+    if (!ok_run) atomicOr(&fail_s, 1);
   } else if (warp == 8) {
     // ================================================================ MMA issue (one thread)
     if (lane == 0) {
