@@ -28,8 +28,12 @@
 namespace dsv {
 namespace {
 
+#ifndef DSV_FWD64_MIN_BLOCKS
+#define DSV_FWD64_MIN_BLOCKS 2
+#endif
+
 constexpr int kChunk = 128;
-constexpr int kStages = 2;
+constexpr int kStages = 2;  // one producer group (64 threads) per stage
 constexpr int kThreads = 288;
 constexpr float kStaleLimit = 8.f;  // log2 units
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -110,7 +114,7 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, D == 64 ? DSV_FWD64_MIN_BLOCKS : 1)
 sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ idx, bf16* __restrict__ o, float* __restrict__ lse, int64_t N,
                      int64_t NB, int64_t kk, float scale_log2, unsigned int* status) {
@@ -167,10 +171,9 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     const bf16* vh = v + bh * N * D;
     const int32_t* ib = idx + (bh * NB + blk) * kk;
     if (grp == 0) {
-      for (int i = t; i < 64 * (D / 8); i += 64) {
-        const int row = i / (D / 8), e = (i % (D / 8)) * 8;
-        cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
-      }
+#pragma unroll
+      for (int e = 0; e < D; e += 8)
+        cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(t, e & 63), qb + t * D + e, true);
     }
     bool ok_run = true;
     for (int c = grp; c < nchunks; c += kStages) {
@@ -180,19 +183,28 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         break;
       }
       const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
-      for (int i = t; i < kChunk * (D / 8); i += 64) {
-        const int row = i / (D / 8), e = (i % (D / 8)) * 8;
+      // this thread copies whole rows t and t + 64; both indices are loaded before any copy
+      int64_t j[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + t + 64 * h;
+        j[h] = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = t + 64 * h;
         const int64_t slot = static_cast<int64_t>(c) * kChunk + row;
-        const int64_t j = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
-        const bool ok = j >= 0 && j < N;
-        if (e == 0) {
-          valid_s[st][row] = ok;
-          if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
+        const bool ok = j[h] >= 0 && j[h] < N;
+        valid_s[st][row] = ok;
+        if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
+        const bf16* ks = kh + (ok ? j[h] : 0) * D;
+        const bf16* vs = vh + (ok ? j[h] : 0) * D;
+#pragma unroll
+        for (int e = 0; e < D; e += 8) {
+          const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
+          cp_async_16(dK + off, ks + e, ok);
+          cp_async_16(dV + off, vs + e, ok);
         }
-        const int64_t src = ok ? j : 0;
-        const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
-        cp_async_16(dK + off, kh + src * D + e, ok);
-        cp_async_16(dV + off, vh + src * D + e, ok);
       }
       cp_async_commit();
       cp_async_wait<0>();
@@ -255,14 +267,14 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       tc::tc_fence_after();
       float x[64];
       {
-        uint32_t r[16];
+        uint32_t r[4][16];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          tc::tmem_ld16(tmem + lane_base + (b ? kColS1 : kColS0) + h * 16, r);
-          tc::tmem_wait_ld();
+        for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + (b ? kColS1 : kColS0) + h * 16, r[h]);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[h * 16 + i] = __uint_as_float(r[i]);
-        }
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[h * 16 + i] = __uint_as_float(r[h][i]);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty[b]));
@@ -307,7 +319,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       }
       // ---- P^T row of this key: exp2(x - m), into the B tile (64 queries = one 128-byte row)
       if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[b]), ((c - 2) >> 1) & 1, kWaitLimit);
-      float p[64];
+      float (&p)[64] = x;  // probabilities overwrite the logits
 #pragma unroll
       for (int i = 0; i < 64; ++i) p[i] = x[i] == -CUDART_INF_F ? 0.f : fast_exp2(x[i] - m_s[i]);
       const uint32_t prow = sP + b * S::P_BYTES + t * 128;
@@ -319,21 +331,24 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
                      "r"(w2), "r"(w3));
       }
       // ---- row sums of this key lane, accumulated in TMEM
-      {
-        const uint32_t base = tmem + lane_base + kColL;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t r[16];
-          if (c > 0) {
-            tc::tmem_ld16(base + h * 16, r);
-            tc::tmem_wait_ld();
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint((c > 0 ? __uint_as_float(r[i]) : 0.f) + p[h * 16 + i]);
-          tc::tmem_st16(base + h * 16, r);
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t base = tmem + lane_base + kColL + half * 32;
+        uint32_t r[2][16];
+        if (c > 0) {
+          tc::tmem_ld16(base, r[0]);
+          tc::tmem_ld16(base + 16, r[1]);
+          tc::tmem_wait_ld();
         }
-        tc::tmem_wait_st();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            r[h][i] = __float_as_uint((c > 0 ? __uint_as_float(r[h][i]) : 0.f) + p[half * 32 + h * 16 + i]);
+          tc::tmem_st16(base + h * 16, r[h]);
+        }
       }
+      tc::tmem_wait_st();
       tc::fence_async_shared();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.p_full[b]));
