@@ -61,6 +61,8 @@ dsv_status check_dims(const dsv_dims* d, bool need_d, bool need_r) {
   if (d->N > 0x7fffffffLL) return fail(DSV_ERR_INVALID_ARG, "N must fit int32 key indices");
   if (d->k < 1 || d->k > d->N) return fail(DSV_ERR_INVALID_ARG, "need 1 <= k <= N (k=%lld)", (long long)d->k);
   if (d->B * d->H > (1LL << 31) - 1) return fail(DSV_ERR_INVALID_ARG, "B*H too large");
+  if (d->B * d->H * d->N > 0x7fffffffLL)
+    return fail(DSV_ERR_INVALID_ARG, "B*H*N must fit int32 row coordinates (split the heads over calls)");
   if (need_d && d->d != 64 && d->d != 128)
     return fail(DSV_ERR_UNSUPPORTED, "head dim d must be 64 or 128 (got %lld)", (long long)d->d);
   if (need_r && (d->r < 16 || d->r > 64 || d->r % 16))

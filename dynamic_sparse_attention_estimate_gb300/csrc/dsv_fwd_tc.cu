@@ -5,20 +5,22 @@
 // chunks of 128 with keys on the MMA's M dimension (the "transposed" formulation):
 //     S^T[128 keys x 64 q]  = K_c . Q^T           (tcgen05, M=128, N=64, K=d)
 //     O^T[d x 64 q]        += V_c^T . P^T         (tcgen05, M=d,   N=64, K=128)
-// so both products keep M = 128 (M = 64 for d = 64), the MMA's efficient shape, even though
-// a query block has only 64 rows.  Roles (288 threads):
+// so both products keep M = 128 (M = 64 for d = 64) although a block has 64 queries.
+// Roles (192 threads):
 //   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
-//              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16) to shared
-//              memory as the B operand of the next product;
-//   warps 4-7  producers, two groups of 64 threads, one per stage: gather a chunk's K and
-//              V rows with cp.async into 128-byte-swizzled shared memory, wait for their
-//              own copies, then signal the stage's mbarrier;
-//   warp 8     one thread issues every MMA and commits them to mbarriers.
+//              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16, one 128-byte
+//              row) to shared memory as the B operand of the PV product;
+//   warp 4     producer: gathers the chunk's K and V rows with TMA tile::gather4 (four rows
+//              per instruction, 128-byte swizzle) into a ring of stages; selected keys past
+//              k or out of range use an out-of-bounds row, which TMA fills with zeros;
+//   warp 5     one thread issues every MMA as soon as its inputs are ready (it polls the
+//              stage, P and S barriers without blocking on any single one).
 // The running max m_q is kept STALE: a chunk only triggers the cross-thread column max and
 // an O/L rescale when one of its logits exceeds m_q by more than 8 (in log2 units; the
-// first chunk always does).  Otherwise P <= 2^8, which bf16 and fp32 hold exactly enough,
-// and softmax is invariant to the subtracted constant.  Row sums are accumulated per key
-// lane in TMEM and reduced across lanes once, at the end.
+// first chunk always does).  Otherwise P <= 2^8, and softmax is invariant to the
+// subtracted constant.  Row sums accumulate per key lane in TMEM and are reduced once.
+#include <cuda.h>
+
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -28,20 +30,16 @@
 namespace dsv {
 namespace {
 
-#ifndef DSV_FWD64_MIN_BLOCKS
-#define DSV_FWD64_MIN_BLOCKS 2
-#endif
-
 constexpr int kChunk = 128;
-constexpr int kStages = 2;  // one producer group (64 threads) per stage
-constexpr int kThreads = 288;
+constexpr int kThreads = 192;
 constexpr float kStaleLimit = 8.f;  // log2 units
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kPollLimit = 1u << 28;
 
 // TMEM columns
 constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kColL = 192, kTmemCols = 256;
 
-template <int D>
+template <int D, int NST>
 struct Smem {
   static constexpr int BLK = D / 64;                 // 64-element column blocks
   static constexpr int Q_BYTES = BLK * 64 * 128;
@@ -49,14 +47,16 @@ struct Smem {
   static constexpr int P_BYTES = kChunk * 128;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + kStages * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + kStages * KV_BYTES;
+  static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + NST * KV_BYTES;
   static constexpr int TOTAL = OFF_P + 2 * P_BYTES;
 };
 
+template <int NST>
 struct Bars {
-  uint64_t full[kStages];   // producers -> MMA / softmax: K, V (and Q) of a stage landed
-  uint64_t empty[kStages];  // MMA commit: the PV product that last read a stage is done
+  uint64_t q_full;          // TMA: the Q tile landed
+  uint64_t full[NST];       // TMA: K and V of a stage landed
+  uint64_t empty[NST];      // MMA commit: the PV product that last read a stage is done
   uint64_t s_full[2];       // MMA commit: S^T in TMEM buffer b is ready
   uint64_t s_empty[2];      // softmax: S^T buffer b has been read
   uint64_t p_full[2];       // softmax: P^T tile b written
@@ -75,18 +75,39 @@ DSV_DEVICE bool named_sync_or(bool v) {
   return r != 0;
 }
 
+DSV_DEVICE void expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Four rows (r0..r3) x 64 columns starting at column x of a 2-D bf16 tensor map, into four
+// consecutive 128-byte rows of shared memory (swizzled by address), completing on `bar`.
+DSV_DEVICE void gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
 // Column reduction over the 128 softmax threads of 64 per-thread values (v[c] is this
 // thread's value for column c).  Fixed order, so the result is deterministic.  Returns
 // through red[64] in shared memory (visible after the trailing barrier).
 template <bool MAX>
 DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* red, int warp, int lane) {
-  // butterfly halving: after the step with mask m each lane keeps half of its columns
   float cur[64];
 #pragma unroll
   for (int i = 0; i < 64; ++i) cur[i] = v[i];
   int n = 64;
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
+  for (int m = 16; m >= 1; m >>= 1) {  // after the step with mask m each lane keeps half its columns
     const bool upper = (lane & m) != 0;
     n >>= 1;
 #pragma unroll
@@ -99,8 +120,7 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
       }
     }
   }
-  // lane holds columns 2 lane, 2 lane + 1 (reduced over its warp)
-  red_w[warp * 64 + 2 * lane] = cur[0];
+  red_w[warp * 64 + 2 * lane] = cur[0];  // lane holds columns 2 lane and 2 lane + 1
   red_w[warp * 64 + 2 * lane + 1] = cur[1];
   named_sync_softmax();
   if (warp * 32 + lane < 64) {
@@ -113,17 +133,17 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
   named_sync_softmax();
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, D == 64 ? DSV_FWD64_MIN_BLOCKS : 1)
-sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
-                     const int32_t* __restrict__ idx, bf16* __restrict__ o, float* __restrict__ lse, int64_t N,
-                     int64_t NB, int64_t kk, float scale_log2, unsigned int* status) {
-  using S = Smem<D>;
+template <int D, int NST, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ idx, bf16* __restrict__ o,
+                     float* __restrict__ lse, int64_t N, int64_t NB, int64_t kk, int32_t oob_row, float scale_log2,
+                     unsigned int* status) {
+  using S = Smem<D, NST>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) Bars bars;
+  __shared__ __align__(8) Bars<NST> bars;
   __shared__ uint32_t tmem_base_s;
   __shared__ float m_s[64], alpha_s[64], red_w[4 * 64], red_s[64];
-  __shared__ uint8_t valid_s[kStages][kChunk];
   __shared__ int flag_s[2];
   __shared__ int fail_s;
 
@@ -132,15 +152,23 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V, sP = sbase + S::OFF_P;
+  const int32_t* ib = idx + (bh * NB + blk) * kk;
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
+  // the 128-byte swizzle of TMA and of the MMA descriptors both follow address bits, so the
+  // tiles must start on 1024-byte boundaries
+  if (sbase & 1023u) {
+    if (tid == 0) flag_status(status, kStatusTimeout);
+    return;
+  }
   if (warp == 0) {
     tc::tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(bar(bars.full[s]), 64);
+    tc::mbar_init(bar(bars.q_full), 1);
+    for (int s = 0; s < NST; ++s) {
+      tc::mbar_init(bar(bars.full[s]), 1);
       tc::mbar_init(bar(bars.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -160,110 +188,98 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  if (warp >= 4 && warp < 8) {
-    // ================================================================ producers
-    // Two groups of 64 threads; group g owns stage g and the chunks c with c % 2 == g, so
-    // each group can block on its own copies while the other group's are in flight.
-    const int grp = (warp - 4) >> 1;
-    const int t = tid - 128 - grp * 64;
-    const bf16* qb = q + (bh * N + blk * 64) * D;
-    const bf16* kh = k + bh * N * D;
-    const bf16* vh = v + bh * N * D;
-    const int32_t* ib = idx + (bh * NB + blk) * kk;
-    if (grp == 0) {
+  if (warp == 4) {
+    // ================================================================ producer (TMA gathers)
+    const int32_t row_base = static_cast<int32_t>(bh * N);
+    if (lane == 0) expect_tx(bar(bars.q_full), 64 * D * 2);
+    __syncwarp();
+    if (lane < 16) {
+      const int32_t r = row_base + static_cast<int32_t>(blk * 64) + 4 * lane;
 #pragma unroll
-      for (int e = 0; e < D; e += 8)
-        cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(t, e & 63), qb + t * D + e, true);
+      for (int cb = 0; cb < D / 64; ++cb)
+        gather4(sQ + cb * (64 * 128) + lane * 512, &tmQ, cb * 64, r, r + 1, r + 2, r + 3, bar(bars.q_full));
     }
     bool ok_run = true;
-    for (int c = grp; c < nchunks; c += kStages) {
-      const int st = grp;
-      if (c >= kStages && !tc::mbar_wait(bar(bars.empty[st]), ((c / kStages) - 1) & 1, kWaitLimit)) {
-        ok_run = false;
-        break;
-      }
-      const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
-      // this thread copies whole rows t and t + 64; both indices are loaded before any copy
-      int64_t j[2];
+    for (int c = 0; c < nchunks && ok_run; ++c) {
+      const int st = c % NST;
+      if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / NST) - 1) & 1, kWaitLimit);
+      ok_run = __all_sync(0xffffffffu, ok_run);
+      if (!ok_run) break;
+      int32_t rr[4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + t + 64 * h;
-        j[h] = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = t + 64 * h;
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + row;
-        const bool ok = j[h] >= 0 && j[h] < N;
-        valid_s[st][row] = ok;
+      for (int h = 0; h < 4; ++h) {
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + 4 * lane + h;
+        const int64_t j = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
+        const bool ok = j >= 0 && j < N;
         if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
-        const bf16* ks = kh + (ok ? j[h] : 0) * D;
-        const bf16* vs = vh + (ok ? j[h] : 0) * D;
-#pragma unroll
-        for (int e = 0; e < D; e += 8) {
-          const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
-          cp_async_16(dK + off, ks + e, ok);
-          cp_async_16(dV + off, vs + e, ok);
-        }
+        rr[h] = ok ? row_base + static_cast<int32_t>(j) : oob_row;
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      tc::fence_async_shared();
-      tc::mbar_arrive(bar(bars.full[st]));
+      if (lane == 0) expect_tx(bar(bars.full[st]), kChunk * D * 2 * 2);
+      __syncwarp();
+#pragma unroll
+      for (int cb = 0; cb < D / 64; ++cb) {
+        const uint32_t off = st * S::KV_BYTES + cb * (kChunk * 128) + lane * 512;
+        gather4(sK + off, &tmK, cb * 64, rr[0], rr[1], rr[2], rr[3], bar(bars.full[st]));
+        gather4(sV + off, &tmV, cb * 64, rr[0], rr[1], rr[2], rr[3], bar(bars.full[st]));
+      }
     }
-    cp_async_wait<0>();
-    if (!ok_run) atomicOr(&fail_s, 1);
-  } else if (warp == 8) {
+    if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
+  } else if (warp == 5) {
     // ================================================================ MMA issue (one thread)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16(D, 64, 1, 1);
-      bool ok_run = true;
-      for (int c = 0; c <= nchunks && ok_run; ++c) {
-        if (c < nchunks) {
-          const int st = c % kStages, b = c & 1;
-          ok_run = tc::mbar_wait(bar(bars.full[st]), (c / kStages) & 1, kWaitLimit);
-          if (ok_run && c >= 2) ok_run = tc::mbar_wait(bar(bars.s_empty[b]), ((c - 2) >> 1) & 1, kWaitLimit);
-          if (!ok_run) break;
+      bool ok_run = tc::mbar_wait(bar(bars.q_full), 0, kWaitLimit);
+      int cs = 0, cp = 0;
+      uint32_t idle = 0;
+      while (ok_run && cp < nchunks) {
+        if (cp < cs && mbar_test(bar(bars.p_full[cp & 1]), (cp >> 1) & 1)) {
+          // PV(cp): O^T += V_c^T P^T
           tc::tc_fence_after();
-          const uint32_t aK = sK + st * S::KV_BYTES;
-#pragma unroll
-          for (int j = 0; j < D / 16; ++j) {
-            const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
-            const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
-            tc::mma_ss(tmem + (b ? kColS1 : kColS0), tc::smem_desc(aK + off_a, 16, 1024),
-                       tc::smem_desc(sQ + off_b, 16, 1024), idS, j > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(bar(bars.s_full[b]));
-        }
-        if (c >= 1) {
-          const int cp = c - 1, st = cp % kStages, b = cp & 1;
-          ok_run = tc::mbar_wait(bar(bars.p_full[b]), (cp >> 1) & 1, kWaitLimit);
-          if (!ok_run) break;
-          tc::tc_fence_after();
-          const uint32_t aV = sV + st * S::KV_BYTES, bP = sP + b * S::P_BYTES;
+          const uint32_t aV = sV + (cp % NST) * S::KV_BYTES, bP = sP + (cp & 1) * S::P_BYTES;
 #pragma unroll
           for (int j = 0; j < kChunk / 16; ++j)
             tc::mma_ss(tmem + kColO, tc::smem_desc(aV + j * 2048, kChunk * 128, 1024),
                        tc::smem_desc(bP + j * 2048, 8192, 1024), idO, (cp > 0 || j > 0) ? 1u : 0u);
-          tc::mma_commit(bar(bars.pv_done[b]));
-          tc::mma_commit(bar(bars.empty[st]));
+          tc::mma_commit(bar(bars.pv_done[cp & 1]));
+          tc::mma_commit(bar(bars.empty[cp % NST]));
           if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
+          ++cp;
+          idle = 0;
+        } else if (cs < nchunks && mbar_test(bar(bars.full[cs % NST]), (cs / NST) & 1) &&
+                   (cs < 2 || mbar_test(bar(bars.s_empty[cs & 1]), ((cs - 2) >> 1) & 1))) {
+          // S(cs): S^T = K_c Q^T
+          tc::tc_fence_after();
+          const uint32_t aK = sK + (cs % NST) * S::KV_BYTES;
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
+            const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
+            tc::mma_ss(tmem + ((cs & 1) ? kColS1 : kColS0), tc::smem_desc(aK + off_a, 16, 1024),
+                       tc::smem_desc(sQ + off_b, 16, 1024), idS, j > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bars.s_full[cs & 1]));
+          ++cs;
+          idle = 0;
+        } else if (++idle > kPollLimit) {
+          ok_run = false;
         }
       }
       if (!ok_run) atomicOr(&fail_s, 1);
     }
   } else {
     // ================================================================ softmax (threads 0..127)
-    const int t = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     // Every softmax thread runs every iteration and reaches every named barrier, also after
     // a timed-out wait (later waits are then skipped and the results are discarded).
+    const int t = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok_run = true;
     for (int c = 0; c < nchunks; ++c) {
-      const int st = c % kStages, b = c & 1;
+      const int b = c & 1;
+      const int64_t slot = static_cast<int64_t>(c) * kChunk + t;
+      const int64_t jkey = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
+      const bool valid = jkey >= 0 && jkey < N;
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full[b]), (c >> 1) & 1, kWaitLimit);
-      ok_run = ok_run && tc::mbar_wait(bar(bars.full[st]), (c / kStages) & 1, kWaitLimit);
       tc::tc_fence_after();
       float x[64];
       {
@@ -278,7 +294,6 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty[b]));
-      const bool valid = (static_cast<int64_t>(c) * kChunk + t < kk) && valid_s[st][t];
       bool over = false;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
@@ -361,19 +376,19 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       tc::tc_fence_after();
       float lsum[64];
       {
-        uint32_t r[16];
+        uint32_t r[4][16];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          tc::tmem_ld16(tmem + lane_base + kColL + h * 16, r);
-          tc::tmem_wait_ld();
+        for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + kColL + h * 16, r[h]);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) lsum[h * 16 + i] = __uint_as_float(r[i]);
-        }
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lsum[h * 16 + i] = __uint_as_float(r[h][i]);
       }
       column_reduce<false>(lsum, red_w, red_s, warp, lane);
       // O^T lane -> head dim: identity for d = 128; for d = 64 (M = 64) rows sit 16 per lane quadrant
       const int dim = D == 128 ? t : ((lane < 16) ? warp * 16 + lane : -1);
-      bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D], K stage 0 is free now
+      bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D]: K stage 0 is free now
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t r[16];
@@ -407,15 +422,57 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   }
 }
 
-template <int D>
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// [rows][D] bf16 tensor, boxes of 64 columns x 1 row (the gather4 unit), 128-byte swizzle.
+bool row_map(CUtensorMap* m, const void* base, int64_t rows, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#ifndef DSV_FWD64_STAGES
+#define DSV_FWD64_STAGES 2
+#endif
+#ifndef DSV_FWD64_MIN_BLOCKS
+#define DSV_FWD64_MIN_BLOCKS 2
+#endif
+
+template <int D, int NST, int MINB>
 cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
-  const int smem = Smem<D>::TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(sparse_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int64_t rows = p.BH * p.N;
+  alignas(64) CUtensorMap mq, mk, mv;
+  if (!row_map(&mq, p.q, rows, D) || !row_map(&mk, p.k, rows, D) || !row_map(&mv, p.v, rows, D))
+    return cudaErrorInvalidValue;
+  const int smem = Smem<D, NST>::TOTAL;
+  auto kern = sparse_fwd_tc_kernel<D, NST, MINB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
   ProfScope prof("sparse_fwd", stream);
-  sparse_fwd_tc_kernel<D><<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.o, p.lse, p.N, p.NB, p.topk,
-                                                             p.scale * kLog2e, p.status);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p.idx, p.o, p.lse, p.N, p.NB, p.topk,
+                                         static_cast<int32_t>(rows), p.scale * kLog2e, p.status);
   return cudaGetLastError();
 }
 
@@ -423,8 +480,8 @@ cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_sparse_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   switch (p.d) {
-    case 64: return launch_d<64>(p, stream);
-    case 128: return launch_d<128>(p, stream);
+    case 64: return launch_d<64, DSV_FWD64_STAGES, DSV_FWD64_MIN_BLOCKS>(p, stream);
+    case 128: return launch_d<128, 2, 1>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
