@@ -200,20 +200,31 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         gather4(sQ + cb * (64 * 128) + lane * 512, &tmQ, cb * 64, r, r + 1, r + 2, r + 3, bar(bars.q_full));
     }
     bool ok_run = true;
+    // key indices of chunk c + 1 are loaded while chunk c's stage is awaited and issued
+    int32_t nxt[4];
+    auto load_rows = [&](int c, int32_t (&rr)[4]) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + 4 * lane + h;
+        rr[h] = (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
+      }
+    };
+    load_rows(0, nxt);
     for (int c = 0; c < nchunks && ok_run; ++c) {
       const int st = c % NST;
-      if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / NST) - 1) & 1, kWaitLimit);
-      ok_run = __all_sync(0xffffffffu, ok_run);
-      if (!ok_run) break;
       int32_t rr[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const int64_t slot = static_cast<int64_t>(c) * kChunk + 4 * lane + h;
-        const int64_t j = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
+        const int32_t j = nxt[h];
         const bool ok = j >= 0 && j < N;
         if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
-        rr[h] = ok ? row_base + static_cast<int32_t>(j) : oob_row;
+        rr[h] = ok ? row_base + j : oob_row;
       }
+      load_rows(c + 1, nxt);
+      if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / NST) - 1) & 1, kWaitLimit);
+      ok_run = __all_sync(0xffffffffu, ok_run);
+      if (!ok_run) break;
       if (lane == 0) expect_tx(bar(bars.full[st]), kChunk * D * 2 * 2);
       __syncwarp();
 #pragma unroll
@@ -261,8 +272,9 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           tc::mma_commit(bar(bars.s_full[cs & 1]));
           ++cs;
           idle = 0;
-        } else if (++idle > kPollLimit) {
-          ok_run = false;
+        } else {
+          if (++idle > kPollLimit) ok_run = false;
+          __nanosleep(32);  // nothing ready: yield issue slots to the softmax warps
         }
       }
       if (!ok_run) atomicOr(&fail_s, 1);
@@ -274,11 +286,14 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int t = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok_run = true;
+    int32_t jnext = t < kk ? __ldg(ib + t) : -1;  // this lane's key index, one chunk ahead
     for (int c = 0; c < nchunks; ++c) {
       const int b = c & 1;
-      const int64_t slot = static_cast<int64_t>(c) * kChunk + t;
-      const int64_t jkey = slot < kk ? static_cast<int64_t>(__ldg(ib + slot)) : -1;
-      const bool valid = jkey >= 0 && jkey < N;
+      const bool valid = jnext >= 0 && jnext < N;
+      {
+        const int64_t slot = static_cast<int64_t>(c + 1) * kChunk + t;
+        jnext = slot < kk ? __ldg(ib + slot) : -1;
+      }
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full[b]), (c >> 1) & 1, kWaitLimit);
       tc::tc_fence_after();
       float x[64];
