@@ -10,17 +10,16 @@
 //   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
 //              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16, one 128-byte
 //              row) to shared memory as the B operand of the PV product;
-//   warp 4     producer: gathers the chunk's K and V rows with TMA tile::gather4 (four rows
-//              per instruction, 128-byte swizzle) into a ring of stages; selected keys past
-//              k or out of range use an out-of-bounds row, which TMA fills with zeros;
+//   warp 4     producer: gathers the chunk's K and V rows with cp.async (16 bytes per
+//              copy, into 128-byte-swizzled tiles) into a ring of stages and lets the stage's
+//              mbarrier count the copies' completion (cp.async.mbarrier.arrive), so it never
+//              waits for its own copies; keys past k or out of range are zero-filled;
 //   warp 5     one thread issues every MMA as soon as its inputs are ready (it polls the
 //              stage, P and S barriers without blocking on any single one).
 // The running max m_q is kept STALE: a chunk only triggers the cross-thread column max and
 // an O/L rescale when one of its logits exceeds m_q by more than 8 (in log2 units; the
 // first chunk always does).  Otherwise P <= 2^8, and softmax is invariant to the
 // subtracted constant.  Row sums accumulate per key lane in TMEM and are reduced once.
-#include <cuda.h>
-
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -54,8 +53,7 @@ struct Smem {
 
 template <int NST>
 struct Bars {
-  uint64_t q_full;          // TMA: the Q tile landed
-  uint64_t full[NST];       // TMA: K and V of a stage landed
+  uint64_t full[NST];       // cp.async completion: K and V of a stage (and Q, with stage 0) landed
   uint64_t empty[NST];      // MMA commit: the PV product that last read a stage is done
   uint64_t s_full[2];       // MMA commit: S^T in TMEM buffer b is ready
   uint64_t s_empty[2];      // softmax: S^T buffer b has been read
@@ -75,9 +73,6 @@ DSV_DEVICE bool named_sync_or(bool v) {
   return r != 0;
 }
 
-DSV_DEVICE void expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-}
 DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -87,14 +82,9 @@ DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Four rows (r0..r3) x 64 columns starting at column x of a 2-D bf16 tensor map, into four
-// consecutive 128-byte rows of shared memory (swizzled by address), completing on `bar`.
-DSV_DEVICE void gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+// Arrive on `bar` once all cp.async copies this thread issued so far have landed.
+DSV_DEVICE void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
 // Column reduction over the 128 softmax threads of 64 per-thread values (v[c] is this
@@ -135,10 +125,9 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
 
 template <int D, int NST, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
-sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ idx, bf16* __restrict__ o,
-                     float* __restrict__ lse, int64_t N, int64_t NB, int64_t kk, int32_t oob_row, float scale_log2,
-                     unsigned int* status) {
+sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+                     const int32_t* __restrict__ idx, bf16* __restrict__ o, float* __restrict__ lse, int64_t N,
+                     int64_t NB, int64_t kk, float scale_log2, unsigned int* status) {
   using S = Smem<D, NST>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) Bars<NST> bars;
@@ -166,9 +155,8 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar(bars.q_full), 1);
     for (int s = 0; s < NST; ++s) {
-      tc::mbar_init(bar(bars.full[s]), 1);
+      tc::mbar_init(bar(bars.full[s]), 32);
       tc::mbar_init(bar(bars.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -189,58 +177,63 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
   const uint32_t tmem = tmem_base_s;
 
   if (warp == 4) {
-    // ================================================================ producer (TMA gathers)
-    const int32_t row_base = static_cast<int32_t>(bh * N);
-    if (lane == 0) expect_tx(bar(bars.q_full), 64 * D * 2);
-    __syncwarp();
-    if (lane < 16) {
-      const int32_t r = row_base + static_cast<int32_t>(blk * 64) + 4 * lane;
+    // ================================================================ producer (cp.async)
+    // lane l copies rows l, l + 32, l + 64, l + 96 of each chunk (whole rows, 16 bytes a copy)
+    const bf16* qb = q + (bh * N + blk * 64) * D;
+    const bf16* kh = k + bh * N * D;
+    const bf16* vh = v + bh * N * D;
 #pragma unroll
-      for (int cb = 0; cb < D / 64; ++cb)
-        gather4(sQ + cb * (64 * 128) + lane * 512, &tmQ, cb * 64, r, r + 1, r + 2, r + 3, bar(bars.q_full));
+    for (int h = 0; h < 2; ++h) {
+      const int row = lane + 32 * h;
+#pragma unroll
+      for (int e = 0; e < D; e += 8)
+        cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
     }
     bool ok_run = true;
-    // key indices of chunk c + 1 are loaded while chunk c's stage is awaited and issued
     int32_t nxt[4];
     auto load_rows = [&](int c, int32_t (&rr)[4]) {
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + 4 * lane + h;
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
         rr[h] = (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
       }
     };
     load_rows(0, nxt);
     for (int c = 0; c < nchunks && ok_run; ++c) {
       const int st = c % NST;
-      int32_t rr[4];
+      int32_t cur[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + 4 * lane + h;
-        const int32_t j = nxt[h];
-        const bool ok = j >= 0 && j < N;
-        if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
-        rr[h] = ok ? row_base + j : oob_row;
-      }
+      for (int h = 0; h < 4; ++h) cur[h] = nxt[h];
       load_rows(c + 1, nxt);
       if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / NST) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
-      if (lane == 0) expect_tx(bar(bars.full[st]), kChunk * D * 2 * 2);
-      __syncwarp();
+      const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
 #pragma unroll
-      for (int cb = 0; cb < D / 64; ++cb) {
-        const uint32_t off = st * S::KV_BYTES + cb * (kChunk * 128) + lane * 512;
-        gather4(sK + off, &tmK, cb * 64, rr[0], rr[1], rr[2], rr[3], bar(bars.full[st]));
-        gather4(sV + off, &tmV, cb * 64, rr[0], rr[1], rr[2], rr[3], bar(bars.full[st]));
+      for (int h = 0; h < 4; ++h) {
+        const int row = lane + 32 * h;
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + row;
+        const bool ok = cur[h] >= 0 && cur[h] < N;
+        if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
+        const bf16* ks = kh + (ok ? static_cast<int64_t>(cur[h]) : 0) * D;
+        const bf16* vs = vh + (ok ? static_cast<int64_t>(cur[h]) : 0) * D;
+#pragma unroll
+        for (int e = 0; e < D; e += 8) {
+          const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
+          cp_async_16(dK + off, ks + e, ok);
+          cp_async_16(dV + off, vs + e, ok);
+        }
       }
+      cp_async_arrive(bar(bars.full[st]));
     }
+    cp_async_wait<0>();
     if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
   } else if (warp == 5) {
     // ================================================================ MMA issue (one thread)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16(D, 64, 1, 1);
-      bool ok_run = tc::mbar_wait(bar(bars.q_full), 0, kWaitLimit);
+      bool ok_run = true;
       int cs = 0, cp = 0;
       uint32_t idle = 0;
       while (ok_run && cp < nchunks) {
@@ -259,7 +252,9 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
           idle = 0;
         } else if (cs < nchunks && mbar_test(bar(bars.full[cs % NST]), (cs / NST) & 1) &&
                    (cs < 2 || mbar_test(bar(bars.s_empty[cs & 1]), ((cs - 2) >> 1) & 1))) {
-          // S(cs): S^T = K_c Q^T
+          // S(cs): S^T = K_c Q^T.  The stage was written with cp.async (generic proxy):
+          // order those writes before the tensor core's reads.
+          tc::fence_async_shared();
           tc::tc_fence_after();
           const uint32_t aK = sK + (cs % NST) * S::KV_BYTES;
 #pragma unroll
@@ -438,35 +433,6 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// [rows][D] bf16 tensor, boxes of 64 columns x 1 row (the gather4 unit), 128-byte swizzle.
-bool row_map(CUtensorMap* m, const void* base, int64_t rows, int D) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 #ifndef DSV_FWD64_STAGES
 #define DSV_FWD64_STAGES 2
 #endif
@@ -476,18 +442,14 @@ bool row_map(CUtensorMap* m, const void* base, int64_t rows, int D) {
 
 template <int D, int NST, int MINB>
 cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
-  const int64_t rows = p.BH * p.N;
-  alignas(64) CUtensorMap mq, mk, mv;
-  if (!row_map(&mq, p.q, rows, D) || !row_map(&mk, p.k, rows, D) || !row_map(&mv, p.v, rows, D))
-    return cudaErrorInvalidValue;
   const int smem = Smem<D, NST>::TOTAL;
   auto kern = sparse_fwd_tc_kernel<D, NST, MINB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
   ProfScope prof("sparse_fwd", stream);
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p.idx, p.o, p.lse, p.N, p.NB, p.topk,
-                                         static_cast<int32_t>(rows), p.scale * kLog2e, p.status);
+  kern<<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.o, p.lse, p.N, p.NB, p.topk, p.scale * kLog2e,
+                                         p.status);
   return cudaGetLastError();
 }
 
