@@ -291,30 +291,44 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       }
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full[b]), (c >> 1) & 1, kWaitLimit);
       tc::tc_fence_after();
-      float x[64];
+      // ---- one pass over the S^T row: probabilities against the stale max, and the vote on
+      // "some logit exceeds the stale max by more than 8" (the S buffer is released after it)
+      const uint32_t s_col = tmem + lane_base + (b ? kColS1 : kColS0);
+      bool over = false;
+      float p[64];
       {
         uint32_t r[4][16];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + (b ? kColS1 : kColS0) + h * 16, r[h]);
+        for (int h = 0; h < 4; ++h) tc::tmem_ld16(s_col + h * 16, r[h]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+        for (int i4 = 0; i4 < 16; ++i4) {
+          const float4 m4 = reinterpret_cast<const float4*>(m_s)[i4];
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[h * 16 + i] = __uint_as_float(r[h][i]);
+          for (int u = 0; u < 4; ++u) {
+            const int i = i4 * 4 + u;
+            const float dlt = __uint_as_float(r[i >> 4][i & 15]) * scale_log2 - mm[u];
+            over |= dlt > kStaleLimit;
+            p[i] = valid ? fast_exp2(dlt) : 0.f;
+          }
+        }
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(bar(bars.s_empty[b]));
-      bool over = false;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        x[i] = valid ? x[i] * scale_log2 : -CUDART_INF_F;
-        over |= x[i] - m_s[i] > kStaleLimit;
-      }
+      over &= valid;
       if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(&flag_s[c & 1], 1);
       if (t == 0) flag_s[(c + 1) & 1] = 0;
       named_sync_softmax();
       if (flag_s[c & 1]) {
-        // ---- new running max for this chunk; rescale O and L
+        // ---- new running max for this chunk; rescale O and L; redo the probabilities
+        float x[64];
+        {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) tc::tmem_ld16(s_col + h * 16, r[h]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) x[i] = valid ? __uint_as_float(r[i >> 4][i & 15]) * scale_log2 : -CUDART_INF_F;
+        }
         column_reduce<true>(x, red_w, red_s, warp, lane);
         if (t < 64) {
           const float mo = m_s[t];
@@ -341,12 +355,13 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           }
           tc::tmem_wait_st();
         }
-      }
-      // ---- P^T row of this key: exp2(x - m), into the B tile (64 queries = one 128-byte row)
-      if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[b]), ((c - 2) >> 1) & 1, kWaitLimit);
-      float (&p)[64] = x;  // probabilities overwrite the logits
 #pragma unroll
-      for (int i = 0; i < 64; ++i) p[i] = x[i] == -CUDART_INF_F ? 0.f : fast_exp2(x[i] - m_s[i]);
+        for (int i = 0; i < 64; ++i) p[i] = x[i] == -CUDART_INF_F ? 0.f : fast_exp2(x[i] - m_s[i]);
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(bars.s_empty[b]));
+      // ---- P^T row of this key into the B tile (64 queries = one 128-byte row)
+      if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[b]), ((c - 2) >> 1) & 1, kWaitLimit);
       const uint32_t prow = sP + b * S::P_BYTES + t * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
