@@ -210,19 +210,24 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       if (!ok_run) break;
       const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int row = lane + 32 * h;
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + row;
-        const bool ok = cur[h] >= 0 && cur[h] < N;
-        if (slot < kk && !ok) flag_status(status, kStatusBadIndex);
-        const bf16* ks = kh + (ok ? static_cast<int64_t>(cur[h]) : 0) * D;
-        const bf16* vs = vh + (ok ? static_cast<int64_t>(cur[h]) : 0) * D;
+      for (int h = 0; h < 4; ++h) {  // validity of the rows this lane holds the index of
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
+        if (slot < kk && !(cur[h] >= 0 && cur[h] < N)) flag_status(status, kStatusBadIndex);
+      }
+      // each warp-wide copy covers whole rows: LPR lanes per row (8 for d = 64, 16 for d = 128),
+      // so every 32-byte sector is fetched once; a row's index comes from the lane holding it
+      constexpr int LPR = D / 8, RPI = 32 / LPR;
+      const int sub = lane % LPR, rsub = lane / LPR;
 #pragma unroll
-        for (int e = 0; e < D; e += 8) {
-          const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
-          cp_async_16(dK + off, ks + e, ok);
-          cp_async_16(dV + off, vs + e, ok);
-        }
+      for (int it = 0; it < kChunk / RPI; ++it) {
+        const int row = it * RPI + rsub;
+        const int32_t j = __shfl_sync(0xffffffffu, cur[(it * RPI) >> 5], row & 31);
+        const bool ok = j >= 0 && j < N;
+        const int e = sub * 8;
+        const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
+        const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
+        cp_async_16(dK + off, kh + src, ok);
+        cp_async_16(dV + off, vh + src, ok);
       }
       cp_async_arrive(bar(bars.full[st]));
     }
