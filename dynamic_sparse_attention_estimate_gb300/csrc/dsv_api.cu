@@ -100,7 +100,7 @@ Carve carve(const dsv_dims* d, int64_t nh, int64_t nblk, bool sub) {
   c.colpre = o;  o += up(sizeof(uint32_t) * nh * W32 * d->N);
   c.count = o;   o += up(sizeof(uint32_t) * nh * d->N);
   c.offsets = o; o += up(sizeof(int64_t) * nh * d->N);
-  c.partial = o; o += up(sizeof(float) * 2 * d->d * nh * nblk * d->k);
+  c.partial = o; o += up(sizeof(uint16_t) * 2 * d->d * nh * nblk * d->k);   // bf16 rows
   c.acc = o;     o += sub ? up(sizeof(float) * 2 * d->d * d->N) : 0;
   c.total = o;
   return c;
@@ -252,7 +252,7 @@ size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims) {
 size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims) {
   if (check_dims(dims, true, false) != DSV_OK) return 0;
   // the largest plan whose partial rows stay within the recommended budget
-  const size_t per_block = sizeof(float) * 2 * dims->d * dims->k;
+  const size_t per_block = sizeof(uint16_t) * 2 * dims->d * dims->k;
   const int64_t BH = dims->B * dims->H, NB = dims->N / 64;
   const int64_t blocks = static_cast<int64_t>(kRecommendedPartialBytes / (per_block ? per_block : 1));
   WavePlan w;
@@ -314,7 +314,7 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
   p.colpre = reinterpret_cast<uint32_t*>(base + c.colpre);
   p.count = reinterpret_cast<uint32_t*>(base + c.count);
   p.offsets = reinterpret_cast<int64_t*>(base + c.offsets);
-  p.partial = reinterpret_cast<float*>(base + c.partial);
+  p.partial = reinterpret_cast<dsv::bf16*>(base + c.partial);
   p.acc = plan.sub ? reinterpret_cast<float*>(base + c.acc) : nullptr;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -1,0 +1,430 @@
+// Sparse attention backward, main kernel, on the tcgen05 tensor cores (training needs the
+// backward: DSV page 1, technical summary section 2A, stage 2).
+//
+// One CTA = one query block (64 queries).  For every chunk of 128 selected keys, with keys
+// on the MMA's M dimension:
+//     S^T  = K_c . Q^T            dP^T = V_c . dO^T           (M=128, N=64,  K=d)
+//     P = exp2(S scale log2e - LSE2),  dS = P (dP - D)         (compute warps, fp32)
+//     dV_c = P^T . dO             dK_c = dS^T . Q             (M=128, N=d,   K=64)
+//     dQ^T += K_c^T . dS^T                                    (M=d,   N=64,  K=128)
+// dQ accumulates in tensor memory (TMEM) across chunks; dV_c and dK_c (one row per key) go
+// out as bf16 partial rows to their key-major positions in the workspace, where a separate
+// kernel sums every key's rows in a fixed order (deterministic, no float atomics).
+// P and dS are written once to shared memory as bf16 128-byte rows (one per key); the same
+// bytes are the K-major A operand of dV_c / dK_c and the MN-major B operand of dQ^T.
+// Roles (320 threads): warps 0-3 compute P and dS (thread = key lane of S^T / dP^T);
+// warps 4-7 read dV_c / dK_c out of TMEM and store the partial rows (and dQ at the end);
+// warp 8 gathers Q, dO and the chunks' K and V rows with cp.async; one thread of warp 9
+// issues the MMAs as soon as their inputs are ready.  Every wait is bounded.
+#include "dsv_common.cuh"
+#include "dsv_internal.h"
+#include "dsv_tc.cuh"
+
+namespace dsv {
+namespace {
+
+constexpr int kChunk = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 320;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kPollLimit = 1u << 28;
+
+// TMEM columns: S^T, dP^T (64 each), dQ^T (64), dV_c, dK_c (d each)
+constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 192, kTmemCols = 512;
+
+template <int D>
+struct Sm {
+  static constexpr int BLK = D / 64;
+  static constexpr int T64 = BLK * 64 * 128;          // a [64 rows][D] tile
+  static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
+  static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16
+  static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + kStages * KV,
+                       OFF_P = OFF_V + kStages * KV, OFF_DS = OFF_P + P, TOTAL = OFF_DS + P;
+};
+
+struct Bars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full, s_empty;        // S^T, dP^T in TMEM ready / read
+  uint64_t p_full, pds_empty;      // P, dS tiles written / no longer read by any MMA
+  uint64_t dvk_full, dvk_empty;    // dV_c, dK_c in TMEM ready / read
+  uint64_t dq_full;                // last dQ^T update done
+};
+
+DSV_DEVICE void sync_group(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
+DSV_DEVICE bool sync_group_or(int id, bool v) {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %2, 0;\n bar.red.or.pred q, %1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+               : "=r"(r)
+               : "r"(id), "r"(static_cast<uint32_t>(v))
+               : "memory");
+  return r != 0;
+}
+DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+DSV_DEVICE void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Copy `nrows` rows of D bf16 (rows given by row_of(i)) into a 128-byte-swizzled tile of
+// `tile_rows` rows; LPR lanes per row so each warp-wide copy moves whole rows.
+template <int D, typename RowFn>
+DSV_DEVICE void copy_rows(uint32_t dst, int tile_rows, int nrows, const bf16* base, RowFn row_of, int lane) {
+  constexpr int LPR = D / 8, RPI = 32 / LPR;
+  const int sub = lane % LPR, rsub = lane / LPR;
+  for (int r0 = 0; r0 < nrows; r0 += RPI) {
+    const int row = r0 + rsub;
+    const int64_t src_row = row_of(row);
+    const int e = sub * 8;
+    cp_async_16(dst + (e >> 6) * (tile_rows * 128) + tc::sw128(row, e & 63), base + (src_row < 0 ? 0 : src_row) * D + e,
+                src_row >= 0);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32, float scale_log2) {
+  using S = Sm<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ __align__(16) float lse2_s[64];
+  __shared__ __align__(16) float delta_s[64];
+  __shared__ int fail_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t N = p.N, NB = p.NB, kk = p.topk;
+  const int64_t hs = blockIdx.x / nblk, lb = blockIdx.x % nblk;
+  const int64_t bh = bh0 + hs, blk = blk0 + lb;
+  const int64_t row0 = bh * N + blk * 64;
+  const int32_t* ib = p.idx + (bh * NB + blk) * kk;
+  const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + S::OFF_Q, sDO = sbase + S::OFF_DO, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V;
+  const uint32_t sP = sbase + S::OFF_P, sDS = sbase + S::OFF_DS;
+  auto bar = [](uint64_t& b) { return smem_u32(&b); };
+
+  if (sbase & 1023u) {  // swizzled tiles need 1024-byte alignment
+    if (tid == 0) flag_status(p.status, kStatusTimeout);
+    return;
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar(bars.full[s]), 32);
+      tc::mbar_init(bar(bars.empty[s]), 1);
+    }
+    tc::mbar_init(bar(bars.s_full), 1);
+    tc::mbar_init(bar(bars.s_empty), 128);
+    tc::mbar_init(bar(bars.p_full), 128);
+    tc::mbar_init(bar(bars.pds_empty), 1);
+    tc::mbar_init(bar(bars.dvk_full), 1);
+    tc::mbar_init(bar(bars.dvk_empty), 128);
+    tc::mbar_init(bar(bars.dq_full), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    fail_s = 0;
+  }
+  // D_i = dO_i . O_i and LSE in base 2 (compute warps: two threads per query row)
+  if (warp < 4) {
+    const int row = tid >> 1, half = tid & 1;
+    const bf16* dor = p.d_o + (row0 + row) * D + half * (D / 2);
+    const bf16* orow = p.o + (row0 + row) * D + half * (D / 2);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 2; c += 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(dor + c);
+      const uint4 b = *reinterpret_cast<const uint4*>(orow + c);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc += bf16_lo(av[u]) * bf16_lo(bv[u]) + bf16_hi(av[u]) * bf16_hi(bv[u]);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (half == 0) {
+      delta_s[row] = acc;
+      lse2_s[row] = p.lse[row0 + row] * kLog2e;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 8) {
+    // ================================================================ producer (cp.async)
+    const bf16* kh = p.k + bh * N * D;
+    const bf16* vh = p.v + bh * N * D;
+    copy_rows<D>(sQ, 64, 64, p.q, [&](int r) -> int64_t { return row0 + r; }, lane);
+    copy_rows<D>(sDO, 64, 64, p.d_o, [&](int r) -> int64_t { return row0 + r; }, lane);
+    int32_t nxt[4];
+    auto load_rows = [&](int c, int32_t (&rr)[4]) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
+        rr[h] = (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
+      }
+    };
+    load_rows(0, nxt);
+    bool ok_run = true;
+    for (int c = 0; c < nchunks && ok_run; ++c) {
+      const int st = c % kStages;
+      int32_t cur[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) cur[h] = nxt[h];
+      load_rows(c + 1, nxt);
+      if (c >= kStages) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / kStages) - 1) & 1, kWaitLimit);
+      ok_run = __all_sync(0xffffffffu, ok_run);
+      if (!ok_run) break;
+      constexpr int LPR = D / 8, RPI = 32 / LPR;
+      const int sub = lane % LPR, rsub = lane / LPR;
+      const uint32_t dK = sK + st * S::KV, dV = sV + st * S::KV;
+#pragma unroll
+      for (int it = 0; it < kChunk / RPI; ++it) {
+        const int row = it * RPI + rsub;
+        const int32_t j = __shfl_sync(0xffffffffu, cur[(it * RPI) >> 5], row & 31);
+        const bool ok = j >= 0 && j < N;
+        const int e = sub * 8;
+        const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
+        const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
+        cp_async_16(dK + off, kh + src, ok);
+        cp_async_16(dV + off, vh + src, ok);
+      }
+      cp_async_arrive(bar(bars.full[st]));
+    }
+    cp_async_wait<0>();
+    if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
+  } else if (warp == 9) {
+    // ================================================================ MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);   // S^T, dP^T
+      constexpr uint32_t idKV = tc::idesc_bf16(128, D, 0, 1);   // dV_c, dK_c: A K-major, B MN-major
+      constexpr uint32_t idQ = tc::idesc_bf16(D, 64, 1, 1);     // dQ^T: A, B MN-major
+      bool ok_run = true;
+      int cs = 0, cg = 0;
+      uint32_t idle = 0;
+      while (ok_run && cg < nchunks) {
+        if (cg < cs && mbar_test(bar(bars.p_full), cg & 1) &&
+            (cg == 0 || mbar_test(bar(bars.dvk_empty), (cg - 1) & 1))) {
+          tc::tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // K = 64 queries
+            tc::mma_ss(tmem + kColDV, tc::smem_desc(sP + j * 32, 16, 1024),
+                       tc::smem_desc(sDO + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
+            tc::mma_ss(tmem + kColDV + D, tc::smem_desc(sDS + j * 32, 16, 1024),
+                       tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bars.dvk_full));
+          const uint32_t aK = sK + (cg % kStages) * S::KV;
+#pragma unroll
+          for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
+            tc::mma_ss(tmem + kColDQ, tc::smem_desc(aK + j * 2048, kChunk * 128, 1024),
+                       tc::smem_desc(sDS + j * 2048, 8192, 1024), idQ, (cg > 0 || j > 0) ? 1u : 0u);
+          tc::mma_commit(bar(bars.pds_empty));
+          tc::mma_commit(bar(bars.empty[cg % kStages]));
+          if (cg == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
+          ++cg;
+          idle = 0;
+        } else if (cs < nchunks && cs <= cg && mbar_test(bar(bars.full[cs % kStages]), (cs / kStages) & 1) &&
+                   (cs == 0 || mbar_test(bar(bars.s_empty), (cs - 1) & 1))) {
+          tc::fence_async_shared();  // the stage was written with cp.async (generic proxy)
+          tc::tc_fence_after();
+          const uint32_t aK = sK + (cs % kStages) * S::KV, aV = sV + (cs % kStages) * S::KV;
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
+            const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
+            tc::mma_ss(tmem + kColS, tc::smem_desc(aK + off_a, 16, 1024), tc::smem_desc(sQ + off_b, 16, 1024), idS,
+                       j > 0 ? 1u : 0u);
+            tc::mma_ss(tmem + kColDP, tc::smem_desc(aV + off_a, 16, 1024), tc::smem_desc(sDO + off_b, 16, 1024), idS,
+                       j > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bars.s_full));
+          ++cs;
+          idle = 0;
+        } else {
+          if (++idle > kPollLimit) ok_run = false;
+          __nanosleep(32);
+        }
+      }
+      if (!ok_run) atomicOr(&fail_s, 1);
+    }
+  } else if (warp < 4) {
+    // ================================================================ P and dS (threads 0..127)
+    const int t = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok_run = true;
+    int32_t jnext = t < kk ? __ldg(ib + t) : -1;
+    for (int c = 0; c < nchunks; ++c) {
+      const bool valid = jnext >= 0 && jnext < N;
+      {
+        const int64_t slot = static_cast<int64_t>(c + 1) * kChunk + t;
+        jnext = slot < kk ? __ldg(ib + slot) : -1;
+      }
+      ok_run = ok_run && tc::mbar_wait(bar(bars.s_full), c & 1, kWaitLimit);
+      tc::tc_fence_after();
+      uint32_t sr[4][16], dr[4][16];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        tc::tmem_ld16(tmem + lane_base + kColS + h * 16, sr[h]);
+        tc::tmem_ld16(tmem + lane_base + kColDP + h * 16, dr[h]);
+      }
+      tc::tmem_wait_ld();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(bars.s_empty));
+      uint32_t pw[32], dw[32];  // packed bf16 pairs of P and dS
+#pragma unroll
+      for (int i4 = 0; i4 < 16; ++i4) {
+        const float4 l4 = reinterpret_cast<const float4*>(lse2_s)[i4];
+        const float4 d4 = reinterpret_cast<const float4*>(delta_s)[i4];
+        const float ll[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], dv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i4 * 4 + u;
+          const float sv = __uint_as_float(sr[i >> 4][i & 15]);
+          const float dpv = __uint_as_float(dr[i >> 4][i & 15]);
+          pv[u] = valid ? fast_exp2(sv * scale_log2 - ll[u]) : 0.f;
+          dv[u] = pv[u] * (dpv - dd[u]);
+        }
+        pw[i4 * 2] = pack_bf16x2(pv[0], pv[1]);
+        pw[i4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+        dw[i4 * 2] = pack_bf16x2(dv[0], dv[1]);
+        dw[i4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
+      }
+      if (c >= 1) ok_run = ok_run && tc::mbar_wait(bar(bars.pds_empty), (c - 1) & 1, kWaitLimit);
+      const uint32_t prow = sP + t * 128, drow = sDS + t * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = ((ch ^ t) & 7) << 4;
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + off), "r"(pw[ch * 4]), "r"(pw[ch * 4 + 1]),
+                     "r"(pw[ch * 4 + 2]), "r"(pw[ch * 4 + 3]));
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(drow + off), "r"(dw[ch * 4]), "r"(dw[ch * 4 + 1]),
+                     "r"(dw[ch * 4 + 2]), "r"(dw[ch * 4 + 3]));
+      }
+      tc::fence_async_shared();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(bars.p_full));
+    }
+    if (!ok_run) atomicOr(&fail_s, 1);
+  } else {
+    // ================================================================ partial rows and dQ (threads 128..255)
+    const int te = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t* cbits = p.colbits + (hs * W32 + (lb >> 5)) * N;
+    const uint32_t* cpre = p.colpre + (hs * W32 + (lb >> 5)) * N;
+    const int64_t* offs = p.offsets + hs * N;
+    const uint32_t lowmask = (1u << (lb & 31)) - 1u;
+    auto key_of = [&](int c) -> int32_t {
+      const int64_t slot = static_cast<int64_t>(c) * kChunk + te;
+      return (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
+    };
+    // a key's partial row: offsets[j] + (blocks of this wave before this one that selected j);
+    // the three loads are issued one chunk before the row is needed
+    struct PosParts {
+      int64_t off;
+      uint32_t pre, bits;
+      bool valid;
+    };
+    auto pos_load = [&](int32_t j) -> PosParts {
+      PosParts q{0, 0u, 0u, j >= 0 && j < N};
+      if (q.valid) {
+        q.off = offs[j];
+        q.pre = cpre[j];
+        q.bits = cbits[j];
+      }
+      return q;
+    };
+    PosParts pos_next = pos_load(key_of(0));
+    int32_t j_next2 = key_of(1);
+    bool ok_run = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int64_t pos = pos_next.valid ? pos_next.off + pos_next.pre + __popc(pos_next.bits & lowmask) : -1;
+      pos_next = pos_load(j_next2);
+      j_next2 = key_of(c + 2);
+      ok_run = ok_run && tc::mbar_wait(bar(bars.dvk_full), c & 1, kWaitLimit);
+      tc::tc_fence_after();
+      bf16* dst = pos >= 0 ? p.partial + pos * (2 * D) : nullptr;
+#pragma unroll
+      for (int part = 0; part < 2 * D / 32; ++part) {  // dK columns first, then dV
+        const uint32_t col = part < D / 32 ? kColDV + D + part * 32 : kColDV + (part - D / 32) * 32;
+        const float mult = part < D / 32 ? p.scale : 1.f;
+        uint32_t r[2][16];
+        tc::tmem_ld16(tmem + lane_base + col, r[0]);
+        tc::tmem_ld16(tmem + lane_base + col + 16, r[1]);
+        tc::tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(r[i >> 3][(2 * i) & 15]) * mult,
+                             __uint_as_float(r[i >> 3][(2 * i + 1) & 15]) * mult);
+        if (dst) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + part * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(bars.dvk_empty));
+    }
+    // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
+    ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);
+    if (!ok_run) atomicOr(&fail_s, 1);
+    const bool failed = sync_group_or(2, !ok_run);
+    if (!failed) {
+      tc::tc_fence_after();
+      const int dim = D == 128 ? te : ((lane < 16) ? (warp - 4) * 16 + lane : -1);
+      bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D]: stage 0 is free now
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + lane_base + kColDQ + h * 16, r);  // whole warp, converged
+        tc::tmem_wait_ld();
+        if (dim >= 0) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) stage[(h * 16 + i) * D + dim] = __float2bfloat16_rn(__uint_as_float(r[i]) * p.scale);
+        }
+      }
+      sync_group(2);
+      bf16* dqb = p.dq + row0 * D;
+      for (int i = te; i < 64 * D / 8; i += 128) reinterpret_cast<uint4*>(dqb)[i] = reinterpret_cast<const uint4*>(stage)[i];
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (fail_s && tid == 0) flag_status(p.status, kStatusTimeout);
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const BwdParams& p, const BwdWave& w, int64_t W32, cudaStream_t stream) {
+  const int smem = Sm<D>::TOTAL;
+  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ProfScope prof("bwd_main", stream);
+  sparse_bwd_tc_kernel<D><<<static_cast<unsigned>(w.nh * w.nblk), kThreads, smem, stream>>>(
+      p, w.bh0, w.blk0, w.nblk, W32, p.scale * kLog2e);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_tc(const BwdParams& p, const BwdWave& w, int64_t W32, cudaStream_t stream) {
+  switch (p.d) {
+    case 64: return launch_d<64>(p, w, W32, stream);
+    case 128: return launch_d<128>(p, w, W32, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsv

@@ -63,9 +63,10 @@ struct BwdParams {
   uint32_t* colpre;    // [nh][W32][N]   popcount of the words before
   uint32_t* count;     // [nh][N]
   int64_t* offsets;    // [nh][N]        first partial row of key j (absolute within the wave)
-  float* partial;      // [pairs][2 d]   dK part, then dV part
+  bf16* partial;       // [pairs][2 d]   dK part, then dV part (bf16; summed in fp32)
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
 };
 cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream);
+cudaError_t launch_bwd_main_tc(const BwdParams& p, const BwdWave& w, int64_t W32, cudaStream_t stream);
 
 }  // namespace dsv
