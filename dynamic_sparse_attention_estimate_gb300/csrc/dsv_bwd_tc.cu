@@ -12,10 +12,12 @@
 // kernel sums every key's rows in a fixed order (deterministic, no float atomics).
 // P and dS are written once to shared memory as bf16 128-byte rows (one per key); the same
 // bytes are the K-major A operand of dV_c / dK_c and the MN-major B operand of dQ^T.
-// Roles (320 threads): warps 0-3 compute P and dS (thread = key lane of S^T / dP^T);
-// warps 4-7 read dV_c / dK_c out of TMEM and store the partial rows (and dQ at the end);
-// warp 8 gathers Q, dO and the chunks' K and V rows with cp.async; one thread of warp 9
-// issues the MMAs as soon as their inputs are ready.  Every wait is bounded.
+// Roles (448 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
+// on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
+// dK_c out of TMEM and store the partial rows (and dQ at the end); warp 12 gathers Q, dO
+// and the chunks' K and V rows with cp.async into separate K and V rings (V is free after
+// dP, K only after dQ); one thread of warp 13 issues the MMAs as soon as their inputs are
+// ready.  Every wait is bounded.
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -24,8 +26,8 @@ namespace dsv {
 namespace {
 
 constexpr int kChunk = 128;
-constexpr int kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kCompute = 256;  // threads computing P and dS
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kPollLimit = 1u << 28;
 
@@ -34,16 +36,18 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 192, kTmemCols
 
 template <int D>
 struct Sm {
+  static constexpr int KST = D == 64 ? 4 : 3;         // K stages (held until dQ)
+  static constexpr int VST = D == 64 ? 4 : 2;         // V stages (held until dP)
   static constexpr int BLK = D / 64;
   static constexpr int T64 = BLK * 64 * 128;          // a [64 rows][D] tile
   static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
   static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16
-  static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + kStages * KV,
-                       OFF_P = OFF_V + kStages * KV, OFF_DS = OFF_P + P, TOTAL = OFF_DS + P;
+  static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + KST * KV,
+                       OFF_P = OFF_V + VST * KV, OFF_DS = OFF_P + P, TOTAL = OFF_DS + P;
 };
 
 struct Bars {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[4], empty_k[4], empty_v[4];  // per chunk slot: K and V landed / K free / V free
   uint64_t s_full, s_empty;        // S^T, dP^T in TMEM ready / read
   uint64_t p_full, pds_empty;      // P, dS tiles written / no longer read by any MMA
   uint64_t dvk_full, dvk_empty;    // dV_c, dK_c in TMEM ready / read
@@ -119,13 +123,14 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < 4; ++s) {
       tc::mbar_init(bar(bars.full[s]), 32);
-      tc::mbar_init(bar(bars.empty[s]), 1);
+      tc::mbar_init(bar(bars.empty_k[s]), 1);
+      tc::mbar_init(bar(bars.empty_v[s]), 1);
     }
     tc::mbar_init(bar(bars.s_full), 1);
-    tc::mbar_init(bar(bars.s_empty), 128);
-    tc::mbar_init(bar(bars.p_full), 128);
+    tc::mbar_init(bar(bars.s_empty), kCompute);
+    tc::mbar_init(bar(bars.p_full), kCompute);
     tc::mbar_init(bar(bars.pds_empty), 1);
     tc::mbar_init(bar(bars.dvk_full), 1);
     tc::mbar_init(bar(bars.dvk_empty), 128);
@@ -158,7 +163,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  if (warp == 8) {
+  constexpr int KST = S::KST, VST = S::VST;
+  constexpr int FST = KST > VST ? KST : VST;  // slots of the "landed" barrier ring
+  if (warp == 12) {
     // ================================================================ producer (cp.async)
     const bf16* kh = p.k + bh * N * D;
     const bf16* vh = p.v + bh * N * D;
@@ -175,17 +182,18 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     load_rows(0, nxt);
     bool ok_run = true;
     for (int c = 0; c < nchunks && ok_run; ++c) {
-      const int st = c % kStages;
+      const int sk = c % KST, sv = c % VST;
       int32_t cur[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) cur[h] = nxt[h];
       load_rows(c + 1, nxt);
-      if (c >= kStages) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / kStages) - 1) & 1, kWaitLimit);
+      if (c >= KST) ok_run = tc::mbar_wait(bar(bars.empty_k[sk]), ((c / KST) - 1) & 1, kWaitLimit);
+      if (ok_run && c >= VST) ok_run = tc::mbar_wait(bar(bars.empty_v[sv]), ((c / VST) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
       constexpr int LPR = D / 8, RPI = 32 / LPR;
       const int sub = lane % LPR, rsub = lane / LPR;
-      const uint32_t dK = sK + st * S::KV, dV = sV + st * S::KV;
+      const uint32_t dK = sK + sk * S::KV, dV = sV + sv * S::KV;
 #pragma unroll
       for (int it = 0; it < kChunk / RPI; ++it) {
         const int row = it * RPI + rsub;
@@ -197,11 +205,11 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         cp_async_16(dK + off, kh + src, ok);
         cp_async_16(dV + off, vh + src, ok);
       }
-      cp_async_arrive(bar(bars.full[st]));
+      cp_async_arrive(bar(bars.full[c % FST]));
     }
     cp_async_wait<0>();
     if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ================================================================ MMA issue (one thread)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);   // S^T, dP^T
@@ -222,21 +230,21 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
                        tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(bars.dvk_full));
-          const uint32_t aK = sK + (cg % kStages) * S::KV;
+          const uint32_t aK = sK + (cg % KST) * S::KV;
 #pragma unroll
           for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
             tc::mma_ss(tmem + kColDQ, tc::smem_desc(aK + j * 2048, kChunk * 128, 1024),
                        tc::smem_desc(sDS + j * 2048, 8192, 1024), idQ, (cg > 0 || j > 0) ? 1u : 0u);
           tc::mma_commit(bar(bars.pds_empty));
-          tc::mma_commit(bar(bars.empty[cg % kStages]));
+          tc::mma_commit(bar(bars.empty_k[cg % KST]));
           if (cg == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
           ++cg;
           idle = 0;
-        } else if (cs < nchunks && cs <= cg && mbar_test(bar(bars.full[cs % kStages]), (cs / kStages) & 1) &&
+        } else if (cs < nchunks && cs <= cg && mbar_test(bar(bars.full[cs % FST]), (cs / FST) & 1) &&
                    (cs == 0 || mbar_test(bar(bars.s_empty), (cs - 1) & 1))) {
           tc::fence_async_shared();  // the stage was written with cp.async (generic proxy)
           tc::tc_fence_after();
-          const uint32_t aK = sK + (cs % kStages) * S::KV, aV = sV + (cs % kStages) * S::KV;
+          const uint32_t aK = sK + (cs % KST) * S::KV, aV = sV + (cs % VST) * S::KV;
 #pragma unroll
           for (int j = 0; j < D / 16; ++j) {
             const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
@@ -247,6 +255,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
                        j > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(bars.s_full));
+          tc::mma_commit(bar(bars.empty_v[cs % VST]));
           ++cs;
           idle = 0;
         } else {
@@ -256,10 +265,11 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       if (!ok_run) atomicOr(&fail_s, 1);
     }
-  } else if (warp < 4) {
-    // ================================================================ P and dS (threads 0..127)
-    const int t = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ================================================================ P and dS (threads 0..255)
+    const int t = tid & 127;          // key lane
+    const int hq = tid >> 7;          // query columns [32 hq, 32 hq + 32)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok_run = true;
     int32_t jnext = t < kk ? __ldg(ib + t) : -1;
     for (int c = 0; c < nchunks; ++c) {
@@ -270,20 +280,20 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full), c & 1, kWaitLimit);
       tc::tc_fence_after();
-      uint32_t sr[4][16], dr[4][16];
+      uint32_t sr[2][16], dr[2][16];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        tc::tmem_ld16(tmem + lane_base + kColS + h * 16, sr[h]);
-        tc::tmem_ld16(tmem + lane_base + kColDP + h * 16, dr[h]);
+      for (int h = 0; h < 2; ++h) {
+        tc::tmem_ld16(tmem + lane_base + kColS + hq * 32 + h * 16, sr[h]);
+        tc::tmem_ld16(tmem + lane_base + kColDP + hq * 32 + h * 16, dr[h]);
       }
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty));
-      uint32_t pw[32], dw[32];  // packed bf16 pairs of P and dS
+      uint32_t pw[16], dw[16];  // packed bf16 pairs of P and dS
 #pragma unroll
-      for (int i4 = 0; i4 < 16; ++i4) {
-        const float4 l4 = reinterpret_cast<const float4*>(lse2_s)[i4];
-        const float4 d4 = reinterpret_cast<const float4*>(delta_s)[i4];
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 l4 = reinterpret_cast<const float4*>(lse2_s)[hq * 8 + i4];
+        const float4 d4 = reinterpret_cast<const float4*>(delta_s)[hq * 8 + i4];
         const float ll[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
         float pv[4], dv[4];
 #pragma unroll
@@ -302,12 +312,13 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       if (c >= 1) ok_run = ok_run && tc::mbar_wait(bar(bars.pds_empty), (c - 1) & 1, kWaitLimit);
       const uint32_t prow = sP + t * 128, drow = sDS + t * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int cc = 0; cc < 4; ++cc) {
+        const int ch = hq * 4 + cc;
         const uint32_t off = ((ch ^ t) & 7) << 4;
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + off), "r"(pw[ch * 4]), "r"(pw[ch * 4 + 1]),
-                     "r"(pw[ch * 4 + 2]), "r"(pw[ch * 4 + 3]));
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(drow + off), "r"(dw[ch * 4]), "r"(dw[ch * 4 + 1]),
-                     "r"(dw[ch * 4 + 2]), "r"(dw[ch * 4 + 3]));
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + off), "r"(pw[cc * 4]), "r"(pw[cc * 4 + 1]),
+                     "r"(pw[cc * 4 + 2]), "r"(pw[cc * 4 + 3]));
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(drow + off), "r"(dw[cc * 4]), "r"(dw[cc * 4 + 1]),
+                     "r"(dw[cc * 4 + 2]), "r"(dw[cc * 4 + 3]));
       }
       tc::fence_async_shared();
       tc::tc_fence_before();
@@ -315,9 +326,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     }
     if (!ok_run) atomicOr(&fail_s, 1);
   } else {
-    // ================================================================ partial rows and dQ (threads 128..255)
-    const int te = tid - 128;
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    // ================================================================ partial rows and dQ (threads 256..383)
+    const int te = tid - 256;
+    const uint32_t lane_base = static_cast<uint32_t>((warp - 8) * 32) << 16;
     const uint32_t* cbits = p.colbits + (hs * W32 + (lb >> 5)) * N;
     const uint32_t* cpre = p.colpre + (hs * W32 + (lb >> 5)) * N;
     const int64_t* offs = p.offsets + hs * N;
@@ -380,7 +391,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     const bool failed = sync_group_or(2, !ok_run);
     if (!failed) {
       tc::tc_fence_after();
-      const int dim = D == 128 ? te : ((lane < 16) ? (warp - 4) * 16 + lane : -1);
+      const int dim = D == 128 ? te : ((lane < 16) ? (warp - 8) * 16 + lane : -1);
       bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D]: stage 0 is free now
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
