@@ -36,14 +36,17 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 192, kTmemCols
 
 template <int D>
 struct Sm {
-  static constexpr int KST = D == 64 ? 4 : 3;         // K stages (held until dQ)
+  static constexpr int KST = D == 64 ? 4 : 2;         // K stages (held until dQ)
   static constexpr int VST = D == 64 ? 4 : 2;         // V stages (held until dP)
+  static constexpr int ROWB = 256;                    // staging bytes per key: the whole partial
+                                                      // row (d = 64) or half of it (d = 128)
   static constexpr int BLK = D / 64;
   static constexpr int T64 = BLK * 64 * 128;          // a [64 rows][D] tile
   static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
   static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16
   static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + KST * KV,
-                       OFF_P = OFF_V + VST * KV, OFF_DS = OFF_P + P, TOTAL = OFF_DS + P;
+                       OFF_P = OFF_V + VST * KV, OFF_DS = OFF_P + P, OFF_ST = OFF_DS + P,
+                       TOTAL = OFF_ST + kChunk * ROWB;
 };
 
 struct Bars {
@@ -72,6 +75,14 @@ DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Shared -> global bulk copy (TMA), tracked by this thread's bulk groups.
+DSV_DEVICE void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+DSV_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+DSV_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
@@ -362,9 +373,14 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       j_next2 = key_of(c + 2);
       ok_run = ok_run && tc::mbar_wait(bar(bars.dvk_full), c & 1, kWaitLimit);
       tc::tc_fence_after();
+      // dK (times scale) then dV, as bf16, through this key's staging row and one bulk copy
+      // per 256 bytes; the stores rotate over the row's 16-byte chunks to spread the banks
       bf16* dst = pos >= 0 ? p.partial + pos * (2 * D) : nullptr;
+      const uint32_t srow = sbase + S::OFF_ST + te * S::ROWB;
+      constexpr int PARTS_PER_COPY = S::ROWB / 64;  // 32-column parts (64 bytes each) per bulk copy
 #pragma unroll
       for (int part = 0; part < 2 * D / 32; ++part) {  // dK columns first, then dV
+        if (part % PARTS_PER_COPY == 0) bulk_wait_read();  // the staging row is free again
         const uint32_t col = part < D / 32 ? kColDV + D + part * 32 : kColDV + (part - D / 32) * 32;
         const float mult = part < D / 32 ? p.scale : 1.f;
         uint32_t r[2][16];
@@ -376,15 +392,26 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16x2(__uint_as_float(r[i >> 3][(2 * i) & 15]) * mult,
                              __uint_as_float(r[i >> 3][(2 * i + 1) & 15]) * mult);
-        if (dst) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + part * 32);
+        const int base_chunk = (part % PARTS_PER_COPY) * 4;  // 16-byte chunks within the staging row
 #pragma unroll
-          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+          const int vv = (v + te) & 3;  // lanes start at different chunks: fewer bank conflicts
+          uint32_t q4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            q4[u] = vv == 0 ? w[u] : (vv == 1 ? w[4 + u] : (vv == 2 ? w[8 + u] : w[12 + u]));
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (base_chunk + vv) * 16), "r"(q4[0]),
+                       "r"(q4[1]), "r"(q4[2]), "r"(q4[3]));
+        }
+        if (part % PARTS_PER_COPY == PARTS_PER_COPY - 1 && dst) {
+          tc::fence_async_shared();
+          bulk_store(dst + (part / PARTS_PER_COPY) * (S::ROWB / 2), srow, S::ROWB);
         }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.dvk_empty));
     }
+    bulk_wait_all();  // partial rows written before the kernel ends
     // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
     ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);
     if (!ok_run) atomicOr(&fail_s, 1);
