@@ -31,13 +31,16 @@ constexpr int kCompute = 256;  // threads computing P and dS
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kPollLimit = 1u << 28;
 
-// TMEM columns: S^T, dP^T (64 each), dQ^T (64), dV_c, dK_c (d each)
-constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDV = 192, kTmemCols = 512;
+// TMEM columns: S^T, dP^T, dQ^T (64 each), then dV_c, dK_c (d each) in one buffer (d = 128)
+// or two (d = 64: the MMAs of the next chunk fill one while the partial rows leave the other)
+constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
 
 template <int D>
 struct Sm {
   static constexpr int KST = D == 64 ? 4 : 2;         // K stages (held until dQ)
   static constexpr int VST = D == 64 ? 4 : 2;         // V stages (held until dP)
+  static constexpr int NDVK = D == 64 ? 2 : 1;       // dV_c / dK_c accumulator buffers
+  static constexpr uint32_t COL_DV = kColDQ + 64;     // first buffer; buffer b at + b * 2d
   static constexpr int ROWB = 256;                    // staging bytes per key: the whole partial
                                                       // row (d = 64) or half of it (d = 128)
   static constexpr int BLK = D / 64;
@@ -53,7 +56,7 @@ struct Bars {
   uint64_t full[4], empty_k[4], empty_v[4];  // per chunk slot: K and V landed / K free / V free
   uint64_t s_full, s_empty;        // S^T, dP^T in TMEM ready / read
   uint64_t p_full, pds_empty;      // P, dS tiles written / no longer read by any MMA
-  uint64_t dvk_full, dvk_empty;    // dV_c, dK_c in TMEM ready / read
+  uint64_t dvk_full[2], dvk_empty[2];  // per buffer: dV_c, dK_c in TMEM ready / read
   uint64_t dq_full;                // last dQ^T update done
 };
 
@@ -75,14 +78,16 @@ DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Shared -> global bulk copy (TMA), tracked by this thread's bulk groups.
-DSV_DEVICE void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+// Wait for this thread's TMEM loads, and make the 32 destination registers depend on the
+// wait so no use of them is scheduled ahead of it.
+DSV_DEVICE void tmem_wait_ld_into(uint32_t (&r)[2][16]) {
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile("" : "+r"(r[h][0]), "+r"(r[h][1]), "+r"(r[h][2]), "+r"(r[h][3]), "+r"(r[h][4]), "+r"(r[h][5]),
+                 "+r"(r[h][6]), "+r"(r[h][7]), "+r"(r[h][8]), "+r"(r[h][9]), "+r"(r[h][10]), "+r"(r[h][11]),
+                 "+r"(r[h][12]), "+r"(r[h][13]), "+r"(r[h][14]), "+r"(r[h][15]));
 }
-DSV_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
-DSV_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
@@ -143,8 +148,10 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     tc::mbar_init(bar(bars.s_empty), kCompute);
     tc::mbar_init(bar(bars.p_full), kCompute);
     tc::mbar_init(bar(bars.pds_empty), 1);
-    tc::mbar_init(bar(bars.dvk_full), 1);
-    tc::mbar_init(bar(bars.dvk_empty), 128);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(bars.dvk_full[s]), 1);
+      tc::mbar_init(bar(bars.dvk_empty[s]), 128);
+    }
     tc::mbar_init(bar(bars.dq_full), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fail_s = 0;
@@ -176,6 +183,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
 
   constexpr int KST = S::KST, VST = S::VST;
   constexpr int FST = KST > VST ? KST : VST;  // slots of the "landed" barrier ring
+  constexpr int NDVK = S::NDVK;
   if (warp == 12) {
     // ================================================================ producer (cp.async)
     const bf16* kh = p.k + bh * N * D;
@@ -231,16 +239,17 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       uint32_t idle = 0;
       while (ok_run && cg < nchunks) {
         if (cg < cs && mbar_test(bar(bars.p_full), cg & 1) &&
-            (cg == 0 || mbar_test(bar(bars.dvk_empty), (cg - 1) & 1))) {
+            (cg < NDVK || mbar_test(bar(bars.dvk_empty[cg % NDVK]), ((cg / NDVK) - 1) & 1))) {
           tc::tc_fence_after();
+          const uint32_t cdv = S::COL_DV + (cg % NDVK) * 2 * D;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // K = 64 queries
-            tc::mma_ss(tmem + kColDV, tc::smem_desc(sP + j * 32, 16, 1024),
+            tc::mma_ss(tmem + cdv, tc::smem_desc(sP + j * 32, 16, 1024),
                        tc::smem_desc(sDO + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
-            tc::mma_ss(tmem + kColDV + D, tc::smem_desc(sDS + j * 32, 16, 1024),
+            tc::mma_ss(tmem + cdv + D, tc::smem_desc(sDS + j * 32, 16, 1024),
                        tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
           }
-          tc::mma_commit(bar(bars.dvk_full));
+          tc::mma_commit(bar(bars.dvk_full[cg % NDVK]));
           const uint32_t aK = sK + (cg % KST) * S::KV;
 #pragma unroll
           for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
@@ -251,7 +260,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
           if (cg == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
           ++cg;
           idle = 0;
-        } else if (cs < nchunks && cs <= cg && mbar_test(bar(bars.full[cs % FST]), (cs / FST) & 1) &&
+        } else if (cs < nchunks && cs <= cg + 1 && mbar_test(bar(bars.full[cs % FST]), (cs / FST) & 1) &&
                    (cs == 0 || mbar_test(bar(bars.s_empty), (cs - 1) & 1))) {
           tc::fence_async_shared();  // the stage was written with cp.async (generic proxy)
           tc::tc_fence_after();
@@ -371,47 +380,66 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       const int64_t pos = pos_next.valid ? pos_next.off + pos_next.pre + __popc(pos_next.bits & lowmask) : -1;
       pos_next = pos_load(j_next2);
       j_next2 = key_of(c + 2);
-      ok_run = ok_run && tc::mbar_wait(bar(bars.dvk_full), c & 1, kWaitLimit);
+      const int buf = c % NDVK;
+      ok_run = ok_run && tc::mbar_wait(bar(bars.dvk_full[buf]), (c / NDVK) & 1, kWaitLimit);
       tc::tc_fence_after();
-      // dK (times scale) then dV, as bf16, through this key's staging row and one bulk copy
-      // per 256 bytes; the stores rotate over the row's 16-byte chunks to spread the banks
-      bf16* dst = pos >= 0 ? p.partial + pos * (2 * D) : nullptr;
+      // dK (times scale) then dV, as bf16, into this key's staging row (16-byte chunks XOR-
+      // swizzled by the row, so a warp's stores hit distinct banks); then the warp copies its
+      // 32 staged rows out two at a time, 16 lanes per 256-byte row, so that every store
+      // instruction writes whole rows.  The TMEM load of the next 32 columns is in flight
+      // while the current ones are converted.
+      const uint32_t cdv = S::COL_DV + buf * 2 * D;
       const uint32_t srow = sbase + S::OFF_ST + te * S::ROWB;
-      constexpr int PARTS_PER_COPY = S::ROWB / 64;  // 32-column parts (64 bytes each) per bulk copy
+      const uint32_t swarp = sbase + S::OFF_ST + (te & ~31) * S::ROWB;
+      constexpr int NPART = 2 * D / 32;             // 32-column parts: dK columns first, then dV
+      constexpr int PARTS_PER_COPY = S::ROWB / 64;  // parts (64 bytes each) per staging fill
+      auto part_col = [&](int part) -> uint32_t {
+        return part < D / 32 ? cdv + D + part * 32 : cdv + (part - D / 32) * 32;
+      };
+      uint32_t r[2][2][16];
+      tc::tmem_ld16(tmem + lane_base + part_col(0), r[0][0]);
+      tc::tmem_ld16(tmem + lane_base + part_col(0) + 16, r[0][1]);
+      tmem_wait_ld_into(r[0]);
 #pragma unroll
-      for (int part = 0; part < 2 * D / 32; ++part) {  // dK columns first, then dV
-        if (part % PARTS_PER_COPY == 0) bulk_wait_read();  // the staging row is free again
-        const uint32_t col = part < D / 32 ? kColDV + D + part * 32 : kColDV + (part - D / 32) * 32;
+      for (int part = 0; part < NPART; ++part) {
+        const int cur = part & 1;
+        if (part + 1 < NPART) {
+          tc::tmem_ld16(tmem + lane_base + part_col(part + 1), r[cur ^ 1][0]);
+          tc::tmem_ld16(tmem + lane_base + part_col(part + 1) + 16, r[cur ^ 1][1]);
+        }
         const float mult = part < D / 32 ? p.scale : 1.f;
-        uint32_t r[2][16];
-        tc::tmem_ld16(tmem + lane_base + col, r[0]);
-        tc::tmem_ld16(tmem + lane_base + col + 16, r[1]);
-        tc::tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(r[i >> 3][(2 * i) & 15]) * mult,
-                             __uint_as_float(r[i >> 3][(2 * i + 1) & 15]) * mult);
+          w[i] = pack_bf16x2(__uint_as_float(r[cur][i >> 3][(2 * i) & 15]) * mult,
+                             __uint_as_float(r[cur][i >> 3][(2 * i + 1) & 15]) * mult);
         const int base_chunk = (part % PARTS_PER_COPY) * 4;  // 16-byte chunks within the staging row
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int vv = (v + te) & 3;  // lanes start at different chunks: fewer bank conflicts
-          uint32_t q4[4];
+        for (int v = 0; v < 4; ++v)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((base_chunk + v) ^ (te & 7)) << 4)),
+                       "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3]));
+        if (part % PARTS_PER_COPY == PARTS_PER_COPY - 1) {
+          __syncwarp();
+          const int half_off = (part / PARTS_PER_COPY) * (S::ROWB / 2);  // bf16 elements into the row
+          const int chunk = lane & 15, rsel = lane >> 4;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            q4[u] = vv == 0 ? w[u] : (vv == 1 ? w[4 + u] : (vv == 2 ? w[8 + u] : w[12 + u]));
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (base_chunk + vv) * 16), "r"(q4[0]),
-                       "r"(q4[1]), "r"(q4[2]), "r"(q4[3]));
+          for (int rr = 0; rr < 32; rr += 2) {
+            const int row = rr + rsel;
+            const int64_t rpos = __shfl_sync(0xffffffffu, pos, row);
+            uint4 val;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                         : "r"(swarp + row * S::ROWB + ((chunk ^ (row & 7)) << 4)));
+            if (rpos >= 0)
+              *reinterpret_cast<uint4*>(p.partial + rpos * (2 * D) + half_off + chunk * 8) = val;
+          }
+          __syncwarp();
         }
-        if (part % PARTS_PER_COPY == PARTS_PER_COPY - 1 && dst) {
-          tc::fence_async_shared();
-          bulk_store(dst + (part / PARTS_PER_COPY) * (S::ROWB / 2), srow, S::ROWB);
-        }
+        if (part + 1 < NPART) tmem_wait_ld_into(r[cur ^ 1]);
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(bar(bars.dvk_empty));
+      tc::mbar_arrive(bar(bars.dvk_empty[buf]));
     }
-    bulk_wait_all();  // partial rows written before the kernel ends
     // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
     ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);
     if (!ok_run) atomicOr(&fail_s, 1);
