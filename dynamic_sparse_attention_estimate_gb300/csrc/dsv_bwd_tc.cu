@@ -12,12 +12,16 @@
 // kernel sums every key's rows in a fixed order (deterministic, no float atomics).
 // P and dS are written once to shared memory as bf16 128-byte rows (one per key); the same
 // bytes are the K-major A operand of dV_c / dK_c and the MN-major B operand of dQ^T.
-// Roles (448 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
+// Roles (512 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
 // on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
-// dK_c out of TMEM and store the partial rows (and dQ at the end); warp 12 gathers Q, dO
-// and the chunks' K and V rows with cp.async into separate K and V rings (V is free after
-// dP, K only after dQ); one thread of warp 13 issues the MMAs as soon as their inputs are
-// ready.  Every wait is bounded.
+// dK_c out of TMEM into shared-memory staging rows (and write dQ at the end); warp 12
+// gathers Q, dO and the chunks' K and V rows with cp.async into separate K and V rings (V
+// is free after dP, K only after dQ); one thread of warp 13 issues the MMAs in a fixed
+// order, each group as soon as its inputs are there; warps 14-15 copy the staged partial
+// rows to global memory (d = 64; at d = 128 the readout warps copy their own rows).
+// Buffering across chunks: dV_c / dK_c in two TMEM buffers and two staging buffers (d = 64),
+// so that readout and stores of chunk c overlap the MMAs of chunk c + 1.  Every wait is
+// bounded.
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -26,10 +30,9 @@ namespace dsv {
 namespace {
 
 constexpr int kChunk = 128;
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr int kCompute = 256;  // threads computing P and dS
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kPollLimit = 1u << 28;
 
 // TMEM columns: S^T, dP^T, dQ^T (64 each), then dV_c, dK_c (d each) in one buffer (d = 128)
 // or two (d = 64: the MMAs of the next chunk fill one while the partial rows leave the other)
@@ -38,7 +41,10 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
 template <int D>
 struct Sm {
   static constexpr int KST = D == 64 ? 4 : 2;         // K stages (held until dQ)
-  static constexpr int VST = D == 64 ? 4 : 2;         // V stages (held until dP)
+  static constexpr int VST = 2;                       // V stages (held until dP)
+  static constexpr int NPDS = 1;                      // P / dS tile pairs
+  static constexpr int NST = D == 64 ? 2 : 1;         // staging buffers (d = 64: the store warps
+                                                      // drain one while the other fills)
   static constexpr int NDVK = D == 64 ? 2 : 1;       // dV_c / dK_c accumulator buffers
   static constexpr uint32_t COL_DV = kColDQ + 64;     // first buffer; buffer b at + b * 2d
   static constexpr int ROWB = 256;                    // staging bytes per key: the whole partial
@@ -48,16 +54,17 @@ struct Sm {
   static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
   static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16
   static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + KST * KV,
-                       OFF_P = OFF_V + VST * KV, OFF_DS = OFF_P + P, OFF_ST = OFF_DS + P,
-                       TOTAL = OFF_ST + kChunk * ROWB;
+                       OFF_P = OFF_V + VST * KV, OFF_ST = OFF_P + NPDS * 2 * P,  // pair b: P, then dS
+                       TOTAL = OFF_ST + NST * kChunk * ROWB;
 };
 
 struct Bars {
   uint64_t full[4], empty_k[4], empty_v[4];  // per chunk slot: K and V landed / K free / V free
   uint64_t s_full, s_empty;        // S^T, dP^T in TMEM ready / read
-  uint64_t p_full, pds_empty;      // P, dS tiles written / no longer read by any MMA
+  uint64_t p_full[2], pds_empty[2];  // per tile pair: P, dS written / no longer read by any MMA
   uint64_t dvk_full[2], dvk_empty[2];  // per buffer: dV_c, dK_c in TMEM ready / read
   uint64_t dq_full;                // last dQ^T update done
+  uint64_t st_full[2], st_empty[2];  // per staging buffer: rows written / copied out (d = 64)
 };
 
 DSV_DEVICE void sync_group(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
@@ -68,15 +75,6 @@ DSV_DEVICE bool sync_group_or(int id, bool v) {
                : "r"(id), "r"(static_cast<uint32_t>(v))
                : "memory");
   return r != 0;
-}
-DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 // Wait for this thread's TMEM loads, and make the 32 destination registers depend on the
 // wait so no use of them is scheduled ahead of it.
@@ -117,6 +115,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   __shared__ __align__(16) float lse2_s[64];
   __shared__ __align__(16) float delta_s[64];
   __shared__ int fail_s;
+  __shared__ int64_t pos_s[2][kChunk];  // partial-row index of each staged key (-1: none)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t N = p.N, NB = p.NB, kk = p.topk;
@@ -127,7 +126,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sDO = sbase + S::OFF_DO, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V;
-  const uint32_t sP = sbase + S::OFF_P, sDS = sbase + S::OFF_DS;
+  const uint32_t sPDS = sbase + S::OFF_P;  // tile pair b: P at sPDS + b * 2 * S::P, dS after it
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
   if (sbase & 1023u) {  // swizzled tiles need 1024-byte alignment
@@ -146,13 +145,19 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     }
     tc::mbar_init(bar(bars.s_full), 1);
     tc::mbar_init(bar(bars.s_empty), kCompute);
-    tc::mbar_init(bar(bars.p_full), kCompute);
-    tc::mbar_init(bar(bars.pds_empty), 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(bars.p_full[s]), kCompute);
+      tc::mbar_init(bar(bars.pds_empty[s]), 1);
+    }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(bars.dvk_full[s]), 1);
       tc::mbar_init(bar(bars.dvk_empty[s]), 128);
     }
     tc::mbar_init(bar(bars.dq_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bar(bars.st_full[s]), 128);
+      tc::mbar_init(bar(bars.st_empty[s]), 64);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fail_s = 0;
   }
@@ -183,7 +188,10 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
 
   constexpr int KST = S::KST, VST = S::VST;
   constexpr int FST = KST > VST ? KST : VST;  // slots of the "landed" barrier ring
-  constexpr int NDVK = S::NDVK;
+  constexpr int NDVK = S::NDVK, NPDS = S::NPDS;
+  // d = 64: two store warps do nothing but copy staged partial rows out, so the SM's store
+  // path stays busy while the other roles work on later chunks
+  constexpr bool kStoreWarps = D == 64;
   if (warp == 12) {
     // ================================================================ producer (cp.async)
     const bf16* kh = p.k + bh * N * D;
@@ -234,54 +242,61 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);   // S^T, dP^T
       constexpr uint32_t idKV = tc::idesc_bf16(128, D, 0, 1);   // dV_c, dK_c: A K-major, B MN-major
       constexpr uint32_t idQ = tc::idesc_bf16(D, 64, 1, 1);     // dQ^T: A, B MN-major
-      bool ok_run = true;
-      int cs = 0, cg = 0;
-      uint32_t idle = 0;
-      while (ok_run && cg < nchunks) {
-        if (cg < cs && mbar_test(bar(bars.p_full), cg & 1) &&
-            (cg < NDVK || mbar_test(bar(bars.dvk_empty[cg % NDVK]), ((cg / NDVK) - 1) & 1))) {
-          tc::tc_fence_after();
-          const uint32_t cdv = S::COL_DV + (cg % NDVK) * 2 * D;
+      // S^T / dP^T of chunk c
+      auto issue_s = [&](int c) {
+        tc::fence_async_shared();  // the stage was written with cp.async (generic proxy)
+        tc::tc_fence_after();
+        const uint32_t aK = sK + (c % KST) * S::KV, aV = sV + (c % VST) * S::KV;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {  // K = 64 queries
-            tc::mma_ss(tmem + cdv, tc::smem_desc(sP + j * 32, 16, 1024),
-                       tc::smem_desc(sDO + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
-            tc::mma_ss(tmem + cdv + D, tc::smem_desc(sDS + j * 32, 16, 1024),
-                       tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(bar(bars.dvk_full[cg % NDVK]));
-          const uint32_t aK = sK + (cg % KST) * S::KV;
-#pragma unroll
-          for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
-            tc::mma_ss(tmem + kColDQ, tc::smem_desc(aK + j * 2048, kChunk * 128, 1024),
-                       tc::smem_desc(sDS + j * 2048, 8192, 1024), idQ, (cg > 0 || j > 0) ? 1u : 0u);
-          tc::mma_commit(bar(bars.pds_empty));
-          tc::mma_commit(bar(bars.empty_k[cg % KST]));
-          if (cg == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
-          ++cg;
-          idle = 0;
-        } else if (cs < nchunks && cs <= cg + 1 && mbar_test(bar(bars.full[cs % FST]), (cs / FST) & 1) &&
-                   (cs == 0 || mbar_test(bar(bars.s_empty), (cs - 1) & 1))) {
-          tc::fence_async_shared();  // the stage was written with cp.async (generic proxy)
-          tc::tc_fence_after();
-          const uint32_t aK = sK + (cs % KST) * S::KV, aV = sV + (cs % VST) * S::KV;
-#pragma unroll
-          for (int j = 0; j < D / 16; ++j) {
-            const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
-            const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
-            tc::mma_ss(tmem + kColS, tc::smem_desc(aK + off_a, 16, 1024), tc::smem_desc(sQ + off_b, 16, 1024), idS,
-                       j > 0 ? 1u : 0u);
-            tc::mma_ss(tmem + kColDP, tc::smem_desc(aV + off_a, 16, 1024), tc::smem_desc(sDO + off_b, 16, 1024), idS,
-                       j > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(bar(bars.s_full));
-          tc::mma_commit(bar(bars.empty_v[cs % VST]));
-          ++cs;
-          idle = 0;
-        } else {
-          if (++idle > kPollLimit) ok_run = false;
-          __nanosleep(32);
+        for (int j = 0; j < D / 16; ++j) {
+          const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
+          const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
+          tc::mma_ss(tmem + kColS, tc::smem_desc(aK + off_a, 16, 1024), tc::smem_desc(sQ + off_b, 16, 1024), idS,
+                     j > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + kColDP, tc::smem_desc(aV + off_a, 16, 1024), tc::smem_desc(sDO + off_b, 16, 1024), idS,
+                     j > 0 ? 1u : 0u);
         }
+        tc::mma_commit(bar(bars.s_full));
+        tc::mma_commit(bar(bars.empty_v[c % VST]));
+      };
+      // dV_c, dK_c, then the dQ^T update of chunk c
+      auto issue_grads = [&](int c) {
+        tc::tc_fence_after();
+        const uint32_t cdv = S::COL_DV + (c % NDVK) * 2 * D;
+        const uint32_t sP = sPDS + (c % NPDS) * 2 * S::P, sDS = sP + S::P;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // K = 64 queries
+          tc::mma_ss(tmem + cdv, tc::smem_desc(sP + j * 32, 16, 1024), tc::smem_desc(sDO + j * 2048, 64 * 128, 1024),
+                     idKV, j > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + cdv + D, tc::smem_desc(sDS + j * 32, 16, 1024),
+                     tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(bar(bars.dvk_full[c % NDVK]));
+        const uint32_t aK = sK + (c % KST) * S::KV;
+#pragma unroll
+        for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
+          tc::mma_ss(tmem + kColDQ, tc::smem_desc(aK + j * 2048, kChunk * 128, 1024),
+                     tc::smem_desc(sDS + j * 2048, 8192, 1024), idQ, (c > 0 || j > 0) ? 1u : 0u);
+        tc::mma_commit(bar(bars.pds_empty[c % NPDS]));
+        tc::mma_commit(bar(bars.empty_k[c % KST]));
+        if (c == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
+      };
+      // Fixed issue order S(0), then per chunk c: S(c+1), grads(c).  S(c+1) needs only the
+      // loaded stage and S^T(c) read out, both of which precede P(c); each wait blocks in the
+      // hardware (no polling), so an MMA group starts as soon as its inputs are there.
+      bool ok_run = tc::mbar_wait(bar(bars.full[0]), 0, kWaitLimit);
+      if (ok_run) issue_s(0);
+      for (int c = 0; c < nchunks && ok_run; ++c) {
+        if (c + 1 < nchunks) {
+          ok_run = tc::mbar_wait(bar(bars.full[(c + 1) % FST]), ((c + 1) / FST) & 1, kWaitLimit) &&
+                   tc::mbar_wait(bar(bars.s_empty), c & 1, kWaitLimit);
+          if (!ok_run) break;
+          issue_s(c + 1);
+        }
+        ok_run = tc::mbar_wait(bar(bars.p_full[c % NPDS]), (c / NPDS) & 1, kWaitLimit) &&
+                 (c < NDVK || tc::mbar_wait(bar(bars.dvk_empty[c % NDVK]), ((c / NDVK) - 1) & 1, kWaitLimit));
+        if (!ok_run) break;
+        issue_grads(c);
       }
       if (!ok_run) atomicOr(&fail_s, 1);
     }
@@ -329,8 +344,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         dw[i4 * 2] = pack_bf16x2(dv[0], dv[1]);
         dw[i4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
       }
-      if (c >= 1) ok_run = ok_run && tc::mbar_wait(bar(bars.pds_empty), (c - 1) & 1, kWaitLimit);
-      const uint32_t prow = sP + t * 128, drow = sDS + t * 128;
+      const int pb = c % NPDS;
+      if (c >= NPDS) ok_run = ok_run && tc::mbar_wait(bar(bars.pds_empty[pb]), ((c / NPDS) - 1) & 1, kWaitLimit);
+      const uint32_t prow = sPDS + pb * 2 * S::P + t * 128, drow = prow + S::P;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int ch = hq * 4 + cc;
@@ -342,9 +358,41 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       tc::fence_async_shared();
       tc::tc_fence_before();
-      tc::mbar_arrive(bar(bars.p_full));
+      tc::mbar_arrive(bar(bars.p_full[pb]));
     }
     if (!ok_run) atomicOr(&fail_s, 1);
+  } else if (warp >= 14) {
+    // ================================================================ partial-row stores (d = 64)
+    // Warp 14 + w copies staged rows [64 w, 64 w + 64) of each chunk to their key-major
+    // positions, two rows per store instruction (16 lanes per 256-byte row), 8 in flight.
+    if (kStoreWarps) {
+      const int chunk = lane & 15, rsel = lane >> 4;
+      bool ok_run = true;
+      for (int c = 0; c < nchunks && ok_run; ++c) {
+        const int b = c & 1;
+        ok_run = tc::mbar_wait(bar(bars.st_full[b]), (c >> 1) & 1, kWaitLimit);
+        if (!ok_run) break;
+        const uint32_t sst = sbase + S::OFF_ST + b * (kChunk * S::ROWB);
+#pragma unroll 1
+        for (int r0 = (warp - 14) * 64; r0 < (warp - 13) * 64; r0 += 16) {
+          uint4 val[8];
+          int64_t rpos[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = r0 + 2 * i + rsel;
+            rpos[i] = pos_s[b][row];
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(val[i].x), "=r"(val[i].y), "=r"(val[i].z), "=r"(val[i].w)
+                         : "r"(sst + row * S::ROWB + ((chunk ^ (row & 7)) << 4)));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (rpos[i] >= 0) *reinterpret_cast<uint4*>(p.partial + rpos[i] * (2 * D) + chunk * 8) = val[i];
+        }
+        tc::mbar_arrive(bar(bars.st_empty[b]));  // every staged byte of this buffer has been read
+      }
+      if (!ok_run) atomicOr(&fail_s, 1);
+    }
   } else {
     // ================================================================ partial rows and dQ (threads 256..383)
     const int te = tid - 256;
@@ -384,12 +432,13 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       ok_run = ok_run && tc::mbar_wait(bar(bars.dvk_full[buf]), (c / NDVK) & 1, kWaitLimit);
       tc::tc_fence_after();
       // dK (times scale) then dV, as bf16, into this key's staging row (16-byte chunks XOR-
-      // swizzled by the row, so a warp's stores hit distinct banks); then the warp copies its
-      // 32 staged rows out two at a time, 16 lanes per 256-byte row, so that every store
-      // instruction writes whole rows.  The TMEM load of the next 32 columns is in flight
-      // while the current ones are converted.
+      // swizzled by the row, so a warp's stores hit distinct banks).  d = 64: the store warps
+      // copy the chunk's rows out; d = 128: each half row is copied out here, by the warp, two
+      // rows per store instruction.  Either way every store instruction writes whole rows.
+      // The TMEM load of the next 32 columns is in flight while the current ones are converted.
       const uint32_t cdv = S::COL_DV + buf * 2 * D;
-      const uint32_t srow = sbase + S::OFF_ST + te * S::ROWB;
+      const int sb = kStoreWarps ? (c & 1) : 0;  // staging buffer
+      const uint32_t srow = sbase + S::OFF_ST + sb * (kChunk * S::ROWB) + te * S::ROWB;
       const uint32_t swarp = sbase + S::OFF_ST + (te & ~31) * S::ROWB;
       constexpr int NPART = 2 * D / 32;             // 32-column parts: dK columns first, then dV
       constexpr int PARTS_PER_COPY = S::ROWB / 64;  // parts (64 bytes each) per staging fill
@@ -400,6 +449,10 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::tmem_ld16(tmem + lane_base + part_col(0), r[0][0]);
       tc::tmem_ld16(tmem + lane_base + part_col(0) + 16, r[0][1]);
       tmem_wait_ld_into(r[0]);
+      if (kStoreWarps) {  // the store warps have drained this buffer's previous chunk
+        if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.st_empty[sb]), ((c >> 1) - 1) & 1, kWaitLimit);
+        pos_s[sb][te] = pos;
+      }
 #pragma unroll
       for (int part = 0; part < NPART; ++part) {
         const int cur = part & 1;
@@ -418,7 +471,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         for (int v = 0; v < 4; ++v)
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((base_chunk + v) ^ (te & 7)) << 4)),
                        "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3]));
-        if (part % PARTS_PER_COPY == PARTS_PER_COPY - 1) {
+        if (!kStoreWarps && part % PARTS_PER_COPY == PARTS_PER_COPY - 1) {
           __syncwarp();
           const int half_off = (part / PARTS_PER_COPY) * (S::ROWB / 2);  // bf16 elements into the row
           const int chunk = lane & 15, rsel = lane >> 4;
@@ -439,6 +492,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.dvk_empty[buf]));
+      if (kStoreWarps) tc::mbar_arrive(bar(bars.st_full[sb]));
     }
     // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
     ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);
