@@ -5,7 +5,8 @@
 // chunks of 128 with keys on the MMA's M dimension (the "transposed" formulation):
 //     S^T[128 keys x 64 q]  = K_c . Q^T           (tcgen05, M=128, N=64, K=d)
 //     O^T[d x 64 q]        += V_c^T . P^T         (tcgen05, M=d,   N=64, K=128)
-// so both products keep M = 128 (M = 64 for d = 64) although a block has 64 queries.
+// so both products keep M = 128 although a block has 64 queries (for d = 64 the PV operand
+// carries an extra row of ones that yields the softmax row sums; see kOnesRow).
 // Roles (192 threads):
 //   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
 //              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16, one 128-byte
@@ -48,7 +49,11 @@ struct Smem {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
   static constexpr int OFF_P = OFF_V + NST * KV_BYTES;
-  static constexpr int TOTAL = OFF_P + 2 * P_BYTES;
+  // d = 64: a constant 16-key tile whose first M column is 1, the second 64-row block of the
+  // PV product's A operand (see kOnesRow)
+  static constexpr int OFF_ONES = OFF_P + 2 * P_BYTES;
+  static constexpr int ONES_BYTES = D == 64 ? 2048 : 0;
+  static constexpr int TOTAL = OFF_ONES + ONES_BYTES;
 };
 
 template <int NST>
@@ -86,6 +91,13 @@ DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
 DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
+
+// d = 64: the PV product runs with M = 128 instead of 64 (the same tensor-core time: M = 64
+// runs at half rate), its A operand extended past V_c^T by a row of ones, so TMEM lane 64 of
+// O^T accumulates sum_keys P^T = the softmax row sums L, and the softmax threads keep no
+// sums of their own.  L is then the sum of the same bf16 P values that weight V.
+template <int D>
+constexpr bool kOnesRow = D == 64;
 
 // Column reduction over the 128 softmax threads of 64 per-thread values (v[c] is this
 // thread's value for column c).  Fixed order, so the result is deterministic.  Returns
@@ -171,6 +183,11 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     fail_s = 0;
   }
   if (tid < 64) m_s[tid] = -CUDART_INF_F;
+  if (kOnesRow<D> && tid < 128) {  // 16 rows x 128 bytes, 128-byte swizzle: element 0 of row r
+    const int row = tid >> 3, ch = tid & 7;  // sits in 16-byte chunk (r & 7)
+    *reinterpret_cast<uint4*>(smem + S::OFF_ONES + tid * 16) = make_uint4(ch == (row & 7) ? 0x3f80u : 0u, 0u, 0u, 0u);
+    tc::fence_async_shared();  // visible to the tensor core
+  }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -237,7 +254,8 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     // ================================================================ MMA issue (one thread)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(128, 64, 0, 0);
-      constexpr uint32_t idO = tc::idesc_bf16(D, 64, 1, 1);
+      constexpr uint32_t idO = tc::idesc_bf16(kOnesRow<D> ? 128 : D, 64, 1, 1);
+      const uint32_t sOnes = sbase + S::OFF_ONES;
       bool ok_run = true;
       int cs = 0, cp = 0;
       uint32_t idle = 0;
@@ -247,9 +265,12 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           tc::tc_fence_after();
           const uint32_t aV = sV + (cp % NST) * S::KV_BYTES, bP = sP + (cp & 1) * S::P_BYTES;
 #pragma unroll
-          for (int j = 0; j < kChunk / 16; ++j)
-            tc::mma_ss(tmem + kColO, tc::smem_desc(aV + j * 2048, kChunk * 128, 1024),
-                       tc::smem_desc(bP + j * 2048, 8192, 1024), idO, (cp > 0 || j > 0) ? 1u : 0u);
+          for (int j = 0; j < kChunk / 16; ++j) {
+            // second 64-row block of A: the next 64 head dims (d = 128) or the ones tile
+            const uint32_t a = aV + j * 2048, lbo = kOnesRow<D> ? sOnes - a : kChunk * 128;
+            tc::mma_ss(tmem + kColO, tc::smem_desc(a, lbo, 1024), tc::smem_desc(bP + j * 2048, 8192, 1024), idO,
+                       (cp > 0 || j > 0) ? 1u : 0u);
+          }
           tc::mma_commit(bar(bars.pv_done[cp & 1]));
           tc::mma_commit(bar(bars.empty[cp % NST]));
           if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
@@ -346,7 +367,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[(c - 1) & 1]), ((c - 1) >> 1) & 1, kWaitLimit);
           tc::tc_fence_after();
 #pragma unroll
-          for (int col = 0; col < 2; ++col) {  // O^T (lanes = d) then L (lanes = keys)
+          for (int col = 0; col < (kOnesRow<D> ? 1 : 2); ++col) {  // O^T (and L with it), then L
             const uint32_t base = tmem + lane_base + (col ? kColL : kColO);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -375,9 +396,9 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + (((ch ^ t) & 7) << 4)), "r"(w0), "r"(w1),
                      "r"(w2), "r"(w3));
       }
-      // ---- row sums of this key lane, accumulated in TMEM
+      // ---- d = 128: row sums of this key lane, accumulated in TMEM
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < (kOnesRow<D> ? 0 : 2); ++half) {
         const uint32_t base = tmem + lane_base + kColL + half * 32;
         uint32_t r[2][16];
         if (c > 0) {
@@ -393,31 +414,49 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           tc::tmem_st16(base + h * 16, r[h]);
         }
       }
-      tc::tmem_wait_st();
+      if (!kOnesRow<D>) tc::tmem_wait_st();
       tc::fence_async_shared();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.p_full[b]));
     }
-    // ---- epilogue: l = column sums of L, O = O^T / l, LSE = (m + log2 l) ln 2
+    // ---- epilogue: l = row sums (lane 64 of O^T, or column sums of L), O = O^T / l,
+    // LSE = (m + log2 l) ln 2
     ok_run = ok_run && tc::mbar_wait(bar(bars.o_full), 0, kWaitLimit);
     if (!ok_run) atomicOr(&fail_s, 1);
     const bool failed = named_sync_or(!ok_run);
     if (!failed) {
       tc::tc_fence_after();
-      float lsum[64];
-      {
-        uint32_t r[4][16];
+      if (kOnesRow<D>) {
+        if (warp == 2) {  // lane 64 of O^T holds l for all 64 query columns
+          uint32_t r[4][16];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + kColL + h * 16, r[h]);
-        tc::tmem_wait_ld();
+          for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + kColO + h * 16, r[h]);
+          tc::tmem_wait_ld();
+          if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+            for (int h = 0; h < 4; ++h)
 #pragma unroll
-          for (int i = 0; i < 16; ++i) lsum[h * 16 + i] = __uint_as_float(r[h][i]);
+              for (int i = 0; i < 16; ++i) red_s[h * 16 + i] = __uint_as_float(r[h][i]);
+          }
+        }
+        named_sync_softmax();
+      } else {
+        float lsum[64];
+        {
+          uint32_t r[4][16];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + kColL + h * 16, r[h]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) lsum[h * 16 + i] = __uint_as_float(r[h][i]);
+        }
+        column_reduce<false>(lsum, red_w, red_s, warp, lane);
       }
-      column_reduce<false>(lsum, red_w, red_s, warp, lane);
-      // O^T lane -> head dim: identity for d = 128; for d = 64 (M = 64) rows sit 16 per lane quadrant
-      const int dim = D == 128 ? t : ((lane < 16) ? warp * 16 + lane : -1);
+      // O^T lane -> head dim (M = 128: lane = row; lanes 64.. of the d = 64 product are the
+      // row sums and the zero rows of the ones tile)
+      const int dim = t < D ? t : -1;
       bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D]: K stage 0 is free now
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
