@@ -39,7 +39,6 @@ struct FwdParams {
   float scale;
   unsigned int* status;
 };
-cudaError_t launch_sparse_fwd(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_sparse_fwd_tc(const FwdParams& p, cudaStream_t stream);
 
 // One wave of the backward: either whole heads [bh0, bh0 + nh) (blk0 = 0, nblk = NB)
