@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads (small cases for profiler captures)")
     return ap.parse_args()
 
 
@@ -58,6 +60,8 @@ def workload(args):
         wl = wl.with_density(args.density)
     if wl.heads_per_call:
         wl = wl.with_heads(wl.heads_per_call)   # the long clip runs 4 heads per call
+    if args.heads is not None:
+        wl = wl.with_heads(args.heads)
     return wl
 
 
@@ -204,12 +208,14 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-KERNEL_FILES = {"estimate_topk": "dsv_estimate.cu", "estimate_arange": "dsv_estimate.cu", "sparse_fwd": "dsv_fwd.cu"}
+KERNEL_FILES = {"estimate_topk": ("dsv_estimate.cu",), "estimate_arange": ("dsv_estimate.cu",),
+                "sparse_fwd": ("dsv_fwd_tc.cu", "dsv_tc.cuh"), "bwd_main": ("dsv_bwd_tc.cu", "dsv_tc.cuh")}
 
 
 def kernel_source_hash(kernel):
+    """Hash of the sources a kernel is built from: stored DRAM traffic counts only while it matches."""
     h = hashlib.sha256()
-    for f in (KERNEL_FILES.get(kernel, "dsv_bwd.cu"), "dsv_common.cuh"):
+    for f in KERNEL_FILES.get(kernel, ("dsv_bwd.cu",)) + ("dsv_common.cuh",):
         h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:16]
 
