@@ -406,6 +406,29 @@ def dsv_arm(args):
         except Exception as exc:  # a comparator only
             dense = {"error": str(exc)[:200]}
 
+    # ---- this library at density 100 % (k = N: idx = every key, ascending) on the same shape: the
+    # sparse kernels run as a dense attention
+    own_dense = None
+    if not args.no_dense:
+        try:
+            kd = wl.N
+            idx_d = torch.empty((wl.B, wl.H, wl.NB, kd), dtype=torch.int32, device=dev)
+            ws_d = torch.empty(dsv_sparse_attn_bwd_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, kd)),
+                               dtype=torch.uint8, device=dev)
+
+            def own_dense_step():
+                dsv_estimate_topk(g["q_lr"], g["k_lr"], kd, idx=idx_d)
+                dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx_d, out=(o, lse))
+                dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx_d, workspace=ws_d, out=(dq, dk, dv))
+            for _ in range(2):
+                own_dense_step()
+            t_od = timed(own_dense_step, 5)
+            own_dense = {"ms": t_od, "tflops": 14.0 * BH * wl.N * wl.N * wl.d / (t_od / 1e3) / 1e12,
+                         "impl": "this library with k = N (idx = arange), estimate + forward + backward"}
+            del idx_d, ws_d
+        except Exception as exc:  # a comparator only
+            own_dense = {"error": str(exc)[:200]}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -431,7 +454,10 @@ def dsv_arm(args):
         "stages_ms": {"estimate_topk": t_est, "sparse_fwd": t_fwd, "sparse_bwd": t_bwd},
         "attn_only_tflops": 14.0 * BH * wl.N * wl.k * wl.d / ((t_fwd + t_bwd) / 1e3) / 1e12,
         "kernel_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+        "estimate": {"ms": t_est, "score_elements_per_s": BH * wl.NB * wl.N / (t_est / 1e3),
+                     "mma_tflops": 2.0 * wl.r * BH * wl.NB * wl.N / (t_est / 1e3) / 1e12},
         "roofline": rl, "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "dense_comparator": dense,
+        "own_dense_path": own_dense,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

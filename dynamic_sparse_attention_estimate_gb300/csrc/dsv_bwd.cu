@@ -100,7 +100,9 @@ scan_kernel(const uint32_t* __restrict__ count, int64_t* __restrict__ offsets, i
 // ---------------------------------------------------------------- 4. main kernel: dsv_bwd_tc.cu
 
 // ---------------------------------------------------------------- 5. segmented reduction per key
-// One warp per key; lane l owns columns [4 l, 4 l + 4) (and + 128 when 2 D = 256).
+// One warp per key; lane l owns columns [4 l, 4 l + 4) (and + 128 when 2 D = 256).  The key's
+// partial rows are gathered through its list (ascending query block: a fixed order), eight
+// rows in flight; at d = 64 the row's 16-byte chunks sit XOR (row & 7).
 template <int D>
 __global__ void reduce_kernel(BwdParams p, int64_t bh0, int64_t nh, int mode /*0: write, 1: first, 2: middle, 3: last*/) {
   constexpr int W = 2 * D;       // columns per partial row
@@ -112,7 +114,7 @@ __global__ void reduce_kernel(BwdParams p, int64_t bh0, int64_t nh, int mode /*0
        key += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
     const int64_t hs = key / N, j = key % N;
     const int64_t first = p.offsets[key];
-    const int64_t cnt = p.count[key];
+    const int cnt = static_cast<int>(p.count[key]);
     float4 acc[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -120,12 +122,40 @@ __global__ void reduce_kernel(BwdParams p, int64_t bh0, int64_t nh, int mode /*0
 #pragma unroll
       for (int u = 0; u < PER; ++u) acc[u] = *reinterpret_cast<const float4*>(p.acc + j * W + u * 128 + lane * 4);
     }
-    for (int64_t r = 0; r < cnt; ++r) {
-      const bf16* row = p.partial + (first + r) * W;
+    auto row_ptr = [&](int32_t row, int u) -> const uint2* {
+      // element offset of this lane's 4 columns [u 128 + 4 lane, + 4) within partial row `row`
+      int e = u * 128 + lane * 4;
+      if (D == 64) e = ((((e >> 3) ^ (row & 7)) << 3) | (e & 7));
+      return reinterpret_cast<const uint2*>(p.partial + static_cast<int64_t>(row) * W + e);
+    };
+    for (int r0 = 0; r0 < cnt; r0 += 32) {
+      const int32_t mine = r0 + lane < cnt ? p.lists[first + r0 + lane] : 0;
+      const int n = cnt - r0 < 32 ? cnt - r0 : 32;
+      int i = 0;
+      constexpr int kBatch = 8;  // rows in flight per warp
+      for (; i + kBatch <= n; i += kBatch) {
+        uint2 x[kBatch][PER];
 #pragma unroll
-      for (int u = 0; u < PER; ++u) {
-        const uint2 x = *reinterpret_cast<const uint2*>(row + u * 128 + lane * 4);
-        acc[u].x += bf16_lo(x.x); acc[u].y += bf16_hi(x.x); acc[u].z += bf16_lo(x.y); acc[u].w += bf16_hi(x.y);
+        for (int q = 0; q < kBatch; ++q) {
+          const int32_t row = __shfl_sync(0xffffffffu, mine, i + q);
+#pragma unroll
+          for (int u = 0; u < PER; ++u) x[q][u] = *row_ptr(row, u);
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+#pragma unroll
+          for (int u = 0; u < PER; ++u) {
+            acc[u].x += bf16_lo(x[q][u].x); acc[u].y += bf16_hi(x[q][u].x);
+            acc[u].z += bf16_lo(x[q][u].y); acc[u].w += bf16_hi(x[q][u].y);
+          }
+      }
+      for (; i < n; ++i) {
+        const int32_t row = __shfl_sync(0xffffffffu, mine, i);
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const uint2 x = *row_ptr(row, u);
+          acc[u].x += bf16_lo(x.x); acc[u].y += bf16_hi(x.x); acc[u].z += bf16_lo(x.y); acc[u].w += bf16_hi(x.y);
+        }
       }
     }
     if (mode == 1 || mode == 2) {

@@ -8,20 +8,22 @@
 //     dV_c = P^T . dO             dK_c = dS^T . Q             (M=128, N=d,   K=64)
 //     dQ^T += K_c^T . dS^T                                    (M=d,   N=64,  K=128)
 // dQ accumulates in tensor memory (TMEM) across chunks; dV_c and dK_c (one row per key) go
-// out as bf16 partial rows to their key-major positions in the workspace, where a separate
-// kernel sums every key's rows in a fixed order (deterministic, no float atomics).
+// out as bf16 partial rows, block-major (this CTA's k rows are contiguous), and the list of
+// every key's rows in ascending block order is written alongside; a separate kernel sums
+// every key's rows in that fixed order (deterministic, no float atomics).
 // P and dS are written once to shared memory as bf16 128-byte rows (one per key); the same
 // bytes are the K-major A operand of dV_c / dK_c and the MN-major B operand of dQ^T.
 // Roles (512 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
 // on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
-// dK_c out of TMEM into shared-memory staging rows (and write dQ at the end); warp 12
-// gathers Q, dO and the chunks' K and V rows with cp.async into separate K and V rings (V
-// is free after dP, K only after dQ); one thread of warp 13 issues the MMAs in a fixed
-// order, each group as soon as its inputs are there; warps 14-15 copy the staged partial
-// rows to global memory (d = 64; at d = 128 the readout warps copy their own rows).
-// Buffering across chunks: dV_c / dK_c in two TMEM buffers and two staging buffers (d = 64),
-// so that readout and stores of chunk c overlap the MMAs of chunk c + 1.  Every wait is
-// bounded.
+// dK_c out of TMEM into shared-memory staging rows and write the key lists (and dQ at the
+// end); warps 12 and 15 gather with cp.async, warp 12 Q, dO and the chunks' K rows, warp 15
+// their V rows, into separate rings (V is free after dP, K only after dQ); one thread of warp
+// 13 issues the MMAs
+// in a fixed order, each group as soon as its inputs are there; one thread of warp 14 sends
+// each chunk's staged rows out as one bulk copy (d = 64; at d = 128 the readout warps copy
+// their half rows themselves).  Buffering across chunks: dV_c / dK_c in two TMEM buffers and
+// two staging buffers (d = 64), so that readout and stores of chunk c overlap the MMAs of
+// chunk c + 1.  Every wait is bounded.
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -59,7 +61,8 @@ struct Sm {
 };
 
 struct Bars {
-  uint64_t full[4], empty_k[4], empty_v[4];  // per chunk slot: K and V landed / K free / V free
+  uint64_t full_k[4], full_v[4];    // per ring slot: K rows (and Q, dO with chunk 0) / V rows landed
+  uint64_t empty_k[4], empty_v[4];  // per ring slot: K free (after dQ) / V free (after dP)
   uint64_t s_full, s_empty;        // S^T, dP^T in TMEM ready / read
   uint64_t p_full[2], pds_empty[2];  // per tile pair: P, dS written / no longer read by any MMA
   uint64_t dvk_full[2], dvk_empty[2];  // per buffer: dV_c, dK_c in TMEM ready / read
@@ -86,6 +89,15 @@ DSV_DEVICE void tmem_wait_ld_into(uint32_t (&r)[2][16]) {
                  "+r"(r[h][6]), "+r"(r[h][7]), "+r"(r[h][8]), "+r"(r[h][9]), "+r"(r[h][10]), "+r"(r[h][11]),
                  "+r"(r[h][12]), "+r"(r[h][13]), "+r"(r[h][14]), "+r"(r[h][15]));
 }
+// Shared -> global bulk copy by the tensor memory accelerator, tracked by this thread's
+// bulk-async groups.
+DSV_DEVICE void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+DSV_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+DSV_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
@@ -115,7 +127,6 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   __shared__ __align__(16) float lse2_s[64];
   __shared__ __align__(16) float delta_s[64];
   __shared__ int fail_s;
-  __shared__ int64_t pos_s[2][kChunk];  // partial-row index of each staged key (-1: none)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t N = p.N, NB = p.NB, kk = p.topk;
@@ -139,7 +150,8 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   }
   if (tid == 0) {
     for (int s = 0; s < 4; ++s) {
-      tc::mbar_init(bar(bars.full[s]), 32);
+      tc::mbar_init(bar(bars.full_k[s]), 32);
+      tc::mbar_init(bar(bars.full_v[s]), 32);
       tc::mbar_init(bar(bars.empty_k[s]), 1);
       tc::mbar_init(bar(bars.empty_v[s]), 1);
     }
@@ -156,7 +168,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     tc::mbar_init(bar(bars.dq_full), 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(bars.st_full[s]), 128);
-      tc::mbar_init(bar(bars.st_empty[s]), 64);
+      tc::mbar_init(bar(bars.st_empty[s]), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     fail_s = 0;
@@ -187,17 +199,22 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   const uint32_t tmem = tmem_base_s;
 
   constexpr int KST = S::KST, VST = S::VST;
-  constexpr int FST = KST > VST ? KST : VST;  // slots of the "landed" barrier ring
   constexpr int NDVK = S::NDVK, NPDS = S::NPDS;
-  // d = 64: two store warps do nothing but copy staged partial rows out, so the SM's store
-  // path stays busy while the other roles work on later chunks
+  // d = 64: a chunk's staged partial rows leave as one bulk copy (block-major rows are
+  // contiguous); d = 128 stages half rows, which the readout warps copy out themselves
   constexpr bool kStoreWarps = D == 64;
-  if (warp == 12) {
-    // ================================================================ producer (cp.async)
-    const bf16* kh = p.k + bh * N * D;
-    const bf16* vh = p.v + bh * N * D;
-    copy_rows<D>(sQ, 64, 64, p.q, [&](int r) -> int64_t { return row0 + r; }, lane);
-    copy_rows<D>(sDO, 64, 64, p.d_o, [&](int r) -> int64_t { return row0 + r; }, lane);
+  if (warp == 12 || warp == 15) {
+    // ================================================================ producers (cp.async)
+    // warp 12 gathers Q, dO and the chunks' K rows, warp 15 the V rows: one issuing warp
+    // cannot keep both rings fed.  Each ring's "landed" barrier counts its copies.
+    const bool is_k = warp == 12;
+    if (is_k) {
+      copy_rows<D>(sQ, 64, 64, p.q, [&](int r) -> int64_t { return row0 + r; }, lane);
+      copy_rows<D>(sDO, 64, 64, p.d_o, [&](int r) -> int64_t { return row0 + r; }, lane);
+    }
+    const bf16* src_head = (is_k ? p.k : p.v) + bh * N * D;
+    const int NS = is_k ? KST : VST;
+    const uint32_t ring = is_k ? sK : sV;
     int32_t nxt[4];
     auto load_rows = [&](int c, int32_t (&rr)[4]) {
 #pragma unroll
@@ -209,30 +226,28 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     load_rows(0, nxt);
     bool ok_run = true;
     for (int c = 0; c < nchunks && ok_run; ++c) {
-      const int sk = c % KST, sv = c % VST;
+      const int st = c % NS;
       int32_t cur[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) cur[h] = nxt[h];
       load_rows(c + 1, nxt);
-      if (c >= KST) ok_run = tc::mbar_wait(bar(bars.empty_k[sk]), ((c / KST) - 1) & 1, kWaitLimit);
-      if (ok_run && c >= VST) ok_run = tc::mbar_wait(bar(bars.empty_v[sv]), ((c / VST) - 1) & 1, kWaitLimit);
+      if (c >= NS)
+        ok_run = tc::mbar_wait(bar(is_k ? bars.empty_k[st] : bars.empty_v[st]), ((c / NS) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
       constexpr int LPR = D / 8, RPI = 32 / LPR;
       const int sub = lane % LPR, rsub = lane / LPR;
-      const uint32_t dK = sK + sk * S::KV, dV = sV + sv * S::KV;
+      const uint32_t dst = ring + st * S::KV;
 #pragma unroll
       for (int it = 0; it < kChunk / RPI; ++it) {
         const int row = it * RPI + rsub;
         const int32_t j = __shfl_sync(0xffffffffu, cur[(it * RPI) >> 5], row & 31);
         const bool ok = j >= 0 && j < N;
         const int e = sub * 8;
-        const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
-        const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
-        cp_async_16(dK + off, kh + src, ok);
-        cp_async_16(dV + off, vh + src, ok);
+        cp_async_16(dst + (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63),
+                    src_head + (ok ? static_cast<int64_t>(j) : 0) * D + e, ok);
       }
-      cp_async_arrive(bar(bars.full[c % FST]));
+      cp_async_arrive(bar(is_k ? bars.full_k[st] : bars.full_v[st]));
     }
     cp_async_wait<0>();
     if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
@@ -284,11 +299,15 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       // Fixed issue order S(0), then per chunk c: S(c+1), grads(c).  S(c+1) needs only the
       // loaded stage and S^T(c) read out, both of which precede P(c); each wait blocks in the
       // hardware (no polling), so an MMA group starts as soon as its inputs are there.
-      bool ok_run = tc::mbar_wait(bar(bars.full[0]), 0, kWaitLimit);
+      auto wait_kv = [&](int c) {
+        return tc::mbar_wait(bar(bars.full_k[c % KST]), (c / KST) & 1, kWaitLimit) &&
+               tc::mbar_wait(bar(bars.full_v[c % VST]), (c / VST) & 1, kWaitLimit);
+      };
+      bool ok_run = wait_kv(0);
       if (ok_run) issue_s(0);
       for (int c = 0; c < nchunks && ok_run; ++c) {
         if (c + 1 < nchunks) {
-          ok_run = tc::mbar_wait(bar(bars.full[(c + 1) % FST]), ((c + 1) / FST) & 1, kWaitLimit) &&
+          ok_run = wait_kv(c + 1) &&
                    tc::mbar_wait(bar(bars.s_empty), c & 1, kWaitLimit);
           if (!ok_run) break;
           issue_s(c + 1);
@@ -361,36 +380,25 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::mbar_arrive(bar(bars.p_full[pb]));
     }
     if (!ok_run) atomicOr(&fail_s, 1);
-  } else if (warp >= 14) {
+  } else if (warp == 14) {
     // ================================================================ partial-row stores (d = 64)
-    // Warp 14 + w copies staged rows [64 w, 64 w + 64) of each chunk to their key-major
-    // positions, two rows per store instruction (16 lanes per 256-byte row), 8 in flight.
-    if (kStoreWarps) {
-      const int chunk = lane & 15, rsel = lane >> 4;
+    // One thread hands each chunk's staged rows (one contiguous run of block-major partial
+    // rows: 128 x 256 bytes) to the tensor memory accelerator as a single bulk copy, so the
+    // stores take no load/store-unit bandwidth from the gathers.
+    if (kStoreWarps && lane == 0) {
       bool ok_run = true;
       for (int c = 0; c < nchunks && ok_run; ++c) {
         const int b = c & 1;
         ok_run = tc::mbar_wait(bar(bars.st_full[b]), (c >> 1) & 1, kWaitLimit);
         if (!ok_run) break;
-        const uint32_t sst = sbase + S::OFF_ST + b * (kChunk * S::ROWB);
-#pragma unroll 1
-        for (int r0 = (warp - 14) * 64; r0 < (warp - 13) * 64; r0 += 16) {
-          uint4 val[8];
-          int64_t rpos[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = r0 + 2 * i + rsel;
-            rpos[i] = pos_s[b][row];
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(val[i].x), "=r"(val[i].y), "=r"(val[i].z), "=r"(val[i].w)
-                         : "r"(sst + row * S::ROWB + ((chunk ^ (row & 7)) << 4)));
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (rpos[i] >= 0) *reinterpret_cast<uint4*>(p.partial + rpos[i] * (2 * D) + chunk * 8) = val[i];
-        }
-        tc::mbar_arrive(bar(bars.st_empty[b]));  // every staged byte of this buffer has been read
+        const int64_t row0_c = static_cast<int64_t>(blockIdx.x) * kk + static_cast<int64_t>(c) * kChunk;
+        const int64_t nrows = kk - static_cast<int64_t>(c) * kChunk < kChunk ? kk - static_cast<int64_t>(c) * kChunk : kChunk;
+        bulk_store(p.partial + row0_c * (2 * D), sbase + S::OFF_ST + b * (kChunk * S::ROWB),
+                   static_cast<uint32_t>(nrows * S::ROWB));
+        bulk_wait_read();                        // the staging buffer has been read
+        tc::mbar_arrive(bar(bars.st_empty[b]));
       }
+      bulk_wait_all();  // the partial rows are written before the CTA ends
       if (!ok_run) atomicOr(&fail_s, 1);
     }
   } else {
@@ -449,10 +457,15 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::tmem_ld16(tmem + lane_base + part_col(0), r[0][0]);
       tc::tmem_ld16(tmem + lane_base + part_col(0) + 16, r[0][1]);
       tmem_wait_ld_into(r[0]);
-      if (kStoreWarps) {  // the store warps have drained this buffer's previous chunk
-        if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.st_empty[sb]), ((c >> 1) - 1) & 1, kWaitLimit);
-        pos_s[sb][te] = pos;
-      }
+      // this pair's partial row, for the reduction of key j: the list of key j's rows is in
+      // ascending block order at key-major position pos
+      const int64_t prow_index = static_cast<int64_t>(blockIdx.x) * kk + static_cast<int64_t>(c) * kChunk + te;
+      if (pos >= 0) p.lists[pos] = static_cast<int32_t>(prow_index);
+      // 16-byte chunk q of the row is staged at q ^ swz: distinct for 8 consecutive keys (no
+      // bank conflicts); d = 64 keys it on the partial row index, which the reduction undoes
+      const int swz = kStoreWarps ? static_cast<int>(prow_index & 7) : (te & 7);
+      if (kStoreWarps && c >= 2)  // the bulk copy has read this buffer's previous chunk
+        ok_run = ok_run && tc::mbar_wait(bar(bars.st_empty[sb]), ((c >> 1) - 1) & 1, kWaitLimit);
 #pragma unroll
       for (int part = 0; part < NPART; ++part) {
         const int cur = part & 1;
@@ -469,22 +482,23 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         const int base_chunk = (part % PARTS_PER_COPY) * 4;  // 16-byte chunks within the staging row
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((base_chunk + v) ^ (te & 7)) << 4)),
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((base_chunk + v) ^ swz) << 4)),
                        "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3]));
         if (!kStoreWarps && part % PARTS_PER_COPY == PARTS_PER_COPY - 1) {
           __syncwarp();
           const int half_off = (part / PARTS_PER_COPY) * (S::ROWB / 2);  // bf16 elements into the row
           const int chunk = lane & 15, rsel = lane >> 4;
 #pragma unroll
-          for (int rr = 0; rr < 32; rr += 2) {
+          for (int rr = 0; rr < 32; rr += 2) {  // the warp's 32 rows are consecutive partial rows
             const int row = rr + rsel;
-            const int64_t rpos = __shfl_sync(0xffffffffu, pos, row);
+            const int64_t slot = static_cast<int64_t>(c) * kChunk + (te & ~31) + row;
             uint4 val;
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
                          : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
                          : "r"(swarp + row * S::ROWB + ((chunk ^ (row & 7)) << 4)));
-            if (rpos >= 0)
-              *reinterpret_cast<uint4*>(p.partial + rpos * (2 * D) + half_off + chunk * 8) = val;
+            if (slot < kk)
+              *reinterpret_cast<uint4*>(p.partial + (static_cast<int64_t>(blockIdx.x) * kk + slot) * (2 * D) +
+                                        half_off + chunk * 8) = val;
           }
           __syncwarp();
         }
@@ -492,7 +506,10 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.dvk_empty[buf]));
-      if (kStoreWarps) tc::mbar_arrive(bar(bars.st_full[sb]));
+      if (kStoreWarps) {
+        tc::fence_async_shared();  // staged rows visible to the bulk copy
+        tc::mbar_arrive(bar(bars.st_full[sb]));
+      }
     }
     // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
     ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);

@@ -61,8 +61,12 @@ struct BwdParams {
   uint32_t* colbits;   // [nh][W32][N]   bit lb of word (lb / 32): block lb selected key j
   uint32_t* colpre;    // [nh][W32][N]   popcount of the words before
   uint32_t* count;     // [nh][N]
-  int64_t* offsets;    // [nh][N]        first partial row of key j (absolute within the wave)
-  bf16* partial;       // [pairs][2 d]   dK part, then dV part (bf16; summed in fp32)
+  int64_t* offsets;    // [nh][N]        first key-major position of key j (absolute within the wave)
+  int32_t* lists;      // [pairs]        partial row of each key-major position: key j's rows in
+                       //                ascending query-block order
+  bf16* partial;       // [pairs][2 d]   BLOCK-major rows (CTA c's k rows at c k): dK part times the
+                       //                scale, then dV part (bf16; summed in fp32); at d = 64 the
+                       //                16-byte chunks of row n are stored XOR (n & 7)
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
 };
 cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream);
