@@ -105,6 +105,22 @@ def oracle_sample(wl, budget_s, cache={}):
     return 14.0 * 64 * nblocks * wl.k * wl.d, dt, nblocks
 
 
+def max_over_ranks(ms, dev, world):
+    """The slowest rank's time (the job is done when every rank is); identity for one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, steps, flop_per_rank_step, ms):
+    """Whole-job throughput: every rank's work over the slowest rank's time (weak scaling)."""
+    return world * steps * flop_per_rank_step / (ms / 1e3) / 1e12
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -332,11 +348,9 @@ def dsv_arm(args):
     total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     if world > 1:
         dist.barrier()
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, world)
     fl = flops_per_step(wl)
-    value = world * args.steps * fl / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, args.steps, fl, total_ms)
     ms_per_step = total_ms / args.steps
 
     # ---- stage breakdown (separately timed, same inputs)
@@ -381,12 +395,8 @@ def dsv_arm(args):
             if i >= 2:
                 b.record()
             torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in ev)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * n_e2e * fl / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev, world)
+        e2e = {"value": job_tflops(world, n_e2e, fl, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / n_e2e, "steps": n_e2e}
 
     # ---- dense comparator (PyTorch SDPA fwd+bwd on the same shape)
