@@ -90,6 +90,74 @@ def estimate_topk(q_lr, k_lr, block: int, k: int, blocks: Optional[Iterable[int]
 
 # ---------------------------------------------------------------- sparse attention
 
+# ---------------------------------------------------------------- mass-based adaptive k
+# DSV pages, German summary section 2A (stage 2) and Spanish "Fase 2": the low-rank
+# predictors estimate the critical KV pairs, those that make up ~90 % of the attention score.
+# Readings (the pages give no formula):
+#   * a block's estimated attention distribution over keys is softmax_j(tau * s[b, j]), with
+#     tau = 1/64 by default: s is the SUM over the block's 64 queries, tau/s the mean logit;
+#   * the critical set is the shortest prefix of the keys in (score desc, key index asc)
+#     order whose estimated mass reaches the fraction `mass` of the total;
+#   * the mass is taken in integer weights so that the decision is exactly reproducible:
+#     w_j = floor(2^24 * 2^x_j), x_j = tau_log2 * (s_j - max_j s_j) in fp32 (tau_log2 =
+#     tau * log2(e) rounded to fp32), 2^x from the fp32 recipe exp2_recipe(); the target is
+#     ceil(W * mass_num / 2^16) with W = sum_j w_j and mass_num = round(mass * 2^16).
+
+EXP2_TAYLOR = [np.float32(math.log(2.0) ** i / math.factorial(i)) for i in range(7)]
+
+
+def exp2_recipe(x) -> np.ndarray:
+    """2^x for fp32 x <= 0 by the fixed fp32 recipe both the oracle and the kernels follow:
+    n = floor(x), f = x - n (exact), 2^f from its Taylor series to degree 6 in Horner form
+    (every product and sum rounded to fp32, nothing fused), then scaled by 2^n (exact)."""
+    x = np.asarray(x, dtype=np.float32)
+    n = np.floor(x).astype(np.float32)
+    f = (x - n).astype(np.float32)
+    p = np.float32(EXP2_TAYLOR[6]) * np.ones_like(f)
+    for c in EXP2_TAYLOR[5::-1]:
+        p = (p * f).astype(np.float32)
+        p = (p + c).astype(np.float32)
+    return np.ldexp(p, n.astype(np.int32)).astype(np.float32)
+
+
+def mass_weights(scores_row, tau_log2: float) -> np.ndarray:
+    """Integer weights w_j (uint64) of one block's keys; 0 once 2^x < 2^-30."""
+    s = np.asarray(scores_row, dtype=np.float64)
+    smax = s.max()
+    x = (np.float32(tau_log2) * (s - smax).astype(np.float32)).astype(np.float32)
+    w = np.zeros(s.shape, dtype=np.uint64)
+    live = x >= np.float32(-30.0)
+    w[live] = np.floor(exp2_recipe(x[live]).astype(np.float64) * 2.0 ** 24).astype(np.uint64)
+    return w
+
+
+def mass_target(total: int, mass_num: int) -> int:
+    """The smallest integer weight t with t >= total * mass_num / 2^16."""
+    return (int(total) * int(mass_num) + 65535) >> 16
+
+
+def mass_k(scores, tau_log2: float, mass_num: int) -> np.ndarray:
+    """Per block the size of the shortest (score desc, key asc) prefix whose weight reaches
+    ceil(W * mass_num / 2^16) -> int32 [NB]."""
+    scores = np.asarray(scores, dtype=np.float64)
+    out = np.empty(scores.shape[0], dtype=np.int32)
+    for b in range(scores.shape[0]):
+        order = np.lexsort((np.arange(scores.shape[1]), -scores[b]))
+        w = mass_weights(scores[b], tau_log2)[order]
+        target = mass_target(int(w.sum()), mass_num)
+        cum = np.cumsum(w.astype(object))           # exact integers
+        out[b] = int(np.argmax(cum >= target)) + 1
+    return out
+
+
+def estimate_mass_topk(q_lr, k_lr, block: int, tau_log2: float, mass_num: int):
+    """Adaptive selection: per block its mass-based k, then its top-k keys (ascending).
+    Returns (k per block int32 [NB], list of per-block index arrays)."""
+    s = block_scores(block_representatives(q_lr, block), k_lr)
+    ks = mass_k(s, tau_log2, mass_num)
+    return ks, [topk_select(s[b:b + 1], int(ks[b]))[0] for b in range(s.shape[0])]
+
+
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
@@ -104,7 +172,7 @@ def sparse_attn_fwd(q, k, v, idx, block: int, scale: Optional[float] = None,
     Returns O [N, d] and LSE [N] (fp64); rows of blocks not computed are NaN.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    idx = np.asarray(idx)
+    idx = idx if isinstance(idx, (list, tuple)) else np.asarray(idx)  # per-block lists may be ragged
     n, d = q.shape
     if scale is None:
         scale = default_scale(d)
@@ -135,7 +203,7 @@ def sparse_attn_bwd(do, q, k, v, idx, block: int, scale: Optional[float] = None,
     to have dO = 0, which is what zeroing dO outside them does exactly).
     """
     do, q, k, v = _f64(do), _f64(q), _f64(k), _f64(v)
-    idx = np.asarray(idx)
+    idx = idx if isinstance(idx, (list, tuple)) else np.asarray(idx)  # per-block lists may be ragged
     n, d = q.shape
     if scale is None:
         scale = default_scale(d)
