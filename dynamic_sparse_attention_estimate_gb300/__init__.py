@@ -7,7 +7,9 @@ load the library; the first call does, and fails loudly if it has not been built
 """
 from .binding import (  # noqa: F401
     DSVError,
+    dsv_estimate_mass_k,
     dsv_estimate_topk,
+    dsv_estimate_topk_csr,
     dsv_estimate_topk_workspace,
     dsv_sparse_attn_bwd,
     dsv_sparse_attn_bwd_workspace,

@@ -26,6 +26,7 @@ EXPORTED = (
     "dsv_sparse_attn_bwd_workspace", "dsv_sparse_attn_bwd_workspace_min", "dsv_sparse_attn_bwd",
     "dsv_status_string", "dsv_last_error_message", "dsv_last_device_status",
     "dsv_profile_enable", "dsv_profile_read", "dsv_sparse_attn_bwd_noalloc",
+    "dsv_estimate_mass_k", "dsv_estimate_topk_csr",
 )
 
 
@@ -76,6 +77,10 @@ def load_library(path: Optional[str] = None):
     lib.dsv_last_device_status.restype = st
     lib.dsv_sparse_attn_bwd_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.dsv_sparse_attn_bwd_noalloc.restype = st
+    lib.dsv_estimate_mass_k.argtypes = [dp, vp, vp, ctypes.c_float, ctypes.c_uint32, vp, vp, vp]
+    lib.dsv_estimate_mass_k.restype = st
+    lib.dsv_estimate_topk_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp]
+    lib.dsv_estimate_topk_csr.restype = st
     lib.dsv_profile_enable.argtypes = [st]
     lib.dsv_profile_enable.restype = st
     lib.dsv_profile_read.argtypes = [ctypes.c_char_p, sz]
@@ -136,6 +141,53 @@ def dsv_estimate_topk(q_lr: torch.Tensor, k_lr: torch.Tensor, k: int, block: int
     _check(lib.dsv_estimate_topk(ctypes.byref(dims), _ptr(q_lr), _ptr(k_lr), _ptr(idx), _ptr(ws), ws_bytes,
                                  _stream_ptr(q_lr)), "dsv_estimate_topk")
     return idx
+
+
+def mass_parameters(tau: float, mass: float) -> Tuple[float, int]:
+    """(tau_log2, mass_num) as dsv_estimate_mass_k takes them: tau * log2(e) rounded to fp32,
+    and the mass fraction in units of 2^-16 (rounded, 1 .. 65536)."""
+    import numpy as np
+    tau_log2 = float(np.float32(float(tau) / 0.6931471805599453))
+    mass_num = int(min(65536, max(1, round(float(mass) * 65536))))
+    return tau_log2, mass_num
+
+
+def dsv_estimate_mass_k(q_lr: torch.Tensor, k_lr: torch.Tensor, tau: float = 1.0 / 64, mass: float = 0.9,
+                        block: int = 64, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """(k_row int32 [B, H, N/block], rowptr int64 [B*H*N/block + 1]): per query block the
+    smallest number of top keys that carry the fraction `mass` of the estimated attention
+    mass softmax_j(tau s[b, j]) (see include/dsv.h)."""
+    _need(q_lr, "q_lr", torch.bfloat16, 4)
+    _need(k_lr, "k_lr", torch.bfloat16, 4)
+    B, H, N, r = q_lr.shape
+    if k_lr.shape != q_lr.shape:
+        raise ValueError("q_lr and k_lr must have the same shape")
+    dims = make_dims(B, H, N, 0, r, max(N, 1), block)
+    NB = max(N // block, 0)
+    if out is None:
+        k_row = torch.empty((B, H, NB), dtype=torch.int32, device=q_lr.device)
+        rowptr = torch.empty((B * H * NB + 1,), dtype=torch.int64, device=q_lr.device)
+    else:
+        k_row, rowptr = out
+    tau_log2, mass_num = mass_parameters(tau, mass)
+    _check(load_library().dsv_estimate_mass_k(ctypes.byref(dims), _ptr(q_lr), _ptr(k_lr), tau_log2, mass_num,
+                                              _ptr(k_row), _ptr(rowptr), _stream_ptr(q_lr)), "dsv_estimate_mass_k")
+    return k_row, rowptr
+
+
+def dsv_estimate_topk_csr(q_lr: torch.Tensor, k_lr: torch.Tensor, k_row: torch.Tensor, rowptr: torch.Tensor,
+                          block: int = 64, cols: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """cols int32 [rowptr[-1]]: row i's k_row[i] top keys (ascending) at cols[rowptr[i]:rowptr[i+1]].
+    Without `cols` the total is read from the device (a synchronisation)."""
+    _need(q_lr, "q_lr", torch.bfloat16, 4)
+    _need(k_lr, "k_lr", torch.bfloat16, 4)
+    B, H, N, r = q_lr.shape
+    dims = make_dims(B, H, N, 0, r, max(N, 1), block)
+    if cols is None:
+        cols = torch.empty((int(rowptr[-1].item()),), dtype=torch.int32, device=q_lr.device)
+    _check(load_library().dsv_estimate_topk_csr(ctypes.byref(dims), _ptr(q_lr), _ptr(k_lr), _ptr(k_row), _ptr(rowptr),
+                                                _ptr(cols), _stream_ptr(q_lr)), "dsv_estimate_topk_csr")
+    return cols
 
 
 def dsv_sparse_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, block: int = 64,

@@ -213,6 +213,68 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
   return ok();
 }
 
+dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const void* k_lr, float tau_log2,
+                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, void* stream) {
+  dsv_status s = check_dims(dims, false, true);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(q_lr);
+  DSV_NEED_PTR(k_lr);
+  if (!k_row) return fail(DSV_ERR_INVALID_ARG, "k_row is NULL");
+  if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
+  if (!(tau_log2 > 0.f) || !(tau_log2 < 3.0e38f)) return fail(DSV_ERR_INVALID_ARG, "tau_log2 must be finite and > 0");
+  if (mass_num < 1 || mass_num > 65536) return fail(DSV_ERR_INVALID_ARG, "mass_num must be in [1, 65536] (got %u)", mass_num);
+  if (dims->N > (1LL << 20))
+    return fail(DSV_ERR_UNSUPPORTED, "mass selection supports N <= 2^20 (the weight sums are 64-bit)");
+  unsigned int* status = nullptr;
+  if ((s = status_word(&status)) != DSV_OK) return s;
+  dsv::MassParams p;
+  p.q_lr = static_cast<const dsv::bf16*>(q_lr);
+  p.k_lr = static_cast<const dsv::bf16*>(k_lr);
+  p.BH = dims->B * dims->H;
+  p.N = dims->N;
+  p.NB = dims->N / dims->block;
+  p.r = static_cast<int>(dims->r);
+  p.tau_log2 = tau_log2;
+  p.mass_num = mass_num;
+  double fact = 1.0;
+  for (int i = 0; i < 7; ++i) {  // Taylor coefficients of 2^f: (ln 2)^i / i!, rounded to fp32
+    if (i > 0) fact *= i;
+    p.coef[i] = static_cast<float>(std::pow(std::log(2.0), i) / fact);
+  }
+  p.krow = k_row;
+  p.rowptr = rowptr;
+  p.status = status;
+  cudaError_t e = dsv::launch_estimate_mass_k(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "mass selection launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const void* k_lr, const int32_t* k_row,
+                                 const int64_t* rowptr, int32_t* cols, void* stream) {
+  dsv_status s = check_dims(dims, false, true);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(q_lr);
+  DSV_NEED_PTR(k_lr);
+  if (!k_row || !rowptr || !cols) return fail(DSV_ERR_INVALID_ARG, "k_row, rowptr and cols must be non-NULL");
+  unsigned int* status = nullptr;
+  if ((s = status_word(&status)) != DSV_OK) return s;
+  dsv::EstimateParams p;
+  p.q_lr = static_cast<const dsv::bf16*>(q_lr);
+  p.k_lr = static_cast<const dsv::bf16*>(k_lr);
+  p.idx = cols;
+  p.BH = dims->B * dims->H;
+  p.N = dims->N;
+  p.NB = dims->N / dims->block;
+  p.topk = dims->N;
+  p.r = static_cast<int>(dims->r);
+  p.krow = k_row;
+  p.rowptr = rowptr;
+  p.status = status;
+  cudaError_t e = dsv::launch_estimate_topk(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "estimate launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
                                void* o, float* lse, void* stream) {
   dsv_status s = check_dims(dims, true, false);

@@ -177,7 +177,8 @@ DSV_DEVICE void hist_pass(const Frags<R>& A, const bf16* __restrict__ kh, int N,
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
 estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_lr, int32_t* __restrict__ idx,
-                     int N, int NB, int k, unsigned int* status) {
+                     int N, int NB, int k, const int32_t* __restrict__ krow, const int64_t* __restrict__ rowptr,
+                     unsigned int* status) {
   extern __shared__ uint32_t hist[];  // [kRows][kBins]; in the emit phase: gt / eq bitmaps
   __shared__ float qhat[kRows][R];
   __shared__ RowState rs[kRows];
@@ -190,7 +191,12 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
   const int nrows = NB - row0 < kRows ? NB - row0 : kRows;
   const bf16* qh = q_lr + bh * static_cast<int64_t>(N) * R;
   const bf16* kh = k_lr + bh * static_cast<int64_t>(N) * R;
-  int32_t* out = idx + (bh * NB + row0) * static_cast<int64_t>(k);
+  // per row: its k (krow, or the uniform k) and where its indices go (CSR offsets, or row * k)
+  const int64_t grow0 = bh * NB + row0;
+  auto row_k = [&](int row) -> int { return krow ? krow[grow0 + row] : k; };
+  auto row_out = [&](int row) -> int32_t* {
+    return idx + (rowptr ? rowptr[grow0 + row] : (grow0 + row) * static_cast<int64_t>(k));
+  };
 
   // ---- query grouping: q_hat[row] = sum of the block's 64 Q_lr rows (fp32, exact for integers)
   for (int p = tid; p < kRows * R; p += kThreads) {
@@ -203,7 +209,7 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     qhat[row][c] = acc;
   }
   for (int i = tid; i < kRows * kBins; i += kThreads) hist[i] = 0u;
-  if (tid < kRows) rs[tid] = RowState{0u, 0, k, 0u, 0, 0u};
+  if (tid < kRows) rs[tid] = RowState{0u, 0, tid < nrows ? row_k(tid) : k, 0u, 0, 0u};
   __syncthreads();
 
   // ---- A fragments: q_hat = hi + lo (bf16), with the k order permuted so each thread's
@@ -316,7 +322,8 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
       const int nwords = (seg_end - seg) >> 5;
       const uint32_t* gw = gtb + warp * kSegWords;
       const uint32_t* ew = eqb + warp * kSegWords;
-      int32_t* orow = out + static_cast<int64_t>(warp) * k;
+      int32_t* orow = row_out(warp);
+      const int kw = row_k(warp);
       for (int w0 = 0; w0 < nwords; w0 += 32) {
         const int w = w0 + lane;
         const uint32_t gv = w < nwords ? gw[w] : 0u;
@@ -354,7 +361,7 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
         while (sel) {
           const int b = __ffs(sel) - 1;
           sel &= sel - 1;
-          if (o < k) orow[o] = key0 + b;
+          if (o < kw) orow[o] = key0 + b;
           else flag_status(status, kStatusBadIndex);
           ++o;
         }
@@ -364,6 +371,329 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     }
     __syncthreads();
   }
+}
+
+// ---------------------------------------------------------------- mass-based adaptive k
+// Per query block the length of the shortest (score desc, key asc) prefix of its keys whose
+// estimated attention mass reaches the fraction mass_num / 2^16 of the total (DSV pages,
+// German summary section 2A stage 2 and Spanish "Fase 2": the critical pairs carry ~90 % of
+// the attention score).  Mass is counted in integer weights w = floor(2^24 * 2^x), x =
+// tau_log2 * (s - max s), with 2^x by one fixed fp32 recipe (x = n + f, 2^f from its Taylor
+// series to degree 6, every product and sum rounded separately), so the integer decision is
+// reproducible bit for bit.  The search is a radix select on the score's order-preserving
+// key, with per-bin weight sums and counts instead of counts alone:
+//   0. exact row maximum;  1. weights and counts per bin of key bits [31:21], total W;
+//   2. inside the bin where the running weight from the top reaches ceil(W mass), bins of
+//      bits [20:10] (exact when no member has bits [9:0] set: integer scores);
+//   3. otherwise bits [9:0];
+// then k = (keys above the threshold value T) + ceil((target - their weight) / w(T)).
+constexpr int kMassRows = 8;  // query blocks per CTA (MMA rows 8..15 stay zero)
+
+struct MassState {
+  unsigned long long total, target, w_above;
+  uint32_t c_above, maxkey, prefix, orbits;
+  int level;
+};
+
+struct MassCoef {
+  float c[7];
+};
+
+DSV_DEVICE float key_value(uint32_t key) {  // inverse of order_key
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+DSV_DEVICE uint32_t mass_weight(float s, float smax, float tau_log2, const MassCoef& c) {
+  const float x = __fmul_rn(tau_log2, __fsub_rn(s, smax));
+  if (!(x >= -30.f)) return 0u;
+  const float n = floorf(x);
+  const float f = __fsub_rn(x, n);  // exact
+  float p = c.c[6];
+#pragma unroll
+  for (int i = 5; i >= 0; --i) p = __fadd_rn(__fmul_rn(p, f), c.c[i]);
+  return __float2uint_rz(ldexpf(p, static_cast<int>(n) + 24));
+}
+
+// Warp search over one row's per-bin weights hw and counts hc, from the top bin down: the
+// bin where the running weight (starting at w0) first reaches `target`, the running weight
+// before it and the count of this level's bins above it.
+DSV_DEVICE void warp_find_mass_bin(const unsigned long long* hw, const uint32_t* hc, int nbins, unsigned long long w0,
+                                   unsigned long long target, int lane, int& bin, unsigned long long& w_above,
+                                   uint32_t& c_above) {
+  const int per = nbins / 32;
+  const int hi = nbins - lane * per;  // this lane's bins: [hi - per, hi)
+  unsigned long long sw = 0;
+  uint32_t sc = 0;
+  for (int i = 0; i < per; ++i) {
+    const int b = hi - 1 - ((i + lane) % per);
+    sw += hw[b];
+    sc += hc[b];
+  }
+  unsigned long long iw = sw;
+  uint32_t ic = sc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long vw = __shfl_up_sync(0xffffffffu, iw, o);
+    const uint32_t vc = __shfl_up_sync(0xffffffffu, ic, o);
+    if (lane >= o) {
+      iw += vw;
+      ic += vc;
+    }
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, w0 + iw >= target);
+  const int L = m ? __ffs(m) - 1 : 31;
+  int rb = 0;
+  unsigned long long rw = 0;
+  uint32_t rc = 0;
+  if (lane == L) {
+    unsigned long long acc = w0 + iw - sw;
+    uint32_t cacc = ic - sc;
+    for (int i = 0; i < per; ++i) {
+      const int b = hi - 1 - i;
+      if (acc + hw[b] >= target || i == per - 1) {
+        rb = b;
+        rw = acc;
+        rc = cacc;
+        break;
+      }
+      acc += hw[b];
+      cacc += hc[b];
+    }
+  }
+  bin = __shfl_sync(0xffffffffu, rb, L);
+  w_above = __shfl_sync(0xffffffffu, rw, L);
+  c_above = __shfl_sync(0xffffffffu, rc, L);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+mass_k_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_lr, int N, int NB, float tau_log2,
+              uint32_t mass_num, MassCoef coef, int32_t* __restrict__ krow) {
+  extern __shared__ unsigned long long mhw[];                            // [rows][kBins] weights
+  uint32_t* mhc = reinterpret_cast<uint32_t*>(mhw + kMassRows * kBins);  // [rows][kBins] counts
+  __shared__ float qhat[16][R];
+  __shared__ MassState ms[kMassRows];
+  __shared__ int pending;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t bh = blockIdx.y;
+  const int row0 = blockIdx.x * kMassRows;
+  const int nrows = NB - row0 < kMassRows ? NB - row0 : kMassRows;
+  const bf16* qh = q_lr + bh * static_cast<int64_t>(N) * R;
+  const bf16* kh = k_lr + bh * static_cast<int64_t>(N) * R;
+
+  for (int p = tid; p < 16 * R; p += kThreads) {
+    const int row = p / R, c = p % R;
+    float acc = 0.f;
+    if (row < nrows) {
+      const bf16* src = qh + static_cast<int64_t>(row0 + row) * 64 * R + c;
+      for (int i = 0; i < 64; ++i) acc += __bfloat162float(src[i * R]);
+    }
+    qhat[row][c] = acc;
+  }
+  auto clear = [&]() {
+    for (int i = tid; i < kMassRows * kBins; i += kThreads) {
+      mhw[i] = 0ull;
+      mhc[i] = 0u;
+    }
+  };
+  clear();
+  if (tid < kMassRows) ms[tid] = MassState{0ull, 0ull, 0ull, 0u, 0u, 0u, 0u, 0};
+  __syncthreads();
+
+  Frags<R> A;  // q_hat = hi + lo (bf16), as in the top-k kernel
+#pragma unroll
+  for (int ks = 0; ks < Frags<R>::KS; ++ks) {
+    const int c0 = ks * 16 + 4 * t;
+    const float x[4][2] = {{qhat[g][c0], qhat[g][c0 + 1]}, {qhat[g + 8][c0], qhat[g + 8][c0 + 1]},
+                           {qhat[g][c0 + 2], qhat[g][c0 + 3]}, {qhat[g + 8][c0 + 2], qhat[g + 8][c0 + 3]}};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x[i][0]));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x[i][1]));
+      A.hi[ks][i] = pack_bf16x2(h0, h1);
+      A.lo[ks][i] = pack_bf16x2(x[i][0] - h0, x[i][1] - h1);
+    }
+  }
+  const bool act = g < nrows;  // this thread's row is g (MMA rows g + 8 are unused)
+  uint32_t* hcr = mhc + g * kBins;
+  unsigned long long* hwr = mhw + g * kBins;
+
+  // ---- 0. exact row maximum
+  uint32_t mk = 0u;
+  for_each_group<R>(A, kh, N, 0, N, warp, g, t, [&](int, const float (&sc)[4][4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) mk = max(mk, order_key(sc[j][e]));
+  });
+  mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, 1));
+  mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, 2));
+  if (act && t == 0) atomicMax(&ms[g].maxkey, mk);
+  __syncthreads();
+  const float smax = key_value(ms[g].maxkey);
+
+  // ---- 1. weights per bin of bits [31:21], and the total
+  unsigned long long tot = 0ull;
+  for_each_group<R>(A, kh, N, 0, N, warp, g, t, [&](int, const float (&sc)[4][4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t w = act ? mass_weight(sc[j][e], smax, tau_log2, coef) : 0u;
+        if (w == 0u) continue;
+        const uint32_t key = order_key(sc[j][e]);
+        atomicAdd(hwr + (key >> 21), static_cast<unsigned long long>(w));
+        atomicAdd(hcr + (key >> 21), 1u);
+        tot += w;
+      }
+  });
+  tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+  if (act && t == 0) atomicAdd(&ms[g].total, tot);
+  __syncthreads();
+  if (warp < nrows) {
+    MassState st = ms[warp];
+    st.target = (st.total * mass_num + 65535ull) >> 16;
+    int bin;
+    unsigned long long wa;
+    uint32_t ca;
+    warp_find_mass_bin(mhw + warp * kBins, mhc + warp * kBins, kBins, 0ull, st.target, lane, bin, wa, ca);
+    st.prefix = static_cast<uint32_t>(bin);
+    st.w_above = wa;
+    st.c_above = ca;
+    st.level = 1;
+    __syncwarp();
+    if (lane == 0) ms[warp] = st;
+    __syncwarp();
+  }
+  __syncthreads();
+  clear();
+  __syncthreads();
+
+  // ---- 2. inside that bin: bits [20:10]
+  {
+    const uint32_t pre = ms[g].prefix;
+    for_each_group<R>(A, kh, N, 0, N, warp, g, t, [&](int, const float (&sc)[4][4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t key = order_key(sc[j][e]);
+          if (!act || (key >> 21) != pre) continue;
+          const uint32_t w = mass_weight(sc[j][e], smax, tau_log2, coef);
+          if (w == 0u) continue;
+          atomicAdd(hwr + ((key >> 10) & 2047u), static_cast<unsigned long long>(w));
+          atomicAdd(hcr + ((key >> 10) & 2047u), 1u);
+          if (key & 1023u) atomicOr(&ms[g].orbits, key & 1023u);
+        }
+    });
+  }
+  __syncthreads();
+  if (warp < nrows) {
+    MassState st = ms[warp];
+    int bin;
+    unsigned long long wa;
+    uint32_t ca;
+    warp_find_mass_bin(mhw + warp * kBins, mhc + warp * kBins, kBins, st.w_above, st.target, lane, bin, wa, ca);
+    st.prefix = (st.prefix << 11) | static_cast<uint32_t>(bin);
+    st.w_above = wa;
+    st.c_above += ca;
+    st.level = st.orbits == 0u ? 3 : 2;  // no member below bit 10: the key is exact
+    __syncwarp();
+    if (lane == 0) ms[warp] = st;
+    __syncwarp();
+  }
+  if (tid == 0) pending = 0;
+  __syncthreads();
+  if (tid < nrows && ms[tid].level == 2) atomicOr(&pending, 1);
+  __syncthreads();
+
+  // ---- 3. if needed: bits [9:0]
+  if (pending) {
+    clear();
+    __syncthreads();
+    const uint32_t pre = ms[g].prefix;
+    const bool need = act && ms[g].level == 2;
+    for_each_group<R>(A, kh, N, 0, N, warp, g, t, [&](int, const float (&sc)[4][4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t key = order_key(sc[j][e]);
+          if (!need || (key >> 10) != pre) continue;
+          const uint32_t w = mass_weight(sc[j][e], smax, tau_log2, coef);
+          if (w == 0u) continue;
+          atomicAdd(hwr + (key & 1023u), static_cast<unsigned long long>(w));
+          atomicAdd(hcr + (key & 1023u), 1u);
+        }
+    });
+    __syncthreads();
+    if (warp < nrows && ms[warp].level == 2) {
+      MassState st = ms[warp];
+      int bin;
+      unsigned long long wa;
+      uint32_t ca;
+      warp_find_mass_bin(mhw + warp * kBins, mhc + warp * kBins, 1024, st.w_above, st.target, lane, bin, wa, ca);
+      st.prefix = (st.prefix << 10) | static_cast<uint32_t>(bin);
+      st.w_above = wa;
+      st.c_above += ca;
+      st.level = 4;
+      __syncwarp();
+      if (lane == 0) ms[warp] = st;
+      __syncwarp();
+    }
+    __syncthreads();
+  }
+
+  // ---- k = keys above T + the keys equal to T needed to reach the target
+  if (warp < nrows && lane == 0) {
+    const MassState st = ms[warp];
+    const uint32_t T = st.level == 3 ? (st.prefix << 10) : st.prefix;
+    const unsigned long long wt = mass_weight(key_value(T), key_value(st.maxkey), tau_log2, coef);
+    const unsigned long long n_tie = wt ? (st.target - st.w_above + wt - 1ull) / wt : 0ull;
+    krow[bh * NB + row0 + warp] = static_cast<int32_t>(st.c_above + n_tie);
+  }
+}
+
+// CSR row offsets: rowptr[0] = 0, rowptr[i + 1] = krow[0] + ... + krow[i] (one CTA).
+__global__ void __launch_bounds__(1024) csr_scan_kernel(const int32_t* __restrict__ krow, int64_t rows,
+                                                        int64_t* __restrict__ rowptr) {
+  __shared__ long long part[1024];
+  const int t = threadIdx.x;
+  const int64_t per = (rows + 1023) / 1024;
+  const int64_t b = t * per, e = b + per < rows ? b + per : rows;
+  long long s = 0;
+  for (int64_t i = b; i < e; ++i) s += krow[i];
+  part[t] = s;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {
+    const long long v = t >= o ? part[t - o] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  long long run = part[t] - s;
+  if (t == 0) rowptr[0] = 0;
+  for (int64_t i = b; i < e; ++i) {
+    run += krow[i];
+    rowptr[i + 1] = run;
+  }
+}
+
+template <int R>
+cudaError_t launch_mass_r(const MassParams& p, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(kMassRows) * kBins * (sizeof(unsigned long long) + sizeof(uint32_t));
+  cudaError_t e = cudaFuncSetAttribute(mass_k_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  MassCoef coef;
+  for (int i = 0; i < 7; ++i) coef.c[i] = p.coef[i];
+  dim3 grid(static_cast<unsigned>((p.NB + kMassRows - 1) / kMassRows), static_cast<unsigned>(p.BH));
+  ProfScope prof("estimate_mass_k", stream);
+  mass_k_kernel<R><<<grid, kThreads, smem, stream>>>(p.q_lr, p.k_lr, static_cast<int>(p.N), static_cast<int>(p.NB),
+                                                     p.tau_log2, p.mass_num, coef, p.krow);
+  return cudaGetLastError();
 }
 
 // k == N: every key of every block, ascending.
@@ -383,15 +713,30 @@ cudaError_t launch_r(const EstimateParams& p, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>((p.NB + kRows - 1) / kRows), static_cast<unsigned>(p.BH));
   ProfScope prof("estimate_topk", stream);
   estimate_topk_kernel<R><<<grid, kThreads, smem, stream>>>(p.q_lr, p.k_lr, p.idx, static_cast<int>(p.N),
-                                                             static_cast<int>(p.NB), static_cast<int>(p.topk),
-                                                             p.status);
+                                                             static_cast<int>(p.NB), static_cast<int>(p.topk), p.krow,
+                                                             p.rowptr, p.status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+cudaError_t launch_estimate_mass_k(const MassParams& p, cudaStream_t stream) {
+  cudaError_t e;
+  switch (p.r) {
+    case 16: e = launch_mass_r<16>(p, stream); break;
+    case 32: e = launch_mass_r<32>(p, stream); break;
+    case 48: e = launch_mass_r<48>(p, stream); break;
+    case 64: e = launch_mass_r<64>(p, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  ProfScope prof("csr_scan", stream);
+  csr_scan_kernel<<<1, 1024, 0, stream>>>(p.krow, p.BH * p.NB, p.rowptr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_estimate_topk(const EstimateParams& p, cudaStream_t stream) {
-  if (p.topk == p.N) {
+  if (p.topk == p.N && !p.krow) {
     ProfScope prof("estimate_arange", stream);
     arange_kernel<<<4 * 152, 256, 0, stream>>>(p.idx, p.BH * p.NB, p.topk);
     return cudaGetLastError();

@@ -22,12 +22,33 @@ struct ProfScope {
 struct EstimateParams {
   const bf16* q_lr;   // [BH][N][r]
   const bf16* k_lr;   // [BH][N][r]
-  int32_t* idx;       // [BH][NB][k]
+  int32_t* idx;       // [BH][NB][k], or CSR columns when rowptr is set
   int64_t BH, N, NB, topk;
   int r;
+  const int32_t* krow = nullptr;   // per-row k (adaptive selection), or null: topk for every row
+  const int64_t* rowptr = nullptr; // CSR row offsets into idx, or null: row * topk
   unsigned int* status;
 };
 cudaError_t launch_estimate_topk(const EstimateParams& p, cudaStream_t stream);
+
+// Mass-based adaptive k: per query block the length of the shortest (score desc, key asc)
+// prefix of its keys whose integer weight reaches ceil(W * mass_num / 2^16); weights
+// w = floor(2^24 * 2^x), x = tau_log2 * (s - max s) in fp32, 2^x by a fixed fp32 recipe
+// (Taylor coefficients coef[0..6] of 2^f on [0, 1)).  Writes krow [BH][NB] and the CSR
+// offsets rowptr [BH * NB + 1].
+struct MassParams {
+  const bf16* q_lr;
+  const bf16* k_lr;
+  int64_t BH, N, NB;
+  int r;
+  float tau_log2;
+  uint32_t mass_num;
+  float coef[7];
+  int32_t* krow;
+  int64_t* rowptr;
+  unsigned int* status;
+};
+cudaError_t launch_estimate_mass_k(const MassParams& p, cudaStream_t stream);
 
 struct FwdParams {
   const bf16 *q, *k, *v;  // [BH][N][d]

@@ -76,6 +76,41 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
                              int32_t* idx, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Mass-based adaptive k per query block (DSV German summary section 2A, stage 2, and
+ * Spanish summary "Fase 2": the critical KV pairs are those that make up ~90 % of the
+ * attention score).  A block's estimated attention distribution over keys is
+ * softmax_j(tau s[b, j]) with s the block logits above; k_row[b] is the length of the
+ * shortest prefix of its keys, in (s desc, key asc) order, whose mass reaches the fraction
+ * mass_num / 2^16 of the total.  The mass is counted in integer weights
+ *   w_j = floor(2^24 * 2^x_j),  x_j = tau_log2 * (s[b, j] - max_j s[b, j])  (fp32),
+ * 2^x by a fixed fp32 recipe (x = n + f, n = floor(x); 2^f from its Taylor series to degree
+ * 6 with coefficients (ln 2)^i / i! rounded to fp32, evaluated in Horner form with every
+ * product and sum rounded separately; then scaled by 2^n), w_j = 0 when x_j < -30, and the
+ * target is ceil(W * mass_num / 2^16) with W = sum_j w_j.  So the selection is exactly
+ * reproducible (for integer-valued factors, as for dsv_estimate_topk).
+ *   tau_log2: tau * log2(e) as fp32, > 0 (tau: the estimate's inverse temperature; for a
+ *             block-summed logit of 64 queries, 1/64 takes the mean);
+ *   mass_num: the mass fraction times 2^16, 1 .. 65536 (0.9 -> 58982);
+ *   k_row:    int32 [B][H][N/block] (output), 1 <= k_row[b] <= N;
+ *   rowptr:   int64 [B*H*N/block + 1] (output), the CSR offsets: rowptr[0] = 0,
+ *             rowptr[i + 1] = rowptr[i] + k_row[i] (rows in [B][H][N/block] order).
+ * dims->k is not used (it must still pass validation).  All buffers are device memory
+ * owned by the caller; the call only enqueues work on `stream`.
+ */
+dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const void* k_lr, float tau_log2,
+                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, void* stream);
+
+/*
+ * The selected keys of every query block for per-block k (e.g. from dsv_estimate_mass_k),
+ * in CSR form: row i's k_row[i] keys of largest s (ties to the lower key, ascending) at
+ * cols[rowptr[i] .. rowptr[i + 1]).  k_row[i] must be in [1, N]; cols has rowptr[last]
+ * entries (int32, device, caller-owned).  The same selection rule and exactness as
+ * dsv_estimate_topk.
+ */
+dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const void* k_lr, const int32_t* k_row,
+                                 const int64_t* rowptr, int32_t* cols, void* stream);
+
+/*
  * Sparse attention forward over the selected keys (DSV Spanish summary section 3:
  * sparse attention kernels; page 1 section 2A: only the critical KV pairs are used).
  * For query i of block b:  l_ij = scale * Q_i . K_j for j in idx[b];

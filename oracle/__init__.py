@@ -12,13 +12,21 @@ Pins (what ties each function to something other than itself) live in ``tests/``
                      with a -inf mask outside the selected set;
   backward         : torch fp64 autograd of the masked dense form, central finite
                      differences, closed forms (sum dV = sum dO, sum dK = 0,
-                     unselected keys get zero gradient).
+                     unselected keys get zero gradient);
+  mass-based k     : the exp2 recipe against 2^x, the target by its defining inequality,
+                     sufficiency and minimality of every k, closed forms (equal scores,
+                     one dominant key), planted mistakes rejected.
 """
 from .dsv_oracle import (  # noqa: F401
     block_representatives,
     block_scores,
     default_scale,
+    estimate_mass_topk,
     estimate_topk,
+    exp2_recipe,
+    mass_k,
+    mass_target,
+    mass_weights,
     run_heads,
     sparse_attn_bwd,
     sparse_attn_fwd,
