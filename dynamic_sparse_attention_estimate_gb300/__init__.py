@@ -12,8 +12,10 @@ from .binding import (  # noqa: F401
     dsv_estimate_topk_csr,
     dsv_estimate_topk_workspace,
     dsv_sparse_attn_bwd,
+    dsv_sparse_attn_bwd_csr,
     dsv_sparse_attn_bwd_workspace,
     dsv_sparse_attn_fwd,
+    dsv_sparse_attn_fwd_csr,
     library_path,
     load_library,
 )

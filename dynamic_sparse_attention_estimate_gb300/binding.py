@@ -26,7 +26,8 @@ EXPORTED = (
     "dsv_sparse_attn_bwd_workspace", "dsv_sparse_attn_bwd_workspace_min", "dsv_sparse_attn_bwd",
     "dsv_status_string", "dsv_last_error_message", "dsv_last_device_status",
     "dsv_profile_enable", "dsv_profile_read", "dsv_sparse_attn_bwd_noalloc",
-    "dsv_estimate_mass_k", "dsv_estimate_topk_csr",
+    "dsv_estimate_mass_k", "dsv_estimate_topk_csr", "dsv_sparse_attn_fwd_csr",
+    "dsv_sparse_attn_bwd_csr_workspace", "dsv_sparse_attn_bwd_csr",
 )
 
 
@@ -81,6 +82,12 @@ def load_library(path: Optional[str] = None):
     lib.dsv_estimate_mass_k.restype = st
     lib.dsv_estimate_topk_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp]
     lib.dsv_estimate_topk_csr.restype = st
+    lib.dsv_sparse_attn_fwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.dsv_sparse_attn_fwd_csr.restype = st
+    lib.dsv_sparse_attn_bwd_csr_workspace.argtypes = [dp, ctypes.c_int64]
+    lib.dsv_sparse_attn_bwd_csr_workspace.restype = sz
+    lib.dsv_sparse_attn_bwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz, vp]
+    lib.dsv_sparse_attn_bwd_csr.restype = st
     lib.dsv_profile_enable.argtypes = [st]
     lib.dsv_profile_enable.restype = st
     lib.dsv_profile_read.argtypes = [ctypes.c_char_p, sz]
@@ -238,6 +245,57 @@ def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: t
     _check(lib.dsv_sparse_attn_bwd(ctypes.byref(dims), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                    _ptr(idx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
                                    _stream_ptr(q)), "dsv_sparse_attn_bwd")
+    return dq, dk, dv
+
+
+def dsv_sparse_attn_fwd_csr(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rowptr: torch.Tensor, cols: torch.Tensor,
+                            block: int = 64, scale: Optional[float] = None,
+                            out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """(O, LSE) of attention where query block i attends to cols[rowptr[i]:rowptr[i+1]]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(rowptr, "rowptr", torch.int64, 1)
+    _need(cols, "cols", torch.int32, 1)
+    B, H, N, d = q.shape
+    dims = make_dims(B, H, N, d, 0, max(N, 1), block, scale)
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    _check(load_library().dsv_sparse_attn_fwd_csr(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(rowptr),
+                                                  _ptr(cols), _ptr(o), _ptr(lse), _stream_ptr(q)),
+           "dsv_sparse_attn_fwd_csr")
+    return o, lse
+
+
+def dsv_sparse_attn_bwd_csr_workspace(dims: Dims, total_pairs: int) -> int:
+    return int(load_library().dsv_sparse_attn_bwd_csr_workspace(ctypes.byref(dims), int(total_pairs)))
+
+
+def dsv_sparse_attn_bwd_csr(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                            lse: torch.Tensor, rowptr: torch.Tensor, cols: torch.Tensor, block: int = 64,
+                            scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None, out=None):
+    """(dQ, dK, dV) for the CSR attention above (one wave; total pairs = cols.numel())."""
+    for t, n in ((do, "do"), (q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    _need(rowptr, "rowptr", torch.int64, 1)
+    _need(cols, "cols", torch.int32, 1)
+    B, H, N, d = q.shape
+    dims = make_dims(B, H, N, d, 0, max(N, 1), block, scale)
+    pairs = cols.numel()
+    lib = load_library()
+    if workspace is None:
+        nbytes = int(lib.dsv_sparse_attn_bwd_csr_workspace(ctypes.byref(dims), pairs))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    _check(lib.dsv_sparse_attn_bwd_csr(ctypes.byref(dims), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                       _ptr(rowptr), _ptr(cols), pairs, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                       workspace.numel(), _stream_ptr(q)), "dsv_sparse_attn_bwd_csr")
     return dq, dk, dv
 
 

@@ -92,16 +92,18 @@ struct Carve {
   size_t colbits, colpre, count, offsets, lists, partial, acc, total;
 };
 
-Carve carve(const dsv_dims* d, int64_t nh, int64_t nblk, bool sub) {
+// pairs: the (block, key) pairs of the largest wave (-1: nh * nblk * k)
+Carve carve(const dsv_dims* d, int64_t nh, int64_t nblk, bool sub, int64_t pairs = -1) {
   const int64_t W32 = (nblk + 31) / 32;
+  if (pairs < 0) pairs = nh * nblk * d->k;
   Carve c;
   size_t o = 0;
   c.colbits = o; o += up(sizeof(uint32_t) * nh * W32 * d->N);
   c.colpre = o;  o += up(sizeof(uint32_t) * nh * W32 * d->N);
   c.count = o;   o += up(sizeof(uint32_t) * nh * d->N);
   c.offsets = o; o += up(sizeof(int64_t) * nh * d->N);
-  c.lists = o;   o += up(sizeof(int32_t) * nh * nblk * d->k);
-  c.partial = o; o += up(sizeof(uint16_t) * 2 * d->d * nh * nblk * d->k);   // bf16 rows
+  c.lists = o;   o += up(sizeof(int32_t) * pairs);
+  c.partial = o; o += up(sizeof(uint16_t) * 2 * d->d * pairs);   // bf16 rows
   c.acc = o;     o += sub ? up(sizeof(float) * 2 * d->d * d->N) : 0;
   c.total = o;
   return c;
@@ -275,8 +277,8 @@ dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const v
   return ok();
 }
 
-dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
-                               void* o, float* lse, void* stream) {
+dsv_status fwd_impl(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
+                    const int64_t* rowptr, void* o, float* lse, void* stream) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
   DSV_NEED_PTR(q);
@@ -301,9 +303,21 @@ dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* 
   p.d = static_cast<int>(dims->d);
   p.scale = eff_scale(dims);
   p.status = status;
+  p.rowptr = rowptr;
   cudaError_t e = dsv::launch_sparse_fwd_tc(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
+                               void* o, float* lse, void* stream) {
+  return fwd_impl(dims, q, k, v, idx, nullptr, o, lse, stream);
+}
+
+dsv_status dsv_sparse_attn_fwd_csr(const dsv_dims* dims, const void* q, const void* k, const void* v,
+                                   const int64_t* rowptr, const int32_t* cols, void* o, float* lse, void* stream) {
+  if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
+  return fwd_impl(dims, q, k, v, cols, rowptr, o, lse, stream);
 }
 
 size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims) {
@@ -329,9 +343,11 @@ size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims) {
   return plan_bytes(dims, w);
 }
 
-dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
-                               const void* o, const float* lse, const int32_t* idx, void* dq, void* dk, void* dv,
-                               void* ws, size_t ws_bytes, void* stream) {
+// rowptr == nullptr: k keys per block, waves planned from the workspace; otherwise CSR rows
+// with total_pairs keys in all, one wave over every head (the workspace must hold it).
+dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
+                    const void* o, const float* lse, const int32_t* idx, const int64_t* rowptr, int64_t total_pairs,
+                    void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
   DSV_NEED_PTR(d_o);
@@ -347,13 +363,19 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
   if (!ws) return fail(DSV_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   WavePlan plan;
-  if (!plan_for(dims, ws_bytes, &plan))
+  if (rowptr) {
+    plan = WavePlan{dims->B * dims->H, dims->N / 64, false};
+    const size_t need = carve(dims, plan.nh, plan.nblk, false, total_pairs).total;
+    if (ws_bytes < need)
+      return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the %zu the CSR backward needs", ws_bytes, need);
+  } else if (!plan_for(dims, ws_bytes, &plan)) {
     return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the minimum %zu", ws_bytes,
                 dsv_sparse_attn_bwd_workspace_min(dims));
+  }
   unsigned int* status = nullptr;
   if ((s = status_word(&status)) != DSV_OK) return s;
 
-  const Carve c = carve(dims, plan.nh, plan.nblk, plan.sub);
+  const Carve c = rowptr ? carve(dims, plan.nh, plan.nblk, false, total_pairs) : carve(dims, plan.nh, plan.nblk, plan.sub);
   uint8_t* base = static_cast<uint8_t*>(ws);
   dsv::BwdParams p;
   p.d_o = static_cast<const dsv::bf16*>(d_o);
@@ -380,6 +402,7 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
   p.lists = reinterpret_cast<int32_t*>(base + c.lists);
   p.partial = reinterpret_cast<dsv::bf16*>(base + c.partial);
   p.acc = plan.sub ? reinterpret_cast<float*>(base + c.acc) : nullptr;
+  p.rowptr = rowptr;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!plan.sub) {
@@ -399,6 +422,27 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
     }
   }
   return ok();
+}
+
+dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
+                               const void* o, const float* lse, const int32_t* idx, void* dq, void* dk, void* dv,
+                               void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(dims, d_o, q, k, v, o, lse, idx, nullptr, 0, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+size_t dsv_sparse_attn_bwd_csr_workspace(const dsv_dims* dims, int64_t total_pairs) {
+  if (check_dims(dims, true, false) != DSV_OK || total_pairs < 0) return 0;
+  return carve(dims, dims->B * dims->H, dims->N / 64, false, total_pairs).total;
+}
+
+dsv_status dsv_sparse_attn_bwd_csr(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
+                                   const void* o, const float* lse, const int64_t* rowptr, const int32_t* cols,
+                                   int64_t total_pairs, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
+  if (total_pairs < 0) return fail(DSV_ERR_INVALID_ARG, "total_pairs must be >= 0");
+  if (total_pairs > 0x7fffffffLL) return fail(DSV_ERR_UNSUPPORTED, "total_pairs must fit int32 partial-row indices");
+  return bwd_impl(dims, d_o, q, k, v, o, lse, cols, rowptr, total_pairs, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 dsv_status dsv_profile_enable(int on) {

@@ -23,19 +23,25 @@ namespace {
 
 
 // ---------------------------------------------------------------- 1. column bitmaps
-__global__ void set_bits_kernel(const int32_t* __restrict__ idx, uint32_t* __restrict__ colbits, int64_t N,
-                                int64_t NB, int64_t kk, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32,
-                                int64_t total, unsigned int* status) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t slot = i % kk;
-    const int64_t lbh = i / kk;            // (head slot, local block)
-    const int64_t hs = lbh / nblk, lb = lbh % nblk;
-    const int64_t j = __ldg(idx + ((bh0 + hs) * NB + blk0 + lb) * kk + slot);
-    if (j < 0 || j >= N) { flag_status(status, kStatusBadIndex); continue; }
+// One warp per query block of the wave, over that block's keys (k per block, or a CSR row).
+__global__ void set_bits_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr,
+                                uint32_t* __restrict__ colbits, int64_t N, int64_t NB, int64_t kk, int64_t bh0,
+                                int64_t blk0, int64_t nblk, int64_t W32, int64_t rows, unsigned int* status) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows;
+       r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+    const int64_t hs = r / nblk, lb = r % nblk;
+    const int64_t grow = (bh0 + hs) * NB + blk0 + lb;
+    const int64_t first = rowptr ? rowptr[grow] : grow * kk;
+    const int64_t last = rowptr ? rowptr[grow + 1] : first + kk;
     const uint32_t bit = 1u << (lb & 31);
-    const uint32_t old = atomicOr(colbits + (hs * W32 + (lb >> 5)) * N + j, bit);
-    if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
+    uint32_t* col = colbits + (hs * W32 + (lb >> 5)) * N;
+    for (int64_t i = first + lane; i < last; i += 32) {
+      const int64_t j = __ldg(idx + i);
+      if (j < 0 || j >= N) { flag_status(status, kStatusBadIndex); continue; }
+      const uint32_t old = atomicOr(col + j, bit);
+      if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
+    }
   }
 }
 
@@ -59,7 +65,8 @@ __global__ void colpre_kernel(const uint32_t* __restrict__ colbits, uint32_t* __
 // ---------------------------------------------------------------- 3. exclusive scan per head slot
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads)
-scan_kernel(const uint32_t* __restrict__ count, int64_t* __restrict__ offsets, int64_t N, int64_t pairs_per_head) {
+scan_kernel(const uint32_t* __restrict__ count, int64_t* __restrict__ offsets, int64_t N, int64_t pairs_per_head,
+            const int64_t* __restrict__ rowptr, int64_t NB, int64_t bh0, int64_t blk0) {
   __shared__ int64_t warp_sums[kScanThreads / 32];
   const int64_t hs = blockIdx.x;
   const uint32_t* c = count + hs * N;
@@ -90,7 +97,9 @@ scan_kernel(const uint32_t* __restrict__ count, int64_t* __restrict__ offsets, i
     warp_sums[lane] = wi - ws;
   }
   __syncthreads();
-  int64_t run = hs * pairs_per_head + warp_sums[warp] + incl - s;
+  // first key-major position of this head slot: its blocks' pairs come after the earlier slots'
+  const int64_t base = rowptr ? rowptr[(bh0 + hs) * NB + blk0] - rowptr[bh0 * NB + blk0] : hs * pairs_per_head;
+  int64_t run = base + warp_sums[warp] + incl - s;
   for (int64_t i = lo; i < hi; ++i) {
     off[i] = run;
     run += c[i];
@@ -189,14 +198,15 @@ cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t str
   const int64_t N = p.N;
   cudaError_t e = cudaMemsetAsync(p.colbits, 0, sizeof(uint32_t) * w.nh * W32 * N, stream);
   if (e != cudaSuccess) return e;
-  const int64_t pairs = w.nh * w.nblk * p.topk;
+  const int64_t rows = w.nh * w.nblk;
   { ProfScope prof("bwd_set_bits", stream);
-  set_bits_kernel<<<grid_for(pairs, 256), 256, 0, stream>>>(p.idx, p.colbits, N, p.NB, p.topk, w.bh0, w.blk0, w.nblk,
-                                                             W32, pairs, p.status); }
+  set_bits_kernel<<<grid_for(rows * 32, 256), 256, 0, stream>>>(p.idx, p.rowptr, p.colbits, N, p.NB, p.topk, w.bh0,
+                                                                 w.blk0, w.nblk, W32, rows, p.status); }
   { ProfScope prof("bwd_colpre", stream);
   colpre_kernel<<<grid_for(w.nh * N, 256), 256, 0, stream>>>(p.colbits, p.colpre, p.count, N, W32, w.nh); }
   { ProfScope prof("bwd_scan", stream);
-  scan_kernel<<<static_cast<unsigned>(w.nh), kScanThreads, 0, stream>>>(p.count, p.offsets, N, w.nblk * p.topk); }
+  scan_kernel<<<static_cast<unsigned>(w.nh), kScanThreads, 0, stream>>>(p.count, p.offsets, N, w.nblk * p.topk,
+                                                                          p.rowptr, p.NB, w.bh0, w.blk0); }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if ((e = launch_bwd_main_tc(p, w, W32, stream)) != cudaSuccess) return e;

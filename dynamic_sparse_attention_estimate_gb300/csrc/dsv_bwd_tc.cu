@@ -129,12 +129,21 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   __shared__ int fail_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t N = p.N, NB = p.NB, kk = p.topk;
+  const int64_t N = p.N, NB = p.NB;
   const int64_t hs = blockIdx.x / nblk, lb = blockIdx.x % nblk;
   const int64_t bh = bh0 + hs, blk = blk0 + lb;
   const int64_t row0 = bh * N + blk * 64;
-  const int32_t* ib = p.idx + (bh * NB + blk) * kk;
+  // this block's keys: k of them (or its CSR row), and its first partial row in the wave
+  const int64_t grow = bh * NB + blk;
+  const int64_t kk = p.rowptr ? p.rowptr[grow + 1] - p.rowptr[grow] : p.topk;
+  const int32_t* ib = p.idx + (p.rowptr ? p.rowptr[grow] : grow * p.topk);
+  const int64_t prow0 = p.rowptr ? p.rowptr[grow] - p.rowptr[bh0 * NB + blk0] : static_cast<int64_t>(blockIdx.x) * kk;
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
+  if (nchunks == 0) {  // a block with no keys: dQ = 0 (uniform for the CTA, before any barrier)
+    for (int i = tid; i < 64 * D / 8; i += kThreads)
+      reinterpret_cast<uint4*>(p.dq + row0 * D)[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sDO = sbase + S::OFF_DO, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V;
   const uint32_t sPDS = sbase + S::OFF_P;  // tile pair b: P at sPDS + b * 2 * S::P, dS after it
@@ -391,7 +400,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         const int b = c & 1;
         ok_run = tc::mbar_wait(bar(bars.st_full[b]), (c >> 1) & 1, kWaitLimit);
         if (!ok_run) break;
-        const int64_t row0_c = static_cast<int64_t>(blockIdx.x) * kk + static_cast<int64_t>(c) * kChunk;
+        const int64_t row0_c = prow0 + static_cast<int64_t>(c) * kChunk;
         const int64_t nrows = kk - static_cast<int64_t>(c) * kChunk < kChunk ? kk - static_cast<int64_t>(c) * kChunk : kChunk;
         bulk_store(p.partial + row0_c * (2 * D), sbase + S::OFF_ST + b * (kChunk * S::ROWB),
                    static_cast<uint32_t>(nrows * S::ROWB));
@@ -459,7 +468,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tmem_wait_ld_into(r[0]);
       // this pair's partial row, for the reduction of key j: the list of key j's rows is in
       // ascending block order at key-major position pos
-      const int64_t prow_index = static_cast<int64_t>(blockIdx.x) * kk + static_cast<int64_t>(c) * kChunk + te;
+      const int64_t prow_index = prow0 + static_cast<int64_t>(c) * kChunk + te;
       if (pos >= 0) p.lists[pos] = static_cast<int32_t>(prow_index);
       // 16-byte chunk q of the row is staged at q ^ swz: distinct for 8 consecutive keys (no
       // bank conflicts); d = 64 keys it on the partial row index, which the reduction undoes
@@ -497,7 +506,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
                          : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
                          : "r"(swarp + row * S::ROWB + ((chunk ^ (row & 7)) << 4)));
             if (slot < kk)
-              *reinterpret_cast<uint4*>(p.partial + (static_cast<int64_t>(blockIdx.x) * kk + slot) * (2 * D) +
+              *reinterpret_cast<uint4*>(p.partial + (prow0 + slot) * (2 * D) +
                                         half_off + chunk * 8) = val;
           }
           __syncwarp();

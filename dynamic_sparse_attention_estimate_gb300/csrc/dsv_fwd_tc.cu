@@ -138,8 +138,9 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
 template <int D, int NST, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
 sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
-                     const int32_t* __restrict__ idx, bf16* __restrict__ o, float* __restrict__ lse, int64_t N,
-                     int64_t NB, int64_t kk, float scale_log2, unsigned int* status) {
+                     const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr, bf16* __restrict__ o,
+                     float* __restrict__ lse, int64_t N, int64_t NB, int64_t k_uniform, float scale_log2,
+                     unsigned int* status) {
   using S = Smem<D, NST>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) Bars<NST> bars;
@@ -150,10 +151,19 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t bh = blockIdx.y, blk = blockIdx.x;
+  // this block's keys: k of them, or its CSR row
+  const int64_t grow = bh * NB + blk;
+  const int64_t kk = rowptr ? rowptr[grow + 1] - rowptr[grow] : k_uniform;
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
+  if (nchunks == 0) {  // a block with no keys: O = 0, LSE = -inf (uniform for the CTA, before any barrier)
+    for (int i = tid; i < 64 * D / 8; i += kThreads)
+      reinterpret_cast<uint4*>(o + (bh * N + blk * 64) * D)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < 64) lse[bh * N + blk * 64 + tid] = -CUDART_INF_F;
+    return;
+  }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V, sP = sbase + S::OFF_P;
-  const int32_t* ib = idx + (bh * NB + blk) * kk;
+  const int32_t* ib = idx + (rowptr ? rowptr[grow] : grow * k_uniform);
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
   // the 128-byte swizzle of TMA and of the MMA descriptors both follow address bits, so the
@@ -507,8 +517,8 @@ cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
   ProfScope prof("sparse_fwd", stream);
-  kern<<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.o, p.lse, p.N, p.NB, p.topk, p.scale * kLog2e,
-                                         p.status);
+  kern<<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.rowptr, p.o, p.lse, p.N, p.NB, p.topk,
+                                         p.scale * kLog2e, p.status);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,7 @@ struct FwdParams {
   int d;
   float scale;
   unsigned int* status;
+  const int64_t* rowptr = nullptr;  // CSR row offsets into idx (per-block k), or null: row * topk
 };
 cudaError_t launch_sparse_fwd_tc(const FwdParams& p, cudaStream_t stream);
 
@@ -78,6 +79,7 @@ struct BwdParams {
   int d;
   float scale;
   unsigned int* status;
+  const int64_t* rowptr = nullptr;  // CSR row offsets into idx (per-block k), or null: row * topk
   // workspace carve-out for one wave (sized for the largest wave)
   uint32_t* colbits;   // [nh][W32][N]   bit lb of word (lb / 32): block lb selected key j
   uint32_t* colpre;    // [nh][W32][N]   popcount of the words before

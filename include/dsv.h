@@ -171,6 +171,27 @@ dsv_status dsv_sparse_attn_bwd_noalloc(const dsv_dims* dims, const void* d_o, co
                                        const void* v, const void* o, const float* lse, const int32_t* idx,
                                        void* dq, void* dk, void* dv, void* stream);
 
+/*
+ * Sparse attention over per-block key lists in CSR form (e.g. from dsv_estimate_mass_k and
+ * dsv_estimate_topk_csr): query block i (rows in [B][H][N/block] order) attends to the keys
+ * cols[rowptr[i] .. rowptr[i + 1]) (distinct, within [0, N); ascending order is not needed).
+ * The same computation, layouts and outputs as dsv_sparse_attn_fwd / dsv_sparse_attn_bwd;
+ * dims->k is not used (it must still pass validation).  A block with no keys gets O = 0,
+ * LSE = -inf, dQ = 0.  rowptr: int64 [B*H*N/block + 1], cols: int32 [total_pairs], both
+ * device memory owned by the caller.
+ * The backward runs as one wave over every head: its workspace must hold
+ * dsv_sparse_attn_bwd_csr_workspace(dims, total_pairs) bytes (256-byte aligned), where
+ * total_pairs = rowptr[B*H*N/block] (the caller knows it: it sized cols); otherwise
+ * DSV_ERR_WORKSPACE.  total_pairs must fit int32.
+ */
+dsv_status dsv_sparse_attn_fwd_csr(const dsv_dims* dims, const void* q, const void* k, const void* v,
+                                   const int64_t* rowptr, const int32_t* cols, void* o, float* lse, void* stream);
+size_t dsv_sparse_attn_bwd_csr_workspace(const dsv_dims* dims, int64_t total_pairs);
+dsv_status dsv_sparse_attn_bwd_csr(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
+                                   const void* o, const float* lse, const int64_t* rowptr, const int32_t* cols,
+                                   int64_t total_pairs, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                   void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* dsv_status_string(dsv_status status);
 

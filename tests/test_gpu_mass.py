@@ -68,3 +68,91 @@ def test_mass_selection_short_clip_two_heads():
     k_row, rowptr, cols = _select(g, 1 / 64, 0.9)
     for h in range(wl.H):
         _check_head(x, 0, h, k_row, rowptr, cols, 1 / 64, 0.9)
+
+
+def _abs_contributions(c, lists, blocks):
+    """Per key, the sum over blocks of |that block's contribution| to dK and dV: each block's
+    contribution is one bf16 partial row, rounded once, so the rounding scales with these."""
+    ak = np.zeros(tuple(c["k"].shape))
+    av = np.zeros_like(ak)
+    for b in blocks:
+        _, dk_b, dv_b = oracle.sparse_attn_bwd(c["do"], c["q"], c["k"], c["v"], lists, 64, blocks=[b])
+        ak += np.abs(dk_b)
+        av += np.abs(dv_b)
+    return ak, av
+
+
+def _assert_grad(name, got, ref, magnitude):
+    from gpu_helpers import EDGE_REL_ELEM, MAX_ABS, REL_L2
+    g = np64(got)
+    err = np.abs(g - ref)
+    rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30))
+    excess = float((err - (MAX_ABS + EDGE_REL_ELEM * magnitude)).max())
+    assert excess <= 0 and rel <= REL_L2, f"{name}: max-abs {err.max():.3e}, excess {excess:.3e}, rel-L2 {rel:.3e}"
+
+
+def _csr_lists(rowptr, cols, b, h, H, NB):
+    return [cols[rowptr[(b * H + h) * NB + i]:rowptr[(b * H + h) * NB + i + 1]] for i in range(NB)]
+
+
+def test_csr_attention_tiny_and_ragged():
+    from dynamic_sparse_attention_estimate_gb300 import dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr
+    from gpu_helpers import EDGE_REL_ELEM, LSE_MAX_ABS, assert_close
+    need_gpu()
+    # adaptive k gives some blocks very few keys, so gradients reach magnitudes where one bf16
+    # spacing exceeds the absolute bound: the edge cases' magnitude-aware element bound, taken
+    # on the sum of the blocks' |contributions| (each is one bf16 partial row)
+    for wl, tau, mass in ((WORKLOADS["tiny"], 0.05, 0.9),
+                          (Workload("ragged_mass", 1, 2, (5, 16, 16), 128, 32, 100, None), 0.02, 0.8)):
+        x = make_inputs(wl)
+        g = {k: v.cuda() for k, v in x.items()}
+        k_row, rowptr, cols = _select(g, tau, mass)
+        rp, cl = torch.from_numpy(rowptr).cuda(), torch.from_numpy(cols).cuda()
+        o, lse = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rp, cl)
+        dq, dk, dv = dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rp, cl)
+        torch.cuda.synchronize()
+        assert dsv_last_device_status() == 0
+        for h in range(wl.H):
+            lists = _csr_lists(rowptr, cols, 0, h, wl.H, wl.NB)
+            c = {key: val[0, h] for key, val in x.items()}
+            ro, rl = oracle.sparse_attn_fwd(c["q"], c["k"], c["v"], lists, 64)
+            assert_close(f"{wl.name} O[h{h}]", o[0, h], ro)
+            assert_close(f"{wl.name} LSE[h{h}]", lse[0, h], rl, max_abs=LSE_MAX_ABS)
+            rdq, rdk, rdv = oracle.sparse_attn_bwd(c["do"], c["q"], c["k"], c["v"], lists, 64)
+            ak, av = _abs_contributions(c, lists, range(wl.NB))
+            _assert_grad(f"{wl.name} dQ[h{h}]", dq[0, h], rdq, np.abs(rdq))
+            _assert_grad(f"{wl.name} dK[h{h}]", dk[0, h], rdk, ak)
+            _assert_grad(f"{wl.name} dV[h{h}]", dv[0, h], rdv, av)
+
+
+def test_csr_attention_short_clip_two_heads():
+    from dynamic_sparse_attention_estimate_gb300 import dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr
+    from dynamic_sparse_attention_estimate_gb300.inputs import sample_blocks
+    from gpu_helpers import EDGE_REL_ELEM, LSE_MAX_ABS, assert_close
+    need_gpu()
+    wl = WORKLOADS["short"].with_heads(2)
+    x = make_inputs(wl)
+    g = {k: v.cuda() for k, v in x.items()}
+    k_row, rowptr, cols = _select(g, 1 / 64, 0.9)
+    rp, cl = torch.from_numpy(rowptr).cuda(), torch.from_numpy(cols).cuda()
+    o, lse = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rp, cl)
+    blocks = sample_blocks(wl.NB, 8)
+    mask = torch.zeros(wl.N, dtype=torch.bool)
+    for b in blocks:
+        mask[b * 64:(b + 1) * 64] = True
+    do_m = g["do"] * mask.cuda()[None, None, :, None]
+    dq, dk, dv = dsv_sparse_attn_bwd_csr(do_m, g["q"], g["k"], g["v"], o, lse, rp, cl)
+    torch.cuda.synchronize()
+    assert dsv_last_device_status() == 0
+    rows = mask.numpy()
+    for h in range(wl.H):
+        lists = _csr_lists(rowptr, cols, 0, h, wl.H, wl.NB)
+        c = {key: val[0, h] for key, val in x.items()}
+        ro, rl = oracle.sparse_attn_fwd(c["q"], c["k"], c["v"], lists, 64, blocks=blocks)
+        assert_close(f"O[h{h}] sampled", np64(o[0, h])[rows], ro[rows])
+        assert_close(f"LSE[h{h}] sampled", np64(lse[0, h])[rows], rl[rows], max_abs=LSE_MAX_ABS)
+        rdq, rdk, rdv = oracle.sparse_attn_bwd(c["do"], c["q"], c["k"], c["v"], lists, 64, blocks=blocks)
+        ak, av = _abs_contributions(c, lists, blocks)
+        _assert_grad(f"dQ[h{h}] sampled", dq[0, h][torch.from_numpy(rows)], rdq[rows], np.abs(rdq[rows]))
+        _assert_grad(f"dK[h{h}] sampled", dk[0, h], rdk, ak)
+        _assert_grad(f"dV[h{h}] sampled", dv[0, h], rdv, av)
