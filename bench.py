@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-adaptive", action="store_true", help="skip the mass-based selection measurement")
     ap.add_argument("--heads", type=int, default=None,
                     help="run the workload with this many heads (small cases for profiler captures)")
     return ap.parse_args()
@@ -103,6 +104,11 @@ def oracle_sample(wl, budget_s, cache={}):
         nblocks += 1
     dt = time.perf_counter() - t0
     return 14.0 * 64 * nblocks * wl.k * wl.d, dt, nblocks
+
+
+def dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs):
+    from dynamic_sparse_attention_estimate_gb300.binding import dsv_sparse_attn_bwd_csr_workspace, make_dims
+    return dsv_sparse_attn_bwd_csr_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, wl.k), pairs)
 
 
 def max_over_ranks(ms, dev, world):
@@ -439,6 +445,33 @@ def dsv_arm(args):
         except Exception as exc:  # a comparator only
             own_dense = {"error": str(exc)[:200]}
 
+    # ---- the adaptive selection (per block the keys carrying 90 % of the estimated mass,
+    # tau = 1/64) on the same inputs: selection, then forward + backward over the CSR lists
+    adaptive = None
+    if not args.no_adaptive:
+        try:
+            from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_mass_k, dsv_estimate_topk_csr,
+                                                                  dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr)
+            k_row, rowptr = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9)
+            cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr)
+            pairs = cols.numel()
+            ws_a = torch.empty(dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs), dtype=torch.uint8, device=dev)
+            t_sel = timed(lambda: (dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9, out=(k_row, rowptr)),
+                                   dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr, cols=cols)), 5)
+            t_af = timed(lambda: dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rowptr, cols, out=(o, lse)), 5)
+            t_ab = timed(lambda: dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rowptr, cols,
+                                                         workspace=ws_a, out=(dq, dk, dv)), 5)
+            fl_a = 14.0 * 64 * pairs * wl.d
+            kr = k_row.float()
+            adaptive = {"tau": 1.0 / 64, "mass": 0.9, "mean_k": float(kr.mean()), "min_k": int(k_row.min()),
+                        "max_k": int(k_row.max()), "density": pairs / (BH * wl.NB * wl.N),
+                        "selection_ms": t_sel, "fwd_ms": t_af, "bwd_ms": t_ab,
+                        "attn_tflops": fl_a / ((t_af + t_ab) / 1e3) / 1e12,
+                        "step_tflops": fl_a / ((t_sel + t_af + t_ab) / 1e3) / 1e12}
+            del ws_a
+        except Exception as exc:  # a side measurement only
+            adaptive = {"error": str(exc)[:200]}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -467,7 +500,7 @@ def dsv_arm(args):
         "estimate": {"ms": t_est, "score_elements_per_s": BH * wl.NB * wl.N / (t_est / 1e3),
                      "mma_tflops": 2.0 * wl.r * BH * wl.NB * wl.N / (t_est / 1e3) / 1e12},
         "roofline": rl, "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "dense_comparator": dense,
-        "own_dense_path": own_dense,
+        "own_dense_path": own_dense, "adaptive_selection": adaptive,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
