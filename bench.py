@@ -452,15 +452,16 @@ def dsv_arm(args):
         try:
             from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_mass_k, dsv_estimate_topk_csr,
                                                                   dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr)
-            k_row, rowptr = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9)
+            k_row, rowptr, order = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9)
             cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr)
             pairs = cols.numel()
             ws_a = torch.empty(dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs), dtype=torch.uint8, device=dev)
-            t_sel = timed(lambda: (dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9, out=(k_row, rowptr)),
+            t_sel = timed(lambda: (dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9, out=(k_row, rowptr, order)),
                                    dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr, cols=cols)), 5)
-            t_af = timed(lambda: dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rowptr, cols, out=(o, lse)), 5)
+            t_af = timed(lambda: dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rowptr, cols, out=(o, lse),
+                                                         order=order), 5)
             t_ab = timed(lambda: dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rowptr, cols,
-                                                         workspace=ws_a, out=(dq, dk, dv)), 5)
+                                                         workspace=ws_a, out=(dq, dk, dv), order=order), 5)
             fl_a = 14.0 * 64 * pairs * wl.d
             kr = k_row.float()
             adaptive = {"tau": 1.0 / 64, "mass": 0.9, "mean_k": float(kr.mean()), "min_k": int(k_row.min()),

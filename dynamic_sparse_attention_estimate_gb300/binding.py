@@ -78,15 +78,16 @@ def load_library(path: Optional[str] = None):
     lib.dsv_last_device_status.restype = st
     lib.dsv_sparse_attn_bwd_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.dsv_sparse_attn_bwd_noalloc.restype = st
-    lib.dsv_estimate_mass_k.argtypes = [dp, vp, vp, ctypes.c_float, ctypes.c_uint32, vp, vp, vp]
+    lib.dsv_estimate_mass_k.argtypes = [dp, vp, vp, ctypes.c_float, ctypes.c_uint32, vp, vp, vp, vp]
     lib.dsv_estimate_mass_k.restype = st
     lib.dsv_estimate_topk_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp]
     lib.dsv_estimate_topk_csr.restype = st
-    lib.dsv_sparse_attn_fwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.dsv_sparse_attn_fwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.dsv_sparse_attn_fwd_csr.restype = st
     lib.dsv_sparse_attn_bwd_csr_workspace.argtypes = [dp, ctypes.c_int64]
     lib.dsv_sparse_attn_bwd_csr_workspace.restype = sz
-    lib.dsv_sparse_attn_bwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz, vp]
+    lib.dsv_sparse_attn_bwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz,
+                                            vp]
     lib.dsv_sparse_attn_bwd_csr.restype = st
     lib.dsv_profile_enable.argtypes = [st]
     lib.dsv_profile_enable.restype = st
@@ -160,10 +161,11 @@ def mass_parameters(tau: float, mass: float) -> Tuple[float, int]:
 
 
 def dsv_estimate_mass_k(q_lr: torch.Tensor, k_lr: torch.Tensor, tau: float = 1.0 / 64, mass: float = 0.9,
-                        block: int = 64, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
-    """(k_row int32 [B, H, N/block], rowptr int64 [B*H*N/block + 1]): per query block the
-    smallest number of top keys that carry the fraction `mass` of the estimated attention
-    mass softmax_j(tau s[b, j]) (see include/dsv.h)."""
+                        block: int = 64, out: Optional[Tuple] = None, with_order: bool = True):
+    """(k_row int32 [B, H, N/block], rowptr int64 [B*H*N/block + 1], order int32 [B*H*N/block] or
+    None): per query block the smallest number of top keys that carry the fraction `mass` of
+    the estimated attention mass softmax_j(tau s[b, j]), the CSR offsets, and a launch order
+    (longest rows first) for the CSR attention calls (see include/dsv.h)."""
     _need(q_lr, "q_lr", torch.bfloat16, 4)
     _need(k_lr, "k_lr", torch.bfloat16, 4)
     B, H, N, r = q_lr.shape
@@ -174,12 +176,14 @@ def dsv_estimate_mass_k(q_lr: torch.Tensor, k_lr: torch.Tensor, tau: float = 1.0
     if out is None:
         k_row = torch.empty((B, H, NB), dtype=torch.int32, device=q_lr.device)
         rowptr = torch.empty((B * H * NB + 1,), dtype=torch.int64, device=q_lr.device)
+        order = torch.empty((B * H * NB,), dtype=torch.int32, device=q_lr.device) if with_order else None
     else:
-        k_row, rowptr = out
+        k_row, rowptr, order = out
     tau_log2, mass_num = mass_parameters(tau, mass)
     _check(load_library().dsv_estimate_mass_k(ctypes.byref(dims), _ptr(q_lr), _ptr(k_lr), tau_log2, mass_num,
-                                              _ptr(k_row), _ptr(rowptr), _stream_ptr(q_lr)), "dsv_estimate_mass_k")
-    return k_row, rowptr
+                                              _ptr(k_row), _ptr(rowptr), _ptr(order), _stream_ptr(q_lr)),
+           "dsv_estimate_mass_k")
+    return k_row, rowptr, order
 
 
 def dsv_estimate_topk_csr(q_lr: torch.Tensor, k_lr: torch.Tensor, k_row: torch.Tensor, rowptr: torch.Tensor,
@@ -250,7 +254,7 @@ def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: t
 
 def dsv_sparse_attn_fwd_csr(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rowptr: torch.Tensor, cols: torch.Tensor,
                             block: int = 64, scale: Optional[float] = None,
-                            out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+                            out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None, order: Optional[torch.Tensor] = None):
     """(O, LSE) of attention where query block i attends to cols[rowptr[i]:rowptr[i+1]]."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
@@ -264,7 +268,7 @@ def dsv_sparse_attn_fwd_csr(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, r
     else:
         o, lse = out
     _check(load_library().dsv_sparse_attn_fwd_csr(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(rowptr),
-                                                  _ptr(cols), _ptr(o), _ptr(lse), _stream_ptr(q)),
+                                                  _ptr(cols), _ptr(order), _ptr(o), _ptr(lse), _stream_ptr(q)),
            "dsv_sparse_attn_fwd_csr")
     return o, lse
 
@@ -275,7 +279,8 @@ def dsv_sparse_attn_bwd_csr_workspace(dims: Dims, total_pairs: int) -> int:
 
 def dsv_sparse_attn_bwd_csr(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                             lse: torch.Tensor, rowptr: torch.Tensor, cols: torch.Tensor, block: int = 64,
-                            scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None, out=None):
+                            scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None, out=None,
+                            order: Optional[torch.Tensor] = None):
     """(dQ, dK, dV) for the CSR attention above (one wave; total pairs = cols.numel())."""
     for t, n in ((do, "do"), (q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _need(t, n, torch.bfloat16, 4)
@@ -294,7 +299,8 @@ def dsv_sparse_attn_bwd_csr(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, 
     else:
         dq, dk, dv = out
     _check(lib.dsv_sparse_attn_bwd_csr(ctypes.byref(dims), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                       _ptr(rowptr), _ptr(cols), pairs, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                       _ptr(rowptr), _ptr(cols), _ptr(order), pairs, _ptr(dq), _ptr(dk), _ptr(dv),
+                                       _ptr(workspace),
                                        workspace.numel(), _stream_ptr(q)), "dsv_sparse_attn_bwd_csr")
     return dq, dk, dv
 

@@ -216,7 +216,7 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
 }
 
 dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const void* k_lr, float tau_log2,
-                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, void* stream) {
+                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, int32_t* order, void* stream) {
   dsv_status s = check_dims(dims, false, true);
   if (s != DSV_OK) return s;
   DSV_NEED_PTR(q_lr);
@@ -227,6 +227,8 @@ dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const voi
   if (mass_num < 1 || mass_num > 65536) return fail(DSV_ERR_INVALID_ARG, "mass_num must be in [1, 65536] (got %u)", mass_num);
   if (dims->N > (1LL << 20))
     return fail(DSV_ERR_UNSUPPORTED, "mass selection supports N <= 2^20 (the weight sums are 64-bit)");
+  if (order && (dims->N + 127) / 128 + 1 > 4096)
+    return fail(DSV_ERR_UNSUPPORTED, "a launch order needs N <= 523904");
   unsigned int* status = nullptr;
   if ((s = status_word(&status)) != DSV_OK) return s;
   dsv::MassParams p;
@@ -245,6 +247,7 @@ dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const voi
   }
   p.krow = k_row;
   p.rowptr = rowptr;
+  p.order = order;
   p.status = status;
   cudaError_t e = dsv::launch_estimate_mass_k(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "mass selection launch: %s", cudaGetErrorString(e));
@@ -278,7 +281,7 @@ dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const v
 }
 
 dsv_status fwd_impl(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
-                    const int64_t* rowptr, void* o, float* lse, void* stream) {
+                    const int64_t* rowptr, const int32_t* order, void* o, float* lse, void* stream) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
   DSV_NEED_PTR(q);
@@ -304,6 +307,7 @@ dsv_status fwd_impl(const dsv_dims* dims, const void* q, const void* k, const vo
   p.scale = eff_scale(dims);
   p.status = status;
   p.rowptr = rowptr;
+  p.order = order;
   cudaError_t e = dsv::launch_sparse_fwd_tc(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return ok();
@@ -311,13 +315,14 @@ dsv_status fwd_impl(const dsv_dims* dims, const void* q, const void* k, const vo
 
 dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
                                void* o, float* lse, void* stream) {
-  return fwd_impl(dims, q, k, v, idx, nullptr, o, lse, stream);
+  return fwd_impl(dims, q, k, v, idx, nullptr, nullptr, o, lse, stream);
 }
 
 dsv_status dsv_sparse_attn_fwd_csr(const dsv_dims* dims, const void* q, const void* k, const void* v,
-                                   const int64_t* rowptr, const int32_t* cols, void* o, float* lse, void* stream) {
+                                   const int64_t* rowptr, const int32_t* cols, const int32_t* order, void* o,
+                                   float* lse, void* stream) {
   if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
-  return fwd_impl(dims, q, k, v, cols, rowptr, o, lse, stream);
+  return fwd_impl(dims, q, k, v, cols, rowptr, order, o, lse, stream);
 }
 
 size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims) {
@@ -346,8 +351,9 @@ size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims) {
 // rowptr == nullptr: k keys per block, waves planned from the workspace; otherwise CSR rows
 // with total_pairs keys in all, one wave over every head (the workspace must hold it).
 dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
-                    const void* o, const float* lse, const int32_t* idx, const int64_t* rowptr, int64_t total_pairs,
-                    void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+                    const void* o, const float* lse, const int32_t* idx, const int64_t* rowptr,
+                    const int32_t* order, int64_t total_pairs, void* dq, void* dk, void* dv, void* ws,
+                    size_t ws_bytes, void* stream) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
   DSV_NEED_PTR(d_o);
@@ -403,6 +409,7 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
   p.partial = reinterpret_cast<dsv::bf16*>(base + c.partial);
   p.acc = plan.sub ? reinterpret_cast<float*>(base + c.acc) : nullptr;
   p.rowptr = rowptr;
+  p.order = order;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!plan.sub) {
@@ -427,7 +434,7 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
 dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
                                const void* o, const float* lse, const int32_t* idx, void* dq, void* dk, void* dv,
                                void* ws, size_t ws_bytes, void* stream) {
-  return bwd_impl(dims, d_o, q, k, v, o, lse, idx, nullptr, 0, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_impl(dims, d_o, q, k, v, o, lse, idx, nullptr, nullptr, 0, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 size_t dsv_sparse_attn_bwd_csr_workspace(const dsv_dims* dims, int64_t total_pairs) {
@@ -437,12 +444,12 @@ size_t dsv_sparse_attn_bwd_csr_workspace(const dsv_dims* dims, int64_t total_pai
 
 dsv_status dsv_sparse_attn_bwd_csr(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
                                    const void* o, const float* lse, const int64_t* rowptr, const int32_t* cols,
-                                   int64_t total_pairs, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                                   void* stream) {
+                                   const int32_t* order, int64_t total_pairs, void* dq, void* dk, void* dv, void* ws,
+                                   size_t ws_bytes, void* stream) {
   if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
   if (total_pairs < 0) return fail(DSV_ERR_INVALID_ARG, "total_pairs must be >= 0");
   if (total_pairs > 0x7fffffffLL) return fail(DSV_ERR_UNSUPPORTED, "total_pairs must fit int32 partial-row indices");
-  return bwd_impl(dims, d_o, q, k, v, o, lse, cols, rowptr, total_pairs, dq, dk, dv, ws, ws_bytes, stream);
+  return bwd_impl(dims, d_o, q, k, v, o, lse, cols, rowptr, order, total_pairs, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 dsv_status dsv_profile_enable(int on) {

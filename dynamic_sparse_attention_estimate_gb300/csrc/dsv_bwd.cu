@@ -23,8 +23,25 @@ namespace {
 
 
 // ---------------------------------------------------------------- 1. column bitmaps
-// One warp per query block of the wave, over that block's keys (k per block, or a CSR row).
-__global__ void set_bits_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr,
+// k keys per block: one thread per (block, key) pair of the wave.
+__global__ void set_bits_kernel(const int32_t* __restrict__ idx, uint32_t* __restrict__ colbits, int64_t N,
+                                int64_t NB, int64_t kk, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32,
+                                int64_t total, unsigned int* status) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t slot = i % kk;
+    const int64_t lbh = i / kk;            // (head slot, local block)
+    const int64_t hs = lbh / nblk, lb = lbh % nblk;
+    const int64_t j = __ldg(idx + ((bh0 + hs) * NB + blk0 + lb) * kk + slot);
+    if (j < 0 || j >= N) { flag_status(status, kStatusBadIndex); continue; }
+    const uint32_t bit = 1u << (lb & 31);
+    const uint32_t old = atomicOr(colbits + (hs * W32 + (lb >> 5)) * N + j, bit);
+    if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
+  }
+}
+
+// CSR rows: one warp per query block of the wave, over that block's key range.
+__global__ void set_bits_csr_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr,
                                 uint32_t* __restrict__ colbits, int64_t N, int64_t NB, int64_t kk, int64_t bh0,
                                 int64_t blk0, int64_t nblk, int64_t W32, int64_t rows, unsigned int* status) {
   const int lane = threadIdx.x & 31;
@@ -200,8 +217,14 @@ cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t str
   if (e != cudaSuccess) return e;
   const int64_t rows = w.nh * w.nblk;
   { ProfScope prof("bwd_set_bits", stream);
-  set_bits_kernel<<<grid_for(rows * 32, 256), 256, 0, stream>>>(p.idx, p.rowptr, p.colbits, N, p.NB, p.topk, w.bh0,
-                                                                 w.blk0, w.nblk, W32, rows, p.status); }
+  if (p.rowptr) {
+    set_bits_csr_kernel<<<grid_for(rows * 32, 256), 256, 0, stream>>>(p.idx, p.rowptr, p.colbits, N, p.NB, p.topk,
+                                                                       w.bh0, w.blk0, w.nblk, W32, rows, p.status);
+  } else {
+    const int64_t pairs = rows * p.topk;
+    set_bits_kernel<<<grid_for(pairs, 256), 256, 0, stream>>>(p.idx, p.colbits, N, p.NB, p.topk, w.bh0, w.blk0,
+                                                               w.nblk, W32, pairs, p.status);
+  } }
   { ProfScope prof("bwd_colpre", stream);
   colpre_kernel<<<grid_for(w.nh * N, 256), 256, 0, stream>>>(p.colbits, p.colpre, p.count, N, W32, w.nh); }
   { ProfScope prof("bwd_scan", stream);

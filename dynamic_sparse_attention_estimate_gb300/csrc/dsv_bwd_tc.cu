@@ -117,7 +117,9 @@ DSV_DEVICE void copy_rows(uint32_t dst, int tile_rows, int nrows, const bf16* ba
   }
 }
 
-template <int D>
+// CSR: per-block key counts from row offsets (and an optional launch order); otherwise k for
+// every block, compiled without those loads.
+template <int D, bool CSR>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32, float scale_log2) {
   using S = Sm<D>;
@@ -130,16 +132,17 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t N = p.N, NB = p.NB;
-  const int64_t hs = blockIdx.x / nblk, lb = blockIdx.x % nblk;
+  const int64_t cta_row = (CSR && p.order) ? p.order[blockIdx.x] : static_cast<int64_t>(blockIdx.x);  // launch order
+  const int64_t hs = cta_row / nblk, lb = cta_row % nblk;
   const int64_t bh = bh0 + hs, blk = blk0 + lb;
   const int64_t row0 = bh * N + blk * 64;
   // this block's keys: k of them (or its CSR row), and its first partial row in the wave
   const int64_t grow = bh * NB + blk;
-  const int64_t kk = p.rowptr ? p.rowptr[grow + 1] - p.rowptr[grow] : p.topk;
-  const int32_t* ib = p.idx + (p.rowptr ? p.rowptr[grow] : grow * p.topk);
-  const int64_t prow0 = p.rowptr ? p.rowptr[grow] - p.rowptr[bh0 * NB + blk0] : static_cast<int64_t>(blockIdx.x) * kk;
+  const int64_t kk = CSR ? p.rowptr[grow + 1] - p.rowptr[grow] : p.topk;
+  const int32_t* ib = p.idx + (CSR ? p.rowptr[grow] : grow * p.topk);
+  const int64_t prow0 = CSR ? p.rowptr[grow] - p.rowptr[bh0 * NB + blk0] : cta_row * kk;
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
-  if (nchunks == 0) {  // a block with no keys: dQ = 0 (uniform for the CTA, before any barrier)
+  if (CSR && nchunks == 0) {  // a block with no keys: dQ = 0 (uniform for the CTA, before any barrier)
     for (int i = tid; i < 64 * D / 8; i += kThreads)
       reinterpret_cast<uint4*>(p.dq + row0 * D)[i] = make_uint4(0u, 0u, 0u, 0u);
     return;
@@ -555,11 +558,12 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
 template <int D>
 cudaError_t launch_d(const BwdParams& p, const BwdWave& w, int64_t W32, cudaStream_t stream) {
   const int smem = Sm<D>::TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(sparse_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = p.rowptr ? sparse_bwd_tc_kernel<D, true> : sparse_bwd_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope prof("bwd_main", stream);
-  sparse_bwd_tc_kernel<D><<<static_cast<unsigned>(w.nh * w.nblk), kThreads, smem, stream>>>(
-      p, w.bh0, w.blk0, w.nblk, W32, p.scale * kLog2e);
+  kern<<<static_cast<unsigned>(w.nh * w.nblk), kThreads, smem, stream>>>(p, w.bh0, w.blk0, w.nblk, W32,
+                                                                          p.scale * kLog2e);
   return cudaGetLastError();
 }
 

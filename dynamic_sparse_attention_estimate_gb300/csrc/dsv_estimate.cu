@@ -682,6 +682,34 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const int32_t* __restric
   }
 }
 
+// Launch order for the attention over CSR rows: rows by descending chunk count (ceil(k / 128)),
+// so the longest blocks start first and the grid's tail is short (the order inside a class is
+// whatever the shared-memory atomics give; results do not depend on it).  One CTA; the
+// per-class counters live in shared memory (nclass <= 4096).
+__global__ void __launch_bounds__(1024) csr_order_kernel(const int64_t* __restrict__ rowptr, int64_t rows, int nclass,
+                                                         int32_t* __restrict__ order) {
+  __shared__ int start[4096];
+  const int t = threadIdx.x;
+  for (int c = t; c < nclass; c += 1024) start[c] = 0;
+  __syncthreads();
+  auto cls = [&](int64_t i) {
+    const int64_t nch = (rowptr[i + 1] - rowptr[i] + 127) / 128;
+    return static_cast<int>(nch < nclass - 1 ? nch : nclass - 1);
+  };
+  for (int64_t i = t; i < rows; i += 1024) atomicAdd(&start[cls(i)], 1);
+  __syncthreads();
+  if (t == 0) {  // exclusive scan from the heaviest class down
+    int run = 0;
+    for (int c = nclass - 1; c >= 0; --c) {
+      const int n = start[c];
+      start[c] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+  for (int64_t i = t; i < rows; i += 1024) order[atomicAdd(&start[cls(i)], 1)] = static_cast<int32_t>(i);
+}
+
 template <int R>
 cudaError_t launch_mass_r(const MassParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(kMassRows) * kBins * (sizeof(unsigned long long) + sizeof(uint32_t));
@@ -730,8 +758,16 @@ cudaError_t launch_estimate_mass_k(const MassParams& p, cudaStream_t stream) {
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  ProfScope prof("csr_scan", stream);
-  csr_scan_kernel<<<1, 1024, 0, stream>>>(p.krow, p.BH * p.NB, p.rowptr);
+  {
+    ProfScope prof("csr_scan", stream);
+    csr_scan_kernel<<<1, 1024, 0, stream>>>(p.krow, p.BH * p.NB, p.rowptr);
+  }
+  if (p.order) {
+    const int64_t nclass = (p.N + 127) / 128 + 1;
+    if (nclass > 4096) return cudaErrorInvalidValue;
+    ProfScope prof("csr_order", stream);
+    csr_order_kernel<<<1, 1024, 0, stream>>>(p.rowptr, p.BH * p.NB, static_cast<int>(nclass), p.order);
+  }
   return cudaGetLastError();
 }
 

@@ -135,10 +135,13 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
   named_sync_softmax();
 }
 
-template <int D, int NST, int MINB>
+// CSR: per-block key counts from row offsets (and an optional launch order); otherwise k for
+// every block, compiled without those loads.
+template <int D, int NST, int MINB, bool CSR>
 __global__ void __launch_bounds__(kThreads, MINB)
 sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
-                     const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr, bf16* __restrict__ o,
+                     const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr,
+                     const int32_t* __restrict__ order, bf16* __restrict__ o,
                      float* __restrict__ lse, int64_t N, int64_t NB, int64_t k_uniform, float scale_log2,
                      unsigned int* status) {
   using S = Smem<D, NST>;
@@ -150,12 +153,15 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   __shared__ int fail_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t bh = blockIdx.y, blk = blockIdx.x;
-  // this block's keys: k of them, or its CSR row
-  const int64_t grow = bh * NB + blk;
-  const int64_t kk = rowptr ? rowptr[grow + 1] - rowptr[grow] : k_uniform;
+  // this CTA's query block (in launch order when one is given), and its keys: k of them, or
+  // its CSR row
+  const int64_t lin = static_cast<int64_t>(blockIdx.y) * NB + blockIdx.x;
+  const bool ordered = CSR && order != nullptr;
+  const int64_t grow = ordered ? order[lin] : lin;
+  const int64_t bh = ordered ? grow / NB : blockIdx.y, blk = ordered ? grow % NB : blockIdx.x;
+  const int64_t kk = CSR ? rowptr[grow + 1] - rowptr[grow] : k_uniform;
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
-  if (nchunks == 0) {  // a block with no keys: O = 0, LSE = -inf (uniform for the CTA, before any barrier)
+  if (CSR && nchunks == 0) {  // a block with no keys: O = 0, LSE = -inf (uniform for the CTA, before any barrier)
     for (int i = tid; i < 64 * D / 8; i += kThreads)
       reinterpret_cast<uint4*>(o + (bh * N + blk * 64) * D)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < 64) lse[bh * N + blk * 64 + tid] = -CUDART_INF_F;
@@ -163,7 +169,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V, sP = sbase + S::OFF_P;
-  const int32_t* ib = idx + (rowptr ? rowptr[grow] : grow * k_uniform);
+  const int32_t* ib = idx + (CSR ? rowptr[grow] : grow * k_uniform);
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
   // the 128-byte swizzle of TMA and of the MMA descriptors both follow address bits, so the
@@ -512,12 +518,12 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 template <int D, int NST, int MINB>
 cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
   const int smem = Smem<D, NST>::TOTAL;
-  auto kern = sparse_fwd_tc_kernel<D, NST, MINB>;
+  auto kern = p.rowptr ? sparse_fwd_tc_kernel<D, NST, MINB, true> : sparse_fwd_tc_kernel<D, NST, MINB, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
   ProfScope prof("sparse_fwd", stream);
-  kern<<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.rowptr, p.o, p.lse, p.N, p.NB, p.topk,
+  kern<<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.rowptr, p.order, p.o, p.lse, p.N, p.NB, p.topk,
                                          p.scale * kLog2e, p.status);
   return cudaGetLastError();
 }

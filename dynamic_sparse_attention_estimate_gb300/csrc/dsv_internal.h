@@ -46,6 +46,7 @@ struct MassParams {
   float coef[7];
   int32_t* krow;
   int64_t* rowptr;
+  int32_t* order = nullptr;  // optional: rows by descending chunk count (launch order)
   unsigned int* status;
 };
 cudaError_t launch_estimate_mass_k(const MassParams& p, cudaStream_t stream);
@@ -60,6 +61,7 @@ struct FwdParams {
   float scale;
   unsigned int* status;
   const int64_t* rowptr = nullptr;  // CSR row offsets into idx (per-block k), or null: row * topk
+  const int32_t* order = nullptr;   // optional launch order of the rows (CSR only)
 };
 cudaError_t launch_sparse_fwd_tc(const FwdParams& p, cudaStream_t stream);
 
@@ -80,6 +82,7 @@ struct BwdParams {
   float scale;
   unsigned int* status;
   const int64_t* rowptr = nullptr;  // CSR row offsets into idx (per-block k), or null: row * topk
+  const int32_t* order = nullptr;   // optional launch order of the rows (CSR, one wave over all heads)
   // workspace carve-out for one wave (sized for the largest wave)
   uint32_t* colbits;   // [nh][W32][N]   bit lb of word (lb / 32): block lb selected key j
   uint32_t* colpre;    // [nh][W32][N]   popcount of the words before

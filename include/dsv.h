@@ -93,12 +93,15 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
  *   mass_num: the mass fraction times 2^16, 1 .. 65536 (0.9 -> 58982);
  *   k_row:    int32 [B][H][N/block] (output), 1 <= k_row[b] <= N;
  *   rowptr:   int64 [B*H*N/block + 1] (output), the CSR offsets: rowptr[0] = 0,
- *             rowptr[i + 1] = rowptr[i] + k_row[i] (rows in [B][H][N/block] order).
+ *             rowptr[i + 1] = rowptr[i] + k_row[i] (rows in [B][H][N/block] order);
+ *   order:    int32 [B*H*N/block] (output, may be NULL): the rows by descending
+ *             ceil(k_row / 128), a launch order for the CSR attention calls below (the
+ *             longest blocks start first); needs N <= 523,904.
  * dims->k is not used (it must still pass validation).  All buffers are device memory
  * owned by the caller; the call only enqueues work on `stream`.
  */
 dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const void* k_lr, float tau_log2,
-                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, void* stream);
+                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, int32_t* order, void* stream);
 
 /*
  * The selected keys of every query block for per-block k (e.g. from dsv_estimate_mass_k),
@@ -178,19 +181,21 @@ dsv_status dsv_sparse_attn_bwd_noalloc(const dsv_dims* dims, const void* d_o, co
  * The same computation, layouts and outputs as dsv_sparse_attn_fwd / dsv_sparse_attn_bwd;
  * dims->k is not used (it must still pass validation).  A block with no keys gets O = 0,
  * LSE = -inf, dQ = 0.  rowptr: int64 [B*H*N/block + 1], cols: int32 [total_pairs], both
- * device memory owned by the caller.
+ * device memory owned by the caller.  order (may be NULL): a permutation of the rows in which
+ * to launch them (e.g. dsv_estimate_mass_k's, longest first); results do not depend on it.
  * The backward runs as one wave over every head: its workspace must hold
  * dsv_sparse_attn_bwd_csr_workspace(dims, total_pairs) bytes (256-byte aligned), where
  * total_pairs = rowptr[B*H*N/block] (the caller knows it: it sized cols); otherwise
  * DSV_ERR_WORKSPACE.  total_pairs must fit int32.
  */
 dsv_status dsv_sparse_attn_fwd_csr(const dsv_dims* dims, const void* q, const void* k, const void* v,
-                                   const int64_t* rowptr, const int32_t* cols, void* o, float* lse, void* stream);
+                                   const int64_t* rowptr, const int32_t* cols, const int32_t* order, void* o,
+                                   float* lse, void* stream);
 size_t dsv_sparse_attn_bwd_csr_workspace(const dsv_dims* dims, int64_t total_pairs);
 dsv_status dsv_sparse_attn_bwd_csr(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
                                    const void* o, const float* lse, const int64_t* rowptr, const int32_t* cols,
-                                   int64_t total_pairs, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                                   void* stream);
+                                   const int32_t* order, int64_t total_pairs, void* dq, void* dk, void* dv, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* dsv_status_string(dsv_status status);

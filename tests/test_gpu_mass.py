@@ -18,12 +18,18 @@ from gpu_helpers import need_gpu, np64
 pytestmark = pytest.mark.gpu
 
 
-def _select(g, tau, mass):
-    k_row, rowptr = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], tau, mass)
+def _select(g, tau, mass, with_order=False):
+    k_row, rowptr, order = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], tau, mass)
     cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr)
     torch.cuda.synchronize()
     assert dsv_last_device_status() == 0
-    return k_row.cpu().numpy(), rowptr.cpu().numpy(), cols.cpu().numpy()
+    # the launch order: a permutation of the rows, by non-increasing number of 128-key chunks
+    o = order.cpu().numpy()
+    assert np.array_equal(np.sort(o), np.arange(o.size))
+    nch = (k_row.cpu().numpy().reshape(-1)[o] + 127) // 128
+    assert np.all(np.diff(nch) <= 0)
+    out = (k_row.cpu().numpy(), rowptr.cpu().numpy(), cols.cpu().numpy())
+    return out + (order,) if with_order else out
 
 
 def _check_head(x, b, h, k_row, rowptr, cols, tau, mass):
@@ -106,10 +112,15 @@ def test_csr_attention_tiny_and_ragged():
                           (Workload("ragged_mass", 1, 2, (5, 16, 16), 128, 32, 100, None), 0.02, 0.8)):
         x = make_inputs(wl)
         g = {k: v.cuda() for k, v in x.items()}
-        k_row, rowptr, cols = _select(g, tau, mass)
+        k_row, rowptr, cols, order = _select(g, tau, mass, with_order=True)
         rp, cl = torch.from_numpy(rowptr).cuda(), torch.from_numpy(cols).cuda()
         o, lse = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rp, cl)
         dq, dk, dv = dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rp, cl)
+        # launch order changes nothing in the results
+        o2, lse2 = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rp, cl, order=order)
+        dq2, dk2, dv2 = dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o2, lse2, rp, cl, order=order)
+        for a, b2 in ((o, o2), (lse, lse2), (dq, dq2), (dk, dk2), (dv, dv2)):
+            assert torch.equal(a, b2)
         torch.cuda.synchronize()
         assert dsv_last_device_status() == 0
         for h in range(wl.H):
@@ -133,15 +144,15 @@ def test_csr_attention_short_clip_two_heads():
     wl = WORKLOADS["short"].with_heads(2)
     x = make_inputs(wl)
     g = {k: v.cuda() for k, v in x.items()}
-    k_row, rowptr, cols = _select(g, 1 / 64, 0.9)
+    k_row, rowptr, cols, order = _select(g, 1 / 64, 0.9, with_order=True)
     rp, cl = torch.from_numpy(rowptr).cuda(), torch.from_numpy(cols).cuda()
-    o, lse = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rp, cl)
+    o, lse = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rp, cl, order=order)
     blocks = sample_blocks(wl.NB, 8)
     mask = torch.zeros(wl.N, dtype=torch.bool)
     for b in blocks:
         mask[b * 64:(b + 1) * 64] = True
     do_m = g["do"] * mask.cuda()[None, None, :, None]
-    dq, dk, dv = dsv_sparse_attn_bwd_csr(do_m, g["q"], g["k"], g["v"], o, lse, rp, cl)
+    dq, dk, dv = dsv_sparse_attn_bwd_csr(do_m, g["q"], g["k"], g["v"], o, lse, rp, cl, order=order)
     torch.cuda.synchronize()
     assert dsv_last_device_status() == 0
     rows = mask.numpy()
