@@ -78,7 +78,7 @@ def load_library(path: Optional[str] = None):
     lib.dsv_last_device_status.restype = st
     lib.dsv_sparse_attn_bwd_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.dsv_sparse_attn_bwd_noalloc.restype = st
-    lib.dsv_estimate_mass_k.argtypes = [dp, vp, vp, ctypes.c_float, ctypes.c_uint32, vp, vp, vp, vp]
+    lib.dsv_estimate_mass_k.argtypes = [dp, vp, vp, ctypes.c_float, ctypes.c_uint32, ctypes.c_uint32, vp, vp, vp, vp]
     lib.dsv_estimate_mass_k.restype = st
     lib.dsv_estimate_topk_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp]
     lib.dsv_estimate_topk_csr.restype = st
@@ -161,11 +161,13 @@ def mass_parameters(tau: float, mass: float) -> Tuple[float, int]:
 
 
 def dsv_estimate_mass_k(q_lr: torch.Tensor, k_lr: torch.Tensor, tau: float = 1.0 / 64, mass: float = 0.9,
-                        block: int = 64, out: Optional[Tuple] = None, with_order: bool = True):
+                        block: int = 64, out: Optional[Tuple] = None, with_order: bool = True,
+                        dense_above: Optional[float] = None):
     """(k_row int32 [B, H, N/block], rowptr int64 [B*H*N/block + 1], order int32 [B*H*N/block] or
     None): per query block the smallest number of top keys that carry the fraction `mass` of
     the estimated attention mass softmax_j(tau s[b, j]), the CSR offsets, and a launch order
-    (longest rows first) for the CSR attention calls (see include/dsv.h)."""
+    (longest rows first) for the CSR attention calls (see include/dsv.h).  With `dense_above`, a block whose k exceeds
+    that fraction of the keys attends to all of them (the per-block sparse/dense switch)."""
     _need(q_lr, "q_lr", torch.bfloat16, 4)
     _need(k_lr, "k_lr", torch.bfloat16, 4)
     B, H, N, r = q_lr.shape
@@ -180,8 +182,9 @@ def dsv_estimate_mass_k(q_lr: torch.Tensor, k_lr: torch.Tensor, tau: float = 1.0
     else:
         k_row, rowptr, order = out
     tau_log2, mass_num = mass_parameters(tau, mass)
+    dense_num = 0 if dense_above is None else int(min(65536, max(0, round(float(dense_above) * 65536))))
     _check(load_library().dsv_estimate_mass_k(ctypes.byref(dims), _ptr(q_lr), _ptr(k_lr), tau_log2, mass_num,
-                                              _ptr(k_row), _ptr(rowptr), _ptr(order), _stream_ptr(q_lr)),
+                                              dense_num, _ptr(k_row), _ptr(rowptr), _ptr(order), _stream_ptr(q_lr)),
            "dsv_estimate_mass_k")
     return k_row, rowptr, order
 

@@ -216,7 +216,8 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
 }
 
 dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const void* k_lr, float tau_log2,
-                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, int32_t* order, void* stream) {
+                               uint32_t mass_num, uint32_t dense_num, int32_t* k_row, int64_t* rowptr, int32_t* order,
+                               void* stream) {
   dsv_status s = check_dims(dims, false, true);
   if (s != DSV_OK) return s;
   DSV_NEED_PTR(q_lr);
@@ -225,6 +226,7 @@ dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const voi
   if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
   if (!(tau_log2 > 0.f) || !(tau_log2 < 3.0e38f)) return fail(DSV_ERR_INVALID_ARG, "tau_log2 must be finite and > 0");
   if (mass_num < 1 || mass_num > 65536) return fail(DSV_ERR_INVALID_ARG, "mass_num must be in [1, 65536] (got %u)", mass_num);
+  if (dense_num > 65536) return fail(DSV_ERR_INVALID_ARG, "dense_num must be in [0, 65536] (got %u)", dense_num);
   if (dims->N > (1LL << 20))
     return fail(DSV_ERR_UNSUPPORTED, "mass selection supports N <= 2^20 (the weight sums are 64-bit)");
   if (order && (dims->N + 127) / 128 + 1 > 4096)
@@ -240,6 +242,7 @@ dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const voi
   p.r = static_cast<int>(dims->r);
   p.tau_log2 = tau_log2;
   p.mass_num = mass_num;
+  p.dense_num = dense_num;
   double fact = 1.0;
   for (int i = 0; i < 7; ++i) {  // Taylor coefficients of 2^f: (ln 2)^i / i!, rounded to fp32
     if (i > 0) fact *= i;

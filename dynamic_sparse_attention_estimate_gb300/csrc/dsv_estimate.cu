@@ -468,7 +468,7 @@ DSV_DEVICE void warp_find_mass_bin(const unsigned long long* hw, const uint32_t*
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
 mass_k_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_lr, int N, int NB, float tau_log2,
-              uint32_t mass_num, MassCoef coef, int32_t* __restrict__ krow) {
+              uint32_t mass_num, uint32_t dense_num, MassCoef coef, int32_t* __restrict__ krow) {
   extern __shared__ unsigned long long mhw[];                            // [rows][kBins] weights
   uint32_t* mhc = reinterpret_cast<uint32_t*>(mhw + kMassRows * kBins);  // [rows][kBins] counts
   __shared__ float qhat[16][R];
@@ -653,7 +653,11 @@ mass_k_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_lr, int 
     const uint32_t T = st.level == 3 ? (st.prefix << 10) : st.prefix;
     const unsigned long long wt = mass_weight(key_value(T), key_value(st.maxkey), tau_log2, coef);
     const unsigned long long n_tie = wt ? (st.target - st.w_above + wt - 1ull) / wt : 0ull;
-    krow[bh * NB + row0 + warp] = static_cast<int32_t>(st.c_above + n_tie);
+    unsigned long long kb = st.c_above + n_tie;
+    // sparse/dense switch: a block whose k exceeds dense_num / 2^16 of the keys takes them all
+    if (dense_num && kb * 65536ull > static_cast<unsigned long long>(dense_num) * static_cast<unsigned long long>(N))
+      kb = static_cast<unsigned long long>(N);
+    krow[bh * NB + row0 + warp] = static_cast<int32_t>(kb);
   }
 }
 
@@ -720,7 +724,7 @@ cudaError_t launch_mass_r(const MassParams& p, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>((p.NB + kMassRows - 1) / kMassRows), static_cast<unsigned>(p.BH));
   ProfScope prof("estimate_mass_k", stream);
   mass_k_kernel<R><<<grid, kThreads, smem, stream>>>(p.q_lr, p.k_lr, static_cast<int>(p.N), static_cast<int>(p.NB),
-                                                     p.tau_log2, p.mass_num, coef, p.krow);
+                                                     p.tau_log2, p.mass_num, p.dense_num, coef, p.krow);
   return cudaGetLastError();
 }
 

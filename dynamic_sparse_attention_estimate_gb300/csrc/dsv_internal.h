@@ -43,6 +43,7 @@ struct MassParams {
   int r;
   float tau_log2;
   uint32_t mass_num;
+  uint32_t dense_num;  // 0, or: k * 2^16 > dense_num * N makes a block dense (k = N)
   float coef[7];
   int32_t* krow;
   int64_t* rowptr;

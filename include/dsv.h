@@ -91,6 +91,10 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
  *   tau_log2: tau * log2(e) as fp32, > 0 (tau: the estimate's inverse temperature; for a
  *             block-summed logit of 64 queries, 1/64 takes the mean);
  *   mass_num: the mass fraction times 2^16, 1 .. 65536 (0.9 -> 58982);
+ *   dense_num: the per-block sparse/dense switch (the pages decide per block, from its
+ *             sparsity, whether sparse attention is used): 0 = off, else a block whose k
+ *             exceeds the fraction dense_num / 2^16 of the keys (k * 2^16 > dense_num * N)
+ *             attends to all N keys (k_row = N);
  *   k_row:    int32 [B][H][N/block] (output), 1 <= k_row[b] <= N;
  *   rowptr:   int64 [B*H*N/block + 1] (output), the CSR offsets: rowptr[0] = 0,
  *             rowptr[i + 1] = rowptr[i] + k_row[i] (rows in [B][H][N/block] order);
@@ -101,7 +105,8 @@ dsv_status dsv_estimate_topk(const dsv_dims* dims, const void* q_lr, const void*
  * owned by the caller; the call only enqueues work on `stream`.
  */
 dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const void* k_lr, float tau_log2,
-                               uint32_t mass_num, int32_t* k_row, int64_t* rowptr, int32_t* order, void* stream);
+                               uint32_t mass_num, uint32_t dense_num, int32_t* k_row, int64_t* rowptr, int32_t* order,
+                               void* stream);
 
 /*
  * The selected keys of every query block for per-block k (e.g. from dsv_estimate_mass_k),

@@ -136,9 +136,13 @@ def mass_target(total: int, mass_num: int) -> int:
     return (int(total) * int(mass_num) + 65535) >> 16
 
 
-def mass_k(scores, tau_log2: float, mass_num: int) -> np.ndarray:
+def mass_k(scores, tau_log2: float, mass_num: int, dense_num: int = 0) -> np.ndarray:
     """Per block the size of the shortest (score desc, key asc) prefix whose weight reaches
-    ceil(W * mass_num / 2^16) -> int32 [NB]."""
+    ceil(W * mass_num / 2^16) -> int32 [NB].
+
+    Per-block sparse/dense switch (the pages decide per block from its sparsity level whether
+    sparse attention is used): with dense_num > 0, a block whose k exceeds the fraction
+    dense_num / 2^16 of the keys (k * 2^16 > dense_num * N) attends to all N keys."""
     scores = np.asarray(scores, dtype=np.float64)
     out = np.empty(scores.shape[0], dtype=np.int32)
     for b in range(scores.shape[0]):
@@ -147,14 +151,16 @@ def mass_k(scores, tau_log2: float, mass_num: int) -> np.ndarray:
         target = mass_target(int(w.sum()), mass_num)
         cum = np.cumsum(w.astype(object))           # exact integers
         out[b] = int(np.argmax(cum >= target)) + 1
+        if dense_num and out[b] * 65536 > dense_num * scores.shape[1]:
+            out[b] = scores.shape[1]
     return out
 
 
-def estimate_mass_topk(q_lr, k_lr, block: int, tau_log2: float, mass_num: int):
+def estimate_mass_topk(q_lr, k_lr, block: int, tau_log2: float, mass_num: int, dense_num: int = 0):
     """Adaptive selection: per block its mass-based k, then its top-k keys (ascending).
     Returns (k per block int32 [NB], list of per-block index arrays)."""
     s = block_scores(block_representatives(q_lr, block), k_lr)
-    ks = mass_k(s, tau_log2, mass_num)
+    ks = mass_k(s, tau_log2, mass_num, dense_num)
     return ks, [topk_select(s[b:b + 1], int(ks[b]))[0] for b in range(s.shape[0])]
 
 

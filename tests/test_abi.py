@@ -88,11 +88,12 @@ def test_estimate_needs_no_workspace(lib):
 def test_mass_selection_arguments_rejected_before_launch(lib):
     dims = make_dims(1, 2, 1024, 64, 16, 1024)
     p = ctypes.c_void_p(0x1000)
-    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.0, 58982, p, p, None, None) == 1       # tau_log2 <= 0
+    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.0, 58982, 0, p, p, None, None) == 1       # tau_log2 <= 0
     assert b"tau_log2" in lib.dsv_last_error_message()
-    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 0, p, p, None, None) == 1          # mass_num 0
-    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 65537, p, p, None, None) == 1      # above 1
-    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 58982, None, p, None, None) == 1   # no k_row
+    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 0, 0, p, p, None, None) == 1       # mass_num 0
+    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 65537, 0, p, p, None, None) == 1   # above 1
+    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 58982, 65537, p, p, None, None) == 1  # dense_num
+    assert lib.dsv_estimate_mass_k(ctypes.byref(dims), p, p, 0.02, 58982, 0, None, p, None, None) == 1  # no k_row
     assert lib.dsv_estimate_topk_csr(ctypes.byref(dims), p, p, p, None, p, None) == 1           # no rowptr
     bad_r = make_dims(1, 2, 1024, 64, 24, 1024)
-    assert lib.dsv_estimate_mass_k(ctypes.byref(bad_r), p, p, 0.02, 58982, p, p, None, None) == 2
+    assert lib.dsv_estimate_mass_k(ctypes.byref(bad_r), p, p, 0.02, 58982, 0, p, p, None, None) == 2

@@ -18,8 +18,8 @@ from gpu_helpers import need_gpu, np64
 pytestmark = pytest.mark.gpu
 
 
-def _select(g, tau, mass, with_order=False):
-    k_row, rowptr, order = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], tau, mass)
+def _select(g, tau, mass, with_order=False, dense_above=None):
+    k_row, rowptr, order = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], tau, mass, dense_above=dense_above)
     cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr)
     torch.cuda.synchronize()
     assert dsv_last_device_status() == 0
@@ -32,10 +32,10 @@ def _select(g, tau, mass, with_order=False):
     return out + (order,) if with_order else out
 
 
-def _check_head(x, b, h, k_row, rowptr, cols, tau, mass):
+def _check_head(x, b, h, k_row, rowptr, cols, tau, mass, dense_num=0):
     tau_log2, mass_num = mass_parameters(tau, mass)
     s = oracle.block_scores(oracle.block_representatives(np64(x["q_lr"][b, h]), 64), np64(x["k_lr"][b, h]))
-    want_k = oracle.mass_k(s, tau_log2, mass_num)
+    want_k = oracle.mass_k(s, tau_log2, mass_num, dense_num)
     H, NB = k_row.shape[1], k_row.shape[2]
     assert np.array_equal(k_row[b, h], want_k), np.flatnonzero(k_row[b, h] != want_k)[:8]
     for blk in range(NB):
@@ -54,6 +54,19 @@ def test_mass_selection_tiny(tau, mass):
     assert rowptr[0] == 0 and np.array_equal(np.diff(rowptr), k_row.reshape(-1))
     for h in range(wl.H):
         _check_head(x, 0, h, k_row, rowptr, cols, tau, mass)
+
+
+def test_sparse_dense_switch_tiny():
+    # blocks whose adaptive k exceeds 72 % of the keys take all of them (ascending)
+    need_gpu()
+    wl = WORKLOADS["tiny"]
+    x = make_inputs(wl)
+    g = {k: v.cuda() for k, v in x.items()}
+    k_row, rowptr, cols = _select(g, 0.003, 0.9, dense_above=0.72)
+    dense_num = int(round(0.72 * 65536))
+    assert (k_row == wl.N).any() and (k_row < wl.N).any()    # both kinds of block occur
+    for h in range(wl.H):
+        _check_head(x, 0, h, k_row, rowptr, cols, 0.003, 0.9, dense_num)
 
 
 def test_mass_selection_ragged_r32():

@@ -161,3 +161,16 @@ def test_ragged_selection_attention_equals_masked_dense():
     dq, dk, dv = real.sparse_attn_bwd(do, q, k, v, sel, block, scale)
     for got, want in ((dq, tq), (dk, tk), (dv, tv)):
         assert np.allclose(got, want.grad[0, 0].numpy(), atol=1e-9)
+
+
+def test_sparse_dense_switch():
+    # dense_num = 0: off; 65536: never (k <= N); otherwise k * 2^16 > dense_num * N -> N
+    rng = np.random.default_rng(7)
+    s = rng.integers(-20, 20, size=(8, 300)).astype(np.float64)
+    base = real.mass_k(s, 0.05, 58982)
+    assert np.array_equal(real.mass_k(s, 0.05, 58982, 0), base)
+    assert np.array_equal(real.mass_k(s, 0.05, 58982, 65536), base)
+    for num in (1, 9830, 32768):
+        got = real.mass_k(s, 0.05, 58982, num)
+        want = np.where(base.astype(np.int64) * 65536 > num * 300, 300, base)
+        assert np.array_equal(got, want)
