@@ -27,7 +27,7 @@ EXPORTED = (
     "dsv_status_string", "dsv_last_error_message", "dsv_last_device_status",
     "dsv_profile_enable", "dsv_profile_read", "dsv_sparse_attn_bwd_noalloc",
     "dsv_estimate_mass_k", "dsv_estimate_topk_csr", "dsv_sparse_attn_fwd_csr",
-    "dsv_sparse_attn_bwd_csr_workspace", "dsv_sparse_attn_bwd_csr",
+    "dsv_sparse_attn_bwd_csr_workspace", "dsv_sparse_attn_bwd_csr", "dsv_csr_launch_order",
 )
 
 
@@ -82,6 +82,8 @@ def load_library(path: Optional[str] = None):
     lib.dsv_estimate_mass_k.restype = st
     lib.dsv_estimate_topk_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp]
     lib.dsv_estimate_topk_csr.restype = st
+    lib.dsv_csr_launch_order.argtypes = [dp, vp, vp, vp]
+    lib.dsv_csr_launch_order.restype = st
     lib.dsv_sparse_attn_fwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.dsv_sparse_attn_fwd_csr.restype = st
     lib.dsv_sparse_attn_bwd_csr_workspace.argtypes = [dp, ctypes.c_int64]
@@ -253,6 +255,16 @@ def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: t
                                    _ptr(idx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
                                    _stream_ptr(q)), "dsv_sparse_attn_bwd")
     return dq, dk, dv
+
+
+def dsv_csr_launch_order(rowptr: torch.Tensor, B: int, H: int, N: int, block: int = 64) -> torch.Tensor:
+    """int32 [B*H*N/block]: the CSR rows by descending number of 128-key chunks."""
+    _need(rowptr, "rowptr", torch.int64, 1)
+    dims = make_dims(B, H, N, 0, 16, max(N, 1), block)
+    order = torch.empty((B * H * (N // block),), dtype=torch.int32, device=rowptr.device)
+    _check(load_library().dsv_csr_launch_order(ctypes.byref(dims), _ptr(rowptr), _ptr(order), _stream_ptr(rowptr)),
+           "dsv_csr_launch_order")
+    return order
 
 
 def dsv_sparse_attn_fwd_csr(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rowptr: torch.Tensor, cols: torch.Tensor,

@@ -257,6 +257,17 @@ dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const voi
   return ok();
 }
 
+dsv_status dsv_csr_launch_order(const dsv_dims* dims, const int64_t* rowptr, int32_t* order, void* stream) {
+  dsv_status s = check_dims(dims, false, false);
+  if (s != DSV_OK) return s;
+  if (!rowptr || !order) return fail(DSV_ERR_INVALID_ARG, "rowptr and order must be non-NULL");
+  if ((dims->N + 127) / 128 + 1 > 4096) return fail(DSV_ERR_UNSUPPORTED, "a launch order needs N <= 523904");
+  cudaError_t e = dsv::launch_csr_order(rowptr, dims->B * dims->H * (dims->N / dims->block), dims->N, order,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "launch order: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const void* k_lr, const int32_t* k_row,
                                  const int64_t* rowptr, int32_t* cols, void* stream) {
   dsv_status s = check_dims(dims, false, true);

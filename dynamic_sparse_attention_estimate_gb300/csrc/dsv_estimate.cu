@@ -766,12 +766,15 @@ cudaError_t launch_estimate_mass_k(const MassParams& p, cudaStream_t stream) {
     ProfScope prof("csr_scan", stream);
     csr_scan_kernel<<<1, 1024, 0, stream>>>(p.krow, p.BH * p.NB, p.rowptr);
   }
-  if (p.order) {
-    const int64_t nclass = (p.N + 127) / 128 + 1;
-    if (nclass > 4096) return cudaErrorInvalidValue;
-    ProfScope prof("csr_order", stream);
-    csr_order_kernel<<<1, 1024, 0, stream>>>(p.rowptr, p.BH * p.NB, static_cast<int>(nclass), p.order);
-  }
+  if (p.order) return launch_csr_order(p.rowptr, p.BH * p.NB, p.N, p.order, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_csr_order(const int64_t* rowptr, int64_t rows, int64_t N, int32_t* order, cudaStream_t stream) {
+  const int64_t nclass = (N + 127) / 128 + 1;
+  if (nclass > 4096) return cudaErrorInvalidValue;
+  ProfScope prof("csr_order", stream);
+  csr_order_kernel<<<1, 1024, 0, stream>>>(rowptr, rows, static_cast<int>(nclass), order);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,8 @@ struct MassParams {
   unsigned int* status;
 };
 cudaError_t launch_estimate_mass_k(const MassParams& p, cudaStream_t stream);
+// rows (CSR offsets) by descending ceil(k / 128): a longest-first launch order
+cudaError_t launch_csr_order(const int64_t* rowptr, int64_t rows, int64_t N, int32_t* order, cudaStream_t stream);
 
 struct FwdParams {
   const bf16 *q, *k, *v;  // [BH][N][d]

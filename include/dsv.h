@@ -109,6 +109,14 @@ dsv_status dsv_estimate_mass_k(const dsv_dims* dims, const void* q_lr, const voi
                                void* stream);
 
 /*
+ * A longest-first launch order for CSR rows with any per-block k (e.g. a different k per
+ * head, all heads in one launch): order (int32 [B*H*N/block], output) lists the rows by
+ * descending ceil(k / 128), where k = rowptr[i + 1] - rowptr[i].  Pass it to the CSR
+ * attention calls below so the longest blocks start first.  Needs N <= 523,904.
+ */
+dsv_status dsv_csr_launch_order(const dsv_dims* dims, const int64_t* rowptr, int32_t* order, void* stream);
+
+/*
  * The selected keys of every query block for per-block k (e.g. from dsv_estimate_mass_k),
  * in CSR form: row i's k_row[i] keys of largest s (ties to the lower key, ascending) at
  * cols[rowptr[i] .. rowptr[i + 1]).  k_row[i] must be in [1, N]; cols has rowptr[last]

@@ -180,3 +180,40 @@ def test_csr_attention_short_clip_two_heads():
         _assert_grad(f"dQ[h{h}] sampled", dq[0, h][torch.from_numpy(rows)], rdq[rows], np.abs(rdq[rows]))
         _assert_grad(f"dK[h{h}] sampled", dk[0, h], rdk, ak)
         _assert_grad(f"dV[h{h}] sampled", dv[0, h], rdv, av)
+
+
+def test_heterogeneous_per_head_k_in_one_launch():
+    # a different k per head (100 and 700), all heads in one CSR launch, longest rows first
+    from dynamic_sparse_attention_estimate_gb300 import dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr
+    from dynamic_sparse_attention_estimate_gb300.binding import dsv_csr_launch_order
+    from gpu_helpers import LSE_MAX_ABS, assert_close
+    need_gpu()
+    wl = WORKLOADS["tiny"]
+    x = make_inputs(wl)
+    g = {k: v.cuda() for k, v in x.items()}
+    ks = (100, 700)
+    k_row = torch.tensor([ks[h] for h in range(wl.H) for _ in range(wl.NB)], dtype=torch.int32).cuda()
+    rowptr = torch.zeros(wl.H * wl.NB + 1, dtype=torch.int64)
+    rowptr[1:] = torch.cumsum(k_row.cpu().to(torch.int64), 0)
+    rowptr = rowptr.cuda()
+    cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row.view(1, wl.H, wl.NB), rowptr)
+    order = dsv_csr_launch_order(rowptr, 1, wl.H, wl.N)
+    o, lse = dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rowptr, cols, order=order)
+    dq, dk, dv = dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rowptr, cols, order=order)
+    torch.cuda.synchronize()
+    assert dsv_last_device_status() == 0
+    od = order.cpu().numpy()
+    assert np.array_equal(np.sort(od), np.arange(od.size)) and np.all(od[:wl.NB] >= wl.NB)   # head 1 first
+    rp, cl = rowptr.cpu().numpy(), cols.cpu().numpy()
+    for h in range(wl.H):
+        c = {key: val[0, h] for key, val in x.items()}
+        idx_h = oracle.estimate_topk(np64(c["q_lr"]), np64(c["k_lr"]), 64, ks[h])
+        lists = _csr_lists(rp, cl, 0, h, wl.H, wl.NB)
+        assert all(np.array_equal(lists[b], idx_h[b]) for b in range(wl.NB))
+        ro, rl = oracle.sparse_attn_fwd(c["q"], c["k"], c["v"], idx_h, 64)
+        assert_close(f"O[h{h}]", o[0, h], ro)
+        assert_close(f"LSE[h{h}]", lse[0, h], rl, max_abs=LSE_MAX_ABS)
+        rdq, rdk, rdv = oracle.sparse_attn_bwd(c["do"], c["q"], c["k"], c["v"], idx_h, 64)
+        assert_close(f"dQ[h{h}]", dq[0, h], rdq)
+        assert_close(f"dK[h{h}]", dk[0, h], rdk)
+        assert_close(f"dV[h{h}]", dv[0, h], rdv)
