@@ -89,7 +89,7 @@ struct WavePlan {
 };
 
 struct Carve {
-  size_t colbits, colpre, count, offsets, lists, partial, acc, total;
+  size_t colbits, colpre, count, offsets, tsum, lists, partial, acc, total;
 };
 
 // pairs: the (block, key) pairs of the largest wave (-1: nh * nblk * k)
@@ -102,6 +102,7 @@ Carve carve(const dsv_dims* d, int64_t nh, int64_t nblk, bool sub, int64_t pairs
   c.colpre = o;  o += up(sizeof(uint32_t) * nh * W32 * d->N);
   c.count = o;   o += up(sizeof(uint32_t) * nh * d->N);
   c.offsets = o; o += up(sizeof(int64_t) * nh * d->N);
+  c.tsum = o;    o += up(sizeof(int64_t) * nh * ((d->N + 1023) / 1024));
   c.lists = o;   o += up(sizeof(int32_t) * pairs);
   c.partial = o; o += up(sizeof(uint16_t) * 2 * d->d * pairs);   // bf16 rows
   c.acc = o;     o += sub ? up(sizeof(float) * 2 * d->d * d->N) : 0;
@@ -419,6 +420,7 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
   p.colpre = reinterpret_cast<uint32_t*>(base + c.colpre);
   p.count = reinterpret_cast<uint32_t*>(base + c.count);
   p.offsets = reinterpret_cast<int64_t*>(base + c.offsets);
+  p.tsum = reinterpret_cast<int64_t*>(base + c.tsum);
   p.lists = reinterpret_cast<int32_t*>(base + c.lists);
   p.partial = reinterpret_cast<dsv::bf16*>(base + c.partial);
   p.acc = plan.sub ? reinterpret_cast<float*>(base + c.acc) : nullptr;

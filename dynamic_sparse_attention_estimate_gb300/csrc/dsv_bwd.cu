@@ -2,17 +2,19 @@
 //
 // dQ is local to a query block; dK and dV of key j sum over every query block that
 // selected j.  To stay deterministic without float atomics the per-(block, key)
-// contributions are written as partial rows into the workspace, laid out KEY-MAJOR:
-// key j's rows are contiguous and ordered by ascending query block, so the final
-// reduction is a fixed-order segmented sum.  Per wave of query blocks:
-//   1. colbits[w][j] bit b  <- block (32 w + b) selected key j      (integer atomicOr)
+// contributions are written as partial rows into the workspace (block-major: each query
+// block's rows in its own chunk order), and a KEY-MAJOR list gives, for each key j, its
+// rows in ascending query-block order, so the final reduction is a fixed-order segmented
+// sum.  Per wave of query blocks:
+//   1. colbits[w][j] bit b  <- block (32 w + b) selected key j   (shared-memory tiles)
 //   2. colpre[w][j]         <- popcount of words before w; count[j] <- total
 //   3. offsets[j]           <- exclusive scan of count (per head)
 //   4. main kernel (dsv_bwd_tc.cu): per query block, per 128-key chunk, on the tcgen05
 //      tensor cores: recompute P from LSE, dP, dS; dQ accumulated in tensor memory;
-//      dV_part = P^T dO, dK_part = scale dS^T Q written as bf16 to row offsets[j] + colpre
-//      + popc(lower bits) -- the block's rank among the blocks that selected j.
-//   5. reduce: dK_j, dV_j = sum of key j's rows in order (fp32), written as bf16.
+//      dV_part = P^T dO, dK_part = scale dS^T Q written as bf16 partial rows; the list
+//      entry at offsets[j] + colpre + popc(lower bits) -- the block's rank among the
+//      blocks that selected j -- is set to the row's index.
+//   5. reduce: dK_j, dV_j = sum of key j's rows in list order (fp32), written as bf16.
 // A head whose partial rows do not fit in the workspace is split into several waves
 // whose sums are chained through an fp32 accumulator.
 #include "dsv_common.cuh"
@@ -23,88 +25,159 @@ namespace {
 
 
 // ---------------------------------------------------------------- 1. column bitmaps
-// k keys per block: one thread per (block, key) pair of the wave.
-__global__ void set_bits_kernel(const int32_t* __restrict__ idx, uint32_t* __restrict__ colbits, int64_t N,
-                                int64_t NB, int64_t kk, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32,
-                                int64_t total, unsigned int* status) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t slot = i % kk;
-    const int64_t lbh = i / kk;            // (head slot, local block)
-    const int64_t hs = lbh / nblk, lb = lbh % nblk;
-    const int64_t j = __ldg(idx + ((bh0 + hs) * NB + blk0 + lb) * kk + slot);
-    if (j < 0 || j >= N) { flag_status(status, kStatusBadIndex); continue; }
-    const uint32_t bit = 1u << (lb & 31);
-    const uint32_t old = atomicOr(colbits + (hs * W32 + (lb >> 5)) * N + j, bit);
-    if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
+// One CTA per (key tile, half of a 32-block word group, head slot).  The half's 16 blocks are
+// contiguous in idx (fixed k and CSR alike), so the CTA walks that range flat, ORs each key's
+// block bit into a shared-memory tile (16 bits per key, two keys per word) and then writes the
+// tile out as its half-words of colbits.  Every word of the wave is written (zeros included):
+// no clearing pass and no global atomics.  A key outside [0, N) or a key twice in one row sets
+// the bad-index status.
+constexpr int kBitsThreads = 1024;
+constexpr int64_t kBitsTile = 32768;  // keys per tile: 64 KB of shared memory
+
+__device__ __forceinline__ void set_bit(uint32_t* tile, const int64_t* rp, int nrows, int64_t first, int64_t kk,
+                                        bool csr, int64_t i, int32_t j, int64_t j0, int64_t tj, int64_t N,
+                                        bool report_range, unsigned int* status) {
+  if (j < 0 || j >= N) {
+    if (report_range) flag_status(status, kStatusBadIndex);
+    return;
   }
+  const int64_t jj = j - j0;
+  if (jj < 0 || jj >= tj) return;
+  int r;
+  if (csr) {  // largest r with rp[r] <= i
+    int lo = 0, hi = nrows - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (rp[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    r = lo;
+  } else {
+    r = static_cast<int>(static_cast<uint32_t>(i - first) / static_cast<uint32_t>(kk));
+  }
+  const uint32_t bit = 1u << (r + 16 * static_cast<int>(jj & 1));
+  const uint32_t old = atomicOr(tile + (jj >> 1), bit);
+  if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
 }
 
-// CSR rows: one warp per query block of the wave, over that block's key range.
-__global__ void set_bits_csr_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr,
-                                uint32_t* __restrict__ colbits, int64_t N, int64_t NB, int64_t kk, int64_t bh0,
-                                int64_t blk0, int64_t nblk, int64_t W32, int64_t rows, unsigned int* status) {
-  const int lane = threadIdx.x & 31;
-  for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows;
-       r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
-    const int64_t hs = r / nblk, lb = r % nblk;
-    const int64_t grow = (bh0 + hs) * NB + blk0 + lb;
-    const int64_t first = rowptr ? rowptr[grow] : grow * kk;
-    const int64_t last = rowptr ? rowptr[grow + 1] : first + kk;
-    const uint32_t bit = 1u << (lb & 31);
-    uint32_t* col = colbits + (hs * W32 + (lb >> 5)) * N;
-    for (int64_t i = first + lane; i < last; i += 32) {
-      const int64_t j = __ldg(idx + i);
-      if (j < 0 || j >= N) { flag_status(status, kStatusBadIndex); continue; }
-      const uint32_t old = atomicOr(col + j, bit);
-      if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
+__global__ void __launch_bounds__(kBitsThreads)
+set_bits_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr, uint32_t* __restrict__ colbits,
+                int64_t N, int64_t NB, int64_t kk, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32, int64_t hs0,
+                unsigned int* status) {
+  extern __shared__ uint32_t tile[];  // word i: key 2 i in bits 0-15, key 2 i + 1 in bits 16-31
+  __shared__ int64_t rp[17];
+  const int tid = threadIdx.x;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kBitsTile;
+  const int64_t tj = N - j0 < kBitsTile ? N - j0 : kBitsTile;
+  const int half = blockIdx.y & 1;
+  const int64_t wg = blockIdx.y >> 1;
+  const int64_t hs = hs0 + blockIdx.z;
+  const int64_t lb0 = wg * 32 + half * 16;
+  const int nrows = nblk - lb0 <= 0 ? 0 : (nblk - lb0 < 16 ? static_cast<int>(nblk - lb0) : 16);
+  const int64_t g0 = (bh0 + hs) * NB + blk0 + lb0;  // global row of the half's first block
+  for (int64_t i = tid; i < (tj + 1) / 2; i += kBitsThreads) tile[i] = 0;
+  if (nrows > 0 && tid <= nrows) rp[tid] = rowptr ? rowptr[g0 + tid] : (g0 + tid) * kk;
+  __syncthreads();
+  const bool csr = rowptr != nullptr;
+  const bool report = blockIdx.x == 0;  // range errors are reported by the first key tile only
+  if (nrows > 0) {
+    const int64_t first = rp[0], last = rp[nrows];
+    // scalar head and tail, 16-byte loads in between
+    const int64_t a0 = ((first + 3) & ~int64_t(3)) < last ? ((first + 3) & ~int64_t(3)) : last;
+    const int64_t a1 = (last & ~int64_t(3)) > a0 ? (last & ~int64_t(3)) : a0;
+    for (int64_t i = first + tid; i < a0; i += kBitsThreads)
+      set_bit(tile, rp, nrows, first, kk, csr, i, __ldg(idx + i), j0, tj, N, report, status);
+    for (int64_t i = a1 + tid; i < last; i += kBitsThreads)
+      set_bit(tile, rp, nrows, first, kk, csr, i, __ldg(idx + i), j0, tj, N, report, status);
+    const int4* v4 = reinterpret_cast<const int4*>(idx + a0);
+    const int64_t n4 = (a1 - a0) >> 2;
+    for (int64_t q = tid; q < n4; q += 2 * kBitsThreads) {
+      const bool two = q + kBitsThreads < n4;
+      const int4 x = __ldg(v4 + q);
+      const int4 y = two ? __ldg(v4 + q + kBitsThreads) : make_int4(0, 0, 0, 0);
+      const int64_t i = a0 + 4 * q, i2 = i + 4 * kBitsThreads;
+      set_bit(tile, rp, nrows, first, kk, csr, i, x.x, j0, tj, N, report, status);
+      set_bit(tile, rp, nrows, first, kk, csr, i + 1, x.y, j0, tj, N, report, status);
+      set_bit(tile, rp, nrows, first, kk, csr, i + 2, x.z, j0, tj, N, report, status);
+      set_bit(tile, rp, nrows, first, kk, csr, i + 3, x.w, j0, tj, N, report, status);
+      if (two) {
+        set_bit(tile, rp, nrows, first, kk, csr, i2, y.x, j0, tj, N, report, status);
+        set_bit(tile, rp, nrows, first, kk, csr, i2 + 1, y.y, j0, tj, N, report, status);
+        set_bit(tile, rp, nrows, first, kk, csr, i2 + 2, y.z, j0, tj, N, report, status);
+        set_bit(tile, rp, nrows, first, kk, csr, i2 + 3, y.w, j0, tj, N, report, status);
+      }
     }
   }
+  __syncthreads();
+  // bits 16 h .. 16 h + 15 of word j are the half-word at byte 2 h (little-endian)
+  uint16_t* out = reinterpret_cast<uint16_t*>(colbits + (hs * W32 + wg) * N + j0) + half;
+  for (int64_t i = tid; i < tj; i += kBitsThreads)
+    out[2 * i] = static_cast<uint16_t>(tile[i >> 1] >> (16 * static_cast<int>(i & 1)));
 }
 
 // ---------------------------------------------------------------- 2. per-key word prefix
-__global__ void colpre_kernel(const uint32_t* __restrict__ colbits, uint32_t* __restrict__ colpre,
-                              uint32_t* __restrict__ count, int64_t N, int64_t W32, int64_t nh) {
-  const int64_t total = nh * N;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t hs = i / N, j = i % N;
-    uint32_t run = 0;
+// One thread per key, 1024 keys per CTA: colpre[w][j] = popcount of the words before w,
+// count[j] = the total, and the tile's sum of counts for the scan.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
+colpre_kernel(const uint32_t* __restrict__ colbits, uint32_t* __restrict__ colpre, uint32_t* __restrict__ count,
+              int64_t* __restrict__ tsum, int64_t N, int64_t W32, int64_t hs0) {
+  __shared__ uint32_t warp_tot[kScanThreads / 32];
+  const int64_t hs = hs0 + blockIdx.y;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * kScanThreads + threadIdx.x;
+  uint32_t run = 0;
+  if (j < N) {
     for (int64_t w = 0; w < W32; ++w) {
       const int64_t a = (hs * W32 + w) * N + j;
       colpre[a] = run;
       run += __popc(colbits[a]);
     }
-    count[i] = run;
+    count[hs * N + j] = run;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t t = run;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  if (lane == 0) warp_tot[warp] = t;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t u = warp_tot[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+    if (lane == 0) tsum[hs * gridDim.x + blockIdx.x] = u;
   }
 }
 
 // ---------------------------------------------------------------- 3. exclusive scan per head slot
-constexpr int kScanThreads = 1024;
+// One thread per key, 1024 keys per CTA: the tile's exclusive scan plus the sum of the
+// earlier tiles of the same head slot plus the head slot's first key-major position.
 __global__ void __launch_bounds__(kScanThreads)
-scan_kernel(const uint32_t* __restrict__ count, int64_t* __restrict__ offsets, int64_t N, int64_t pairs_per_head,
-            const int64_t* __restrict__ rowptr, int64_t NB, int64_t bh0, int64_t blk0) {
+scan_kernel(const uint32_t* __restrict__ count, const int64_t* __restrict__ tsum, int64_t* __restrict__ offsets,
+            int64_t N, int64_t pairs_per_head, const int64_t* __restrict__ rowptr, int64_t NB, int64_t bh0,
+            int64_t blk0, int64_t hs0) {
   __shared__ int64_t warp_sums[kScanThreads / 32];
-  const int64_t hs = blockIdx.x;
-  const uint32_t* c = count + hs * N;
-  int64_t* off = offsets + hs * N;
-  const int64_t per = (N + kScanThreads - 1) / kScanThreads;
-  const int64_t lo_raw = static_cast<int64_t>(threadIdx.x) * per;
-  const int64_t lo = lo_raw < N ? lo_raw : N, hi = lo + per < N ? lo + per : N;
-  int64_t s = 0;
-  for (int64_t i = lo; i < hi; ++i) s += c[i];
-  // block-wide exclusive scan of s
+  __shared__ int64_t tile_base;
+  const int64_t hs = hs0 + blockIdx.y;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * kScanThreads + threadIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t incl = s;
+  const int64_t c = j < N ? count[hs * N + j] : 0;
+  int64_t incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
   if (lane == 31) warp_sums[warp] = incl;
+  if (warp == 1) {  // sum of the earlier tiles, plus where this head slot starts
+    int64_t b = 0;
+    for (int64_t t = lane; t < blockIdx.x; t += 32) b += tsum[hs * gridDim.x + t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+    if (lane == 0)
+      tile_base = b + (rowptr ? rowptr[(bh0 + hs) * NB + blk0] - rowptr[bh0 * NB + blk0] : hs * pairs_per_head);
+  }
   __syncthreads();
   if (warp == 0) {
-    int64_t ws = warp_sums[lane];
+    const int64_t ws = warp_sums[lane];
     int64_t wi = ws;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -114,13 +187,7 @@ scan_kernel(const uint32_t* __restrict__ count, int64_t* __restrict__ offsets, i
     warp_sums[lane] = wi - ws;
   }
   __syncthreads();
-  // first key-major position of this head slot: its blocks' pairs come after the earlier slots'
-  const int64_t base = rowptr ? rowptr[(bh0 + hs) * NB + blk0] - rowptr[bh0 * NB + blk0] : hs * pairs_per_head;
-  int64_t run = base + warp_sums[warp] + incl - s;
-  for (int64_t i = lo; i < hi; ++i) {
-    off[i] = run;
-    run += c[i];
-  }
+  if (j < N) offsets[hs * N + j] = tile_base + warp_sums[warp] + incl - c;
 }
 
 // ---------------------------------------------------------------- 4. main kernel: dsv_bwd_tc.cu
@@ -213,23 +280,25 @@ template <int D>
 cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t stream) {
   const int64_t W32 = (w.nblk + 31) / 32;
   const int64_t N = p.N;
-  cudaError_t e = cudaMemsetAsync(p.colbits, 0, sizeof(uint32_t) * w.nh * W32 * N, stream);
+  const int64_t ntile = (N + kBitsTile - 1) / kBitsTile;
+  const int64_t nscan = (N + kScanThreads - 1) / kScanThreads;
+  const size_t bits_smem = sizeof(uint32_t) * static_cast<size_t>(((N < kBitsTile ? N : kBitsTile) + 1) / 2);
+  cudaError_t e = cudaFuncSetAttribute(set_bits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bits_smem));
   if (e != cudaSuccess) return e;
-  const int64_t rows = w.nh * w.nblk;
-  { ProfScope prof("bwd_set_bits", stream);
-  if (p.rowptr) {
-    set_bits_csr_kernel<<<grid_for(rows * 32, 256), 256, 0, stream>>>(p.idx, p.rowptr, p.colbits, N, p.NB, p.topk,
-                                                                       w.bh0, w.blk0, w.nblk, W32, rows, p.status);
-  } else {
-    const int64_t pairs = rows * p.topk;
-    set_bits_kernel<<<grid_for(pairs, 256), 256, 0, stream>>>(p.idx, p.colbits, N, p.NB, p.topk, w.bh0, w.blk0,
-                                                               w.nblk, W32, pairs, p.status);
-  } }
-  { ProfScope prof("bwd_colpre", stream);
-  colpre_kernel<<<grid_for(w.nh * N, 256), 256, 0, stream>>>(p.colbits, p.colpre, p.count, N, W32, w.nh); }
-  { ProfScope prof("bwd_scan", stream);
-  scan_kernel<<<static_cast<unsigned>(w.nh), kScanThreads, 0, stream>>>(p.count, p.offsets, N, w.nblk * p.topk,
-                                                                          p.rowptr, p.NB, w.bh0, w.blk0); }
+  for (int64_t hs0 = 0; hs0 < w.nh; hs0 += 65535) {  // grid y / z limit
+    const unsigned nh = static_cast<unsigned>(w.nh - hs0 < 65535 ? w.nh - hs0 : 65535);
+    { ProfScope prof("bwd_set_bits", stream);
+    set_bits_kernel<<<dim3(static_cast<unsigned>(ntile), static_cast<unsigned>(2 * W32), nh), kBitsThreads,
+                      bits_smem, stream>>>(p.idx, p.rowptr, p.colbits, N, p.NB, p.topk, w.bh0, w.blk0, w.nblk, W32,
+                                           hs0, p.status); }
+    { ProfScope prof("bwd_colpre", stream);
+    colpre_kernel<<<dim3(static_cast<unsigned>(nscan), nh), kScanThreads, 0, stream>>>(
+        p.colbits, p.colpre, p.count, p.tsum, N, W32, hs0); }
+    { ProfScope prof("bwd_scan", stream);
+    scan_kernel<<<dim3(static_cast<unsigned>(nscan), nh), kScanThreads, 0, stream>>>(
+        p.count, p.tsum, p.offsets, N, w.nblk * p.topk, p.rowptr, p.NB, w.bh0, w.blk0, hs0); }
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if ((e = launch_bwd_main_tc(p, w, W32, stream)) != cudaSuccess) return e;

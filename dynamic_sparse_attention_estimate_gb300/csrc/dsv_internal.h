@@ -91,6 +91,7 @@ struct BwdParams {
   uint32_t* colpre;    // [nh][W32][N]   popcount of the words before
   uint32_t* count;     // [nh][N]
   int64_t* offsets;    // [nh][N]        first key-major position of key j (absolute within the wave)
+  int64_t* tsum;       // [nh][N / 1024] sum of count over each 1024-key tile
   int32_t* lists;      // [pairs]        partial row of each key-major position: key j's rows in
                        //                ascending query-block order
   bf16* partial;       // [pairs][2 d]   BLOCK-major rows (CTA c's k rows at c k): dK part times the
