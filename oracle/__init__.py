@@ -1,4 +1,4 @@
-"""CPU oracle for DSV's dynamic sparse attention -- TEST INFRASTRUCTURE, not product code.
+"""CPU oracles for DSV's dynamic sparse attention and the fused AdaLN operator -- TEST INFRASTRUCTURE, not product code.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU-baseline leg and
 its ``--impl reference`` arm) may import, call or execute anything here.  The product
@@ -15,7 +15,11 @@ Pins (what ties each function to something other than itself) live in ``tests/``
                      unselected keys get zero gradient);
   mass-based k     : the exp2 recipe against 2^x, the target by its defining inequality,
                      sufficiency and minimality of every k, closed forms (equal scores,
-                     one dominant key), planted mistakes rejected.
+                     one dominant key), planted mistakes rejected;
+  fused AdaLN      : torch fp64 layer_norm + modulation and its autograd, central finite
+                     differences, closed forms (constant rows give y = shift, the per-row
+                     invariants sum dx = 0 and sum dx * xhat = 0, d_shift = sum dy),
+                     planted mistakes rejected.
 """
 from .dsv_oracle import (  # noqa: F401
     block_representatives,
@@ -32,3 +36,4 @@ from .dsv_oracle import (  # noqa: F401
     sparse_attn_fwd,
     topk_select,
 )
+from .adaln_oracle import adaln_bwd, adaln_fwd, row_stats  # noqa: F401,E402
