@@ -10,8 +10,9 @@ attention backward (dQ, dK, dV), all through the C ABI (libdsv.so).
 Prints ONE JSON line (rank 0).  `value` is the effective TFLOP/s of the whole job:
 14 * B * H * N * k * d flops per step (4 N k d forward + 10 N k d backward, only the
 selected query-key pairs counted) divided by the step time, which includes the
-estimate/top-k.  Inputs are resident in HBM when the timed region starts; a 512 MiB
-memset between timed steps flushes L2 (outside the timed events).  `e2e` is the same
+estimate/top-k.  Inputs are resident in HBM when the timed region starts; between timed
+steps (outside the timed events) a 512 MiB memset flushes L2 and a read of another 512 MiB
+buffer leaves it holding clean lines.  `e2e` is the same
 metric when every step also copies its inputs host->device from pinned memory and
 its outputs (O, LSE, dQ, dK, dV) back.  Under torchrun each rank runs an independent
 replica (weak scaling, no collective on the data path).
@@ -49,6 +50,7 @@ def parse():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adaptive", action="store_true", help="skip the mass-based selection measurement")
+    ap.add_argument("--no-adaln", action="store_true", help="skip the fused AdaLN measurement")
     ap.add_argument("--heads", type=int, default=None,
                     help="run the workload with this many heads (small cases for profiler captures)")
     return ap.parse_args()
@@ -288,6 +290,44 @@ def roofline(prof, steps, wl):
 
 # ---------------------------------------------------------------- the DSV arm
 
+def adaln_measurements(dev, timed):
+    """Fused AdaLN on its two workloads: forward and backward times (L2 flushed before each call),
+    algorithmic bytes, achieved GB/s and the fraction of the measured HBM copy bandwidth."""
+    import torch
+    from dynamic_sparse_attention_estimate_gb300 import dsv_adaln_bwd, dsv_adaln_bwd_workspace, dsv_adaln_fwd
+    from dynamic_sparse_attention_estimate_gb300.binding import dsv_profile_enable, dsv_profile_read
+    from dynamic_sparse_attention_estimate_gb300.inputs import ADALN_WORKLOADS, make_adaln_inputs
+    hbm = measured_peaks()[0]
+    out = {}
+    for name, (B, N, D) in sorted(ADALN_WORKLOADS.items()):
+        g = {k: v.to(dev) for k, v in make_adaln_inputs(B, N, D).items()}
+        y = torch.empty_like(g["x"])
+        res = (torch.empty_like(g["x"]), torch.empty((B, D), dtype=torch.float32, device=dev),
+               torch.empty((B, D), dtype=torch.float32, device=dev))
+        ws = torch.empty(max(1, dsv_adaln_bwd_workspace(B, N, D)), dtype=torch.uint8, device=dev)
+        fwd = lambda: dsv_adaln_fwd(g["x"], g["scale"], g["shift"], y=y)
+        bwd = lambda: dsv_adaln_bwd(g["x"], g["scale"], g["dy"], out=res, workspace=ws)
+        for _ in range(3):
+            fwd()
+            bwd()
+        t_f, t_b = timed(fwd, 20), timed(bwd, 20)
+        dsv_profile_enable(True)
+        timed(fwd, 20)
+        timed(bwd, 20)
+        kernels = {k: v[1] / v[0] for k, v in dsv_profile_read().items() if k.startswith("adaln")}
+        dsv_profile_enable(False)
+        act = B * N * D * 2
+        b_f = 2 * act + 2 * B * D * 2                  # x in, y out, scale and shift in
+        b_b = 3 * act + B * D * 2 + 2 * B * D * 4      # x, dy in, dx out, scale in, d_scale and d_shift out
+        out[name] = {"B": B, "N": N, "D": D, "fwd_ms": t_f, "bwd_ms": t_b, "fwd_bytes": b_f, "bwd_bytes": b_b,
+                     "fwd_gbs": b_f / (t_f / 1e3) / 1e9, "bwd_gbs": b_b / (t_b / 1e3) / 1e9,
+                     "fwd_frac_of_measured_hbm": b_f / (t_f / 1e3) / 1e9 / hbm,
+                     "bwd_frac_of_measured_hbm": b_b / (t_b / 1e3) / 1e9 / hbm,
+                     "kernel_ms": kernels, "workspace_bytes": ws.numel()}
+        del g, y, res, ws
+    return out
+
+
 def dsv_arm(args):
     import torch
     import torch.distributed as dist
@@ -319,7 +359,15 @@ def dsv_arm(args):
     dq, dk, dv = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
     ws = torch.empty(dsv_sparse_attn_bwd_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, wl.k)),
                      dtype=torch.uint8, device=dev)
+    # L2 flush between timed calls: write a 512 MiB buffer (4x the 129 MB L2), then read another
+    # one, so that the lines left in L2 are clean and the next timed kernel does not pay for
+    # writing the flush's dirty lines back to HBM
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.sum()
 
     def step():
         dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k, idx=idx)
@@ -342,7 +390,7 @@ def dsv_arm(args):
         t_wall0 = time.time()
         dsv_profile_enable(True)
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             starts[i].record()
             step()
             ends[i].record()
@@ -361,16 +409,17 @@ def dsv_arm(args):
 
     # ---- stage breakdown (separately timed, same inputs)
     def timed(fn, n):
-        ts = []
-        for _ in range(n):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        """Median device time of fn over n calls, each after an L2 flush.  All n calls are
+        enqueued before one synchronisation, so the host's launch latency stays outside the
+        events (the flush ahead of each call gives the host time to enqueue)."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            flush_l2()
             a.record()
             fn()
             b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
 
     n_stage = max(3, min(20, args.steps))
     t_est = timed(lambda: dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k, idx=idx), n_stage)
@@ -473,6 +522,15 @@ def dsv_arm(args):
         except Exception as exc:  # a side measurement only
             adaptive = {"error": str(exc)[:200]}
 
+    # ---- fused AdaLN (LayerNorm + modulation) forward and backward, HBM-bound: bytes moved per
+    # call (x, dy read; y, dx written; modulation vectors and gradients) over the measured time
+    adaln = None
+    if not args.no_adaln:
+        try:
+            adaln = adaln_measurements(dev, timed)
+        except Exception as exc:  # a side measurement only
+            adaln = {"error": str(exc)[:200]}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -501,7 +559,7 @@ def dsv_arm(args):
         "estimate": {"ms": t_est, "score_elements_per_s": BH * wl.NB * wl.N / (t_est / 1e3),
                      "mma_tflops": 2.0 * wl.r * BH * wl.NB * wl.N / (t_est / 1e3) / 1e12},
         "roofline": rl, "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "dense_comparator": dense,
-        "own_dense_path": own_dense, "adaptive_selection": adaptive,
+        "own_dense_path": own_dense, "adaptive_selection": adaptive, "adaln": adaln,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

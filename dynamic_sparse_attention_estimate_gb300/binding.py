@@ -28,6 +28,7 @@ EXPORTED = (
     "dsv_profile_enable", "dsv_profile_read", "dsv_sparse_attn_bwd_noalloc",
     "dsv_estimate_mass_k", "dsv_estimate_topk_csr", "dsv_sparse_attn_fwd_csr",
     "dsv_sparse_attn_bwd_csr_workspace", "dsv_sparse_attn_bwd_csr", "dsv_csr_launch_order",
+    "dsv_adaln_fwd", "dsv_adaln_bwd_workspace", "dsv_adaln_bwd",
 )
 
 
@@ -41,6 +42,10 @@ class Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
                 ("d", ctypes.c_int64), ("r", ctypes.c_int64), ("block", ctypes.c_int64),
                 ("k", ctypes.c_int64), ("scale", ctypes.c_float)]
+
+
+class AdalnDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("N", ctypes.c_int64), ("D", ctypes.c_int64), ("eps", ctypes.c_float)]
 
 
 def library_path() -> str:
@@ -91,6 +96,13 @@ def load_library(path: Optional[str] = None):
     lib.dsv_sparse_attn_bwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz,
                                             vp]
     lib.dsv_sparse_attn_bwd_csr.restype = st
+    ap = ctypes.POINTER(AdalnDims)
+    lib.dsv_adaln_fwd.argtypes = [ap, vp, vp, vp, vp, vp]
+    lib.dsv_adaln_fwd.restype = st
+    lib.dsv_adaln_bwd_workspace.argtypes = [ap]
+    lib.dsv_adaln_bwd_workspace.restype = sz
+    lib.dsv_adaln_bwd.argtypes = [ap, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.dsv_adaln_bwd.restype = st
     lib.dsv_profile_enable.argtypes = [st]
     lib.dsv_profile_enable.restype = st
     lib.dsv_profile_read.argtypes = [ctypes.c_char_p, sz]
@@ -318,6 +330,62 @@ def dsv_sparse_attn_bwd_csr(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, 
                                        _ptr(workspace),
                                        workspace.numel(), _stream_ptr(q)), "dsv_sparse_attn_bwd_csr")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------- fused AdaLN
+
+def _adaln_dims(x: torch.Tensor, eps: float) -> AdalnDims:
+    B, N, D = x.shape
+    return AdalnDims(int(B), int(N), int(D), float(eps))
+
+
+def _need_mod(t: torch.Tensor, name: str, x: torch.Tensor):
+    _need(t, name, torch.bfloat16, 2)
+    if t.shape != (x.shape[0], x.shape[2]):
+        raise ValueError(f"{name} must be [B, D] = {(x.shape[0], x.shape[2])}, got {tuple(t.shape)}")
+
+
+def dsv_adaln_fwd(x: torch.Tensor, scale: torch.Tensor, shift: torch.Tensor, eps: float = 1e-6,
+                  y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y [B, N, D] bf16 = LayerNorm(x) * (1 + scale[b]) + shift[b] (see include/dsv.h)."""
+    _need(x, "x", torch.bfloat16, 3)
+    _need_mod(scale, "scale", x)
+    _need_mod(shift, "shift", x)
+    if y is None:
+        y = torch.empty_like(x)
+    dims = _adaln_dims(x, eps)
+    _check(load_library().dsv_adaln_fwd(ctypes.byref(dims), _ptr(x), _ptr(scale), _ptr(shift), _ptr(y),
+                                        _stream_ptr(x)), "dsv_adaln_fwd")
+    return y
+
+
+def dsv_adaln_bwd_workspace(B: int, N: int, D: int, eps: float = 1e-6) -> int:
+    dims = AdalnDims(int(B), int(N), int(D), float(eps))
+    return int(load_library().dsv_adaln_bwd_workspace(ctypes.byref(dims)))
+
+
+def dsv_adaln_bwd(x: torch.Tensor, scale: torch.Tensor, dy: torch.Tensor, eps: float = 1e-6,
+                  out: Optional[Tuple[torch.Tensor, torch.Tensor, torch.Tensor]] = None,
+                  workspace: Optional[torch.Tensor] = None):
+    """(dx bf16 [B, N, D], d_scale fp32 [B, D], d_shift fp32 [B, D]) for the loss gradient dy."""
+    _need(x, "x", torch.bfloat16, 3)
+    _need(dy, "dy", torch.bfloat16, 3)
+    _need_mod(scale, "scale", x)
+    if dy.shape != x.shape:
+        raise ValueError("dy must have the shape of x")
+    B, N, D = x.shape
+    if out is None:
+        out = (torch.empty_like(x), torch.empty((B, D), dtype=torch.float32, device=x.device),
+               torch.empty((B, D), dtype=torch.float32, device=x.device))
+    dx, d_scale, d_shift = out
+    dims = _adaln_dims(x, eps)
+    lib = load_library()
+    need = int(lib.dsv_adaln_bwd_workspace(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check(lib.dsv_adaln_bwd(ctypes.byref(dims), _ptr(x), _ptr(scale), _ptr(dy), _ptr(dx), _ptr(d_scale),
+                             _ptr(d_shift), _ptr(workspace), workspace.numel(), _stream_ptr(x)), "dsv_adaln_bwd")
+    return dx, d_scale, d_shift
 
 
 def dsv_last_device_status(device: Optional[torch.device] = None) -> int:

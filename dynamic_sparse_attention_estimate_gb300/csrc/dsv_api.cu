@@ -533,6 +533,77 @@ dsv_status dsv_last_device_status(void* stream) {
   return ok();
 }
 
+// ---------------------------------------------------------------- fused AdaLN
+static dsv_status check_adaln(const dsv_adaln_dims* d) {
+  if (!d) return fail(DSV_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->N < 1) return fail(DSV_ERR_INVALID_ARG, "B and N must be >= 1");
+  if (d->D < 8 || d->D > 8192 || d->D % 8)
+    return fail(DSV_ERR_INVALID_ARG, "D must be a multiple of 8 in [8, 8192] (got %lld)", (long long)d->D);
+  if (d->B * d->N > (1LL << 40)) return fail(DSV_ERR_INVALID_ARG, "B*N too large");
+  if (!(d->eps >= 0.f) || d->eps > 3.0e38f) return fail(DSV_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  return DSV_OK;
+}
+
+dsv_status dsv_adaln_fwd(const dsv_adaln_dims* dims, const void* x, const void* scale, const void* shift, void* y,
+                         void* stream) {
+  dsv_status s = check_adaln(dims);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(x);
+  DSV_NEED_PTR(scale);
+  DSV_NEED_PTR(shift);
+  DSV_NEED_PTR(y);
+  dsv::AdalnParams p{};
+  p.x = x;
+  p.scale = scale;
+  p.shift = shift;
+  p.y = y;
+  p.B = dims->B;
+  p.N = dims->N;
+  p.D = dims->D;
+  p.eps = dims->eps;
+  if ((s = status_word(&p.status)) != DSV_OK) return s;
+  cudaError_t e = dsv::launch_adaln_fwd(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "adaln forward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+size_t dsv_adaln_bwd_workspace(const dsv_adaln_dims* dims) {
+  if (check_adaln(dims) != DSV_OK) return 0;
+  return up(dsv::adaln_tiling(dims->B, dims->N, dims->D, true).partial_bytes);
+}
+
+dsv_status dsv_adaln_bwd(const dsv_adaln_dims* dims, const void* x, const void* scale, const void* dy, void* dx,
+                         float* d_scale, float* d_shift, void* ws, size_t ws_bytes, void* stream) {
+  dsv_status s = check_adaln(dims);
+  if (s != DSV_OK) return s;
+  DSV_NEED_PTR(x);
+  DSV_NEED_PTR(scale);
+  DSV_NEED_PTR(dy);
+  DSV_NEED_PTR(dx);
+  DSV_NEED_PTR(d_scale);
+  DSV_NEED_PTR(d_shift);
+  const size_t need = dsv::adaln_tiling(dims->B, dims->N, dims->D, true).partial_bytes;
+  if (!ws) return fail(DSV_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need) return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the %zu needed", ws_bytes, need);
+  dsv::AdalnParams p{};
+  p.x = x;
+  p.scale = scale;
+  p.dy = dy;
+  p.dx = dx;
+  p.d_scale = d_scale;
+  p.d_shift = d_shift;
+  p.partial = static_cast<float*>(ws);
+  p.B = dims->B;
+  p.N = dims->N;
+  p.D = dims->D;
+  p.eps = dims->eps;
+  if ((s = status_word(&p.status)) != DSV_OK) return s;
+  cudaError_t e = dsv::launch_adaln_bwd(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "adaln backward launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 // ---------------------------------------------------------------- backward with library-held scratch
 // For callers that cannot allocate device memory (see include/dsv.h).  The scratch is a
 // fixed device array; host code only ever uses the address looked up per device below.

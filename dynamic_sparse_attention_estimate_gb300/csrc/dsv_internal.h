@@ -100,6 +100,32 @@ struct BwdParams {
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
 };
 cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream);
+
+// ---------------------------------------------------------------- fused AdaLN (adaln.cu)
+struct AdalnParams {
+  const void* x;         // bf16 [B][N][D]
+  const void* scale;     // bf16 [B][D]
+  const void* shift;     // bf16 [B][D] (forward)
+  void* y;               // bf16 [B][N][D] (forward)
+  const void* dy;        // bf16 [B][N][D] (backward)
+  void* dx;              // bf16 [B][N][D] (backward)
+  float* d_scale;        // fp32 [B][D] (backward)
+  float* d_shift;        // fp32 [B][D] (backward)
+  float* partial;        // fp32 [B * tiles][2][D] workspace (backward)
+  int64_t B, N, D;
+  float eps;
+  unsigned int* status;  // device status word (timeout bit)
+};
+// Tokens per CTA tile: about this many tiles over all samples (two CTAs on each of the 152 SMs).
+constexpr int64_t kAdalnFwdTiles = 2 * 152;
+constexpr int64_t kAdalnBwdTiles = 2 * 152;
+struct AdalnTiling {
+  int64_t rows_per_tile, tiles_per_b;
+  size_t partial_bytes;
+};
+AdalnTiling adaln_tiling(int64_t B, int64_t N, int64_t D, bool backward);
+cudaError_t launch_adaln_fwd(const AdalnParams& p, cudaStream_t stream);
+cudaError_t launch_adaln_bwd(const AdalnParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main_tc(const BwdParams& p, const BwdWave& w, int64_t W32, cudaStream_t stream);
 
 }  // namespace dsv

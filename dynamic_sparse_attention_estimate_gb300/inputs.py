@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for DSV's dynamic sparse 3D attention.
+"""Seeded synthetic inputs for DSV's dynamic sparse 3D attention and the fused AdaLN operator.
 
 This module only draws random numbers and lays tokens out; it holds none of the
 method's arithmetic (no estimate, no selection, no attention). Both the CUDA path
@@ -195,3 +195,31 @@ def sample_blocks(n_blocks_total: int, count: int, seed: int = 0) -> np.ndarray:
     rng = np.random.default_rng(seed + 31337)
     count = min(count, n_blocks_total)
     return np.sort(rng.choice(n_blocks_total, size=count, replace=False))
+
+
+# ---------------------------------------------------------------- fused AdaLN inputs
+# (B, N, D) of the AdaLN workloads: the short clip's 16,384 tokens at its attention width
+# H * d = 12 * 64 = 768, and the same tokens at a wide MMDiT width of 3,072.
+ADALN_WORKLOADS = {
+    "short": (1, 16384, 768),
+    "wide": (1, 16384, 3072),
+}
+
+
+def make_adaln_inputs(B: int, N: int, D: int, seed: int = 0) -> Dict[str, torch.Tensor]:
+    """x [B, N, D], scale [B, D], shift [B, D], dy [B, N, D] as bf16 CPU tensors.
+
+    One CPU generator seeded with ``seed + 15485863``; draw order: x's N(0, 1) entries, one
+    N(0, 1) offset and one U(0.5, 3) spread per token (x = spread * entry + offset, so rows
+    differ in mean and scale as hidden states do), scale ~ 0.5 N(0, 1), shift ~ N(0, 1),
+    dy ~ N(0, 1); all rounded to bf16.
+    """
+    g = torch.Generator().manual_seed(seed + 15485863)
+    e = torch.randn(B, N, D, generator=g)
+    off = torch.randn(B, N, 1, generator=g)
+    spread = 0.5 + 2.5 * torch.rand(B, N, 1, generator=g)
+    x = (spread * e + off).to(torch.bfloat16)
+    scale = (0.5 * torch.randn(B, D, generator=g)).to(torch.bfloat16)
+    shift = torch.randn(B, D, generator=g).to(torch.bfloat16)
+    dy = torch.randn(B, N, D, generator=g).to(torch.bfloat16)
+    return {"x": x.contiguous(), "scale": scale.contiguous(), "shift": shift.contiguous(), "dy": dy.contiguous()}

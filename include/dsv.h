@@ -235,6 +235,40 @@ dsv_status dsv_last_device_status(void* stream);
 dsv_status dsv_profile_enable(int on);
 size_t dsv_profile_read(char* buf, size_t buf_bytes);
 
+/* ---------------------------------------------------------------- fused AdaLN
+ * LayerNorm + modulation in one pass over HBM, forward and backward (AdaptiveLoad page,
+ * "AdaptiveLoad: Towards Efficient Video Diffusion Transformer Training", technical summary
+ * section 2B: normalisation and modulation fused into one launch, statistics kept on chip,
+ * and the modulation gradients reduced in (D tile, N tile) blocks so that reads stay
+ * coalesced along D).  Per token n of sample b, over its D features:
+ *   mean = sum_d x / D,  var = sum_d (x - mean)^2 / D,  rstd = 1 / sqrt(var + eps),
+ *   xhat = (x - mean) * rstd,   y = xhat * (1 + scale[b]) + shift[b].
+ * The backward recomputes mean and rstd from x (nothing is saved by the forward) and returns
+ *   dx = rstd * (g - mean_d(g) - xhat * mean_d(g * xhat)),  g = dy * (1 + scale[b]),
+ *   d_scale[b] = sum_n dy * xhat,   d_shift[b] = sum_n dy.
+ * Arithmetic: bf16 inputs, fp32 statistics and sums, bf16 y / dx, fp32 d_scale / d_shift;
+ * bitwise reproducible (fixed summation order, no float atomics).
+ * Layouts (contiguous, device memory owned by the caller, 16-byte aligned):
+ *   x, y, dy, dx: bf16 [B][N][D];  scale, shift: bf16 [B][D];  d_scale, d_shift: fp32 [B][D].
+ * Validation before any launch: B, N >= 1; D a multiple of 8 in [8, 8192]; eps >= 0 and
+ * finite; no NULL or misaligned pointer (DSV_ERR_INVALID_ARG).  With eps = 0 a constant row
+ * has var = 0 and its y / dx are NaN, as the definition gives.  Asynchronous on `stream`.
+ */
+typedef struct {
+  int64_t B;   /* samples */
+  int64_t N;   /* tokens per sample */
+  int64_t D;   /* features per token */
+  float eps;   /* added to the variance inside the square root */
+} dsv_adaln_dims;
+
+dsv_status dsv_adaln_fwd(const dsv_adaln_dims* dims, const void* x, const void* scale, const void* shift,
+                         void* y, void* stream);
+/* Bytes of workspace dsv_adaln_bwd needs (per-tile partial sums of the modulation gradients). */
+size_t dsv_adaln_bwd_workspace(const dsv_adaln_dims* dims);
+/* ws: at least dsv_adaln_bwd_workspace(dims) bytes, 256-byte aligned (DSV_ERR_WORKSPACE otherwise). */
+dsv_status dsv_adaln_bwd(const dsv_adaln_dims* dims, const void* x, const void* scale, const void* dy, void* dx,
+                         float* d_scale, float* d_shift, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

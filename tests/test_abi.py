@@ -97,3 +97,25 @@ def test_mass_selection_arguments_rejected_before_launch(lib):
     assert lib.dsv_estimate_topk_csr(ctypes.byref(dims), p, p, p, None, p, None) == 1           # no rowptr
     bad_r = make_dims(1, 2, 1024, 64, 24, 1024)
     assert lib.dsv_estimate_mass_k(ctypes.byref(bad_r), p, p, 0.02, 58982, 0, p, p, None, None) == 2
+
+
+def test_adaln_arguments_rejected_before_launch(lib):
+    from dynamic_sparse_attention_estimate_gb300.binding import AdalnDims
+    p = ctypes.c_void_p(0x1000)
+    good = AdalnDims(1, 16, 768, 1e-6)
+    for bad, what in ((AdalnDims(1, 16, 12, 1e-6), b"D"), (AdalnDims(1, 16, 8200, 1e-6), b"D"),
+                      (AdalnDims(0, 16, 64, 1e-6), b"B and N"), (AdalnDims(1, 0, 64, 1e-6), b"B and N"),
+                      (AdalnDims(1, 16, 64, -1.0), b"eps"), (AdalnDims(1, 16, 64, float("nan")), b"eps")):
+        assert lib.dsv_adaln_fwd(ctypes.byref(bad), p, p, p, p, None) == 1
+        assert what in lib.dsv_last_error_message()
+        assert lib.dsv_adaln_bwd_workspace(ctypes.byref(bad)) == 0
+    assert lib.dsv_adaln_fwd(ctypes.byref(good), p, None, p, p, None) == 1
+    assert b"NULL" in lib.dsv_last_error_message()
+    assert lib.dsv_adaln_fwd(ctypes.byref(good), p, p, ctypes.c_void_p(0x1008), p, None) == 1
+    assert b"aligned" in lib.dsv_last_error_message()
+    need = lib.dsv_adaln_bwd_workspace(ctypes.byref(good))
+    assert need >= 2 * 768 * 4      # at least one tile's partial row of d_scale and d_shift
+    args = [ctypes.byref(good), p, p, p, p, p, p]
+    assert lib.dsv_adaln_bwd(*args, None, 0, None) == 3
+    assert lib.dsv_adaln_bwd(*args, p, need - 256, None) == 3
+    assert lib.dsv_adaln_bwd(*args, ctypes.c_void_p(0x1010), need, None) == 3
