@@ -72,6 +72,11 @@ DSV_DEVICE float2 add2(float2 a, float2 b) {
   asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)));
   return as_f2(d);
 }
+DSV_DEVICE float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(d);
+}
 DSV_DEVICE float2 bcast(float v) { return make_float2(v, v); }
 DSV_DEVICE uint32_t word(const uint4& u, int j) { return j == 0 ? u.x : j == 1 ? u.y : j == 2 ? u.z : u.w; }
 
@@ -94,10 +99,11 @@ DSV_DEVICE float2 row_sum2(float2 v, float2* slot, int W, int rg, int warp, int 
 }
 
 // Row mean and rstd of a packed row (two passes over the registers: the mean, then the
-// squares about it; the division by D is correctly rounded).
+// squares about it).  The mean is sum * (1/D) corrected once by its exact FMA residual
+// sum - mean * D, which makes it exact whenever sum / D is representable (a constant row).
 template <int VPL>
 DSV_DEVICE void row_stats(const uint4 (&r)[VPL], const bool (&valid)[VPL], float* red0, float* red1, const RowGeom& g,
-                          int rg, int warp, int lane, float Df, float eps, float& mean, float& rstd) {
+                          int rg, int warp, int lane, float Df, float invD, float eps, float& mean, float& rstd) {
   float2 s = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
@@ -105,7 +111,9 @@ DSV_DEVICE void row_stats(const uint4 (&r)[VPL], const bool (&valid)[VPL], float
 #pragma unroll
     for (int j = 0; j < 4; ++j) s = add2(s, pair(word(r[i], j)));
   }
-  mean = row_sum(s.x + s.y, red0, g.W, rg, warp, lane) / Df;
+  const float sum = row_sum(s.x + s.y, red0, g.W, rg, warp, lane);
+  const float m0 = sum * invD;
+  mean = fmaf(fmaf(-m0, Df, sum), invD, m0);
   const float2 nm = bcast(-mean);
   float2 q = make_float2(0.f, 0.f);
 #pragma unroll
@@ -117,7 +125,7 @@ DSV_DEVICE void row_stats(const uint4 (&r)[VPL], const bool (&valid)[VPL], float
       q = fma2(c, c, q);
     }
   }
-  rstd = rsqrtf(row_sum(q.x + q.y, red1, g.W, rg, warp, lane) / Df + eps);
+  rstd = rsqrtf(fmaf(row_sum(q.x + q.y, red1, g.W, rg, warp, lane), invD, eps));
 }
 
 // ---------------------------------------------------------------- tensor-memory-accelerator staging
@@ -142,11 +150,13 @@ struct Staging {
 
 // ---------------------------------------------------------------- forward
 template <int VPL>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, const uint4* __restrict__ shift,
-                 uint4* __restrict__ y, int64_t N, RowGeom g, Staging st, float Df, float eps, int64_t rows_per_tile,
-                 int64_t tiles_per_b, unsigned int* status) {
-  extern __shared__ __align__(128) uint4 sbuf[];   // [NS][R][nvec]: x rows
+                 uint4* __restrict__ y, int64_t N, RowGeom g, Staging st, float Df, float invD, float eps,
+                 int64_t rows_per_tile, int64_t tiles_per_b, unsigned int* status) {
+  // [NS][R][nvec] x rows, then the sample's modulation as fp32 pairs: (1 + scale) and shift,
+  // each [4][nvec] (pair j of vector v at j * nvec + v: consecutive lanes, consecutive words)
+  extern __shared__ __align__(128) uint4 sbuf[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ float red[2][kWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,16 +183,25 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
   if (tid == 0)
     for (int c = 0; c < st.NS && c < nchunk; ++c) issue(c);
 
+  float2* mod_s = reinterpret_cast<float2*>(sbuf + st.NS * stage_vecs);   // 1 + scale
+  float2* mod_h = mod_s + 4 * g.nvec;                                      // shift
+  for (int v = tid; v < g.nvec; v += kThreads) {
+    const uint4 a = __ldg(scale + b * g.nvec + v), h = __ldg(shift + b * g.nvec + v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mod_s[j * g.nvec + v] = add2(pair(word(a, j)), bcast(1.f));
+      mod_h[j * g.nvec + v] = pair(word(h, j));
+    }
+  }
+  __syncthreads();
+
   int vec[VPL];
   bool valid[VPL];
-  uint4 s1[VPL], sh[VPL];   // this lane's (scale, shift) vectors of sample b
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int local = lane + 32 * i;
     vec[i] = part * g.slab + local;
     valid[i] = local < g.slab && vec[i] < g.nvec;
-    s1[i] = valid[i] ? __ldg(scale + b * g.nvec + vec[i]) : make_uint4(0, 0, 0, 0);
-    sh[i] = valid[i] ? __ldg(shift + b * g.nvec + vec[i]) : make_uint4(0, 0, 0, 0);
   }
 
   bool ok = true;
@@ -199,9 +218,9 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
       for (int i = 0; i < VPL; ++i)
         cur[i] = (active && valid[i]) ? stage[static_cast<size_t>(lr) * g.nvec + vec[i]] : make_uint4(0, 0, 0, 0);
       float mean, rstd;
-      row_stats<VPL>(cur, valid, red[0], red[1], g, rg, warp, lane, Df, eps, mean, rstd);
+      row_stats<VPL>(cur, valid, red[0], red[1], g, rg, warp, lane, Df, invD, eps, mean, rstd);
       if (active && ok) {
-        // y = xhat * (1 + scale) + shift = fma(xhat, scale, xhat) + shift, xhat = fma(x, rstd, -mean rstd)
+        // y = fma(xhat, 1 + scale, shift), xhat = fma(x, rstd, -mean rstd)
         const float2 rs2 = bcast(rstd), nmr = bcast(-mean * rstd);
         uint4* yr = y + (b * N + row) * g.nvec;
 #pragma unroll
@@ -211,7 +230,7 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float2 xh = fma2(pair(word(cur[i], j)), rs2, nmr);
-            const float2 v = add2(fma2(xh, pair(word(s1[i], j)), xh), pair(word(sh[i], j)));
+            const float2 v = fma2(xh, mod_s[j * g.nvec + vec[i]], mod_h[j * g.nvec + vec[i]]);
             o[j] = pack_bf16x2(v.x, v.y);
           }
           __stcs(yr + vec[i], make_uint4(o[0], o[1], o[2], o[3]));
@@ -229,10 +248,11 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
 template <int VPL>
 __global__ void __launch_bounds__(kThreads, VPL <= 3 ? 2 : 1)
 adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, const uint4* __restrict__ dy,
-                 uint4* __restrict__ dx, float* __restrict__ part_out, int64_t N, RowGeom g, Staging st, int D,
-                 float Df, float eps, int64_t rows_per_tile, int64_t tiles_per_b, unsigned int* status) {
-  // [NS][2][R][nvec]: x rows then dy rows per stage; after the loop the same memory holds the
-  // row groups' modulation-gradient partials [RG][2][D] (fp32)
+                 uint4* __restrict__ dx, float* __restrict__ part_out, unsigned int* __restrict__ tickets,
+                 int tickets_n, int64_t N, RowGeom g, Staging st, int D, float Df, float invD, float eps,
+                 int64_t rows_per_tile, int64_t tiles_per_b, unsigned int* status) {
+  // [NS][2][R][nvec]: x rows then dy rows per stage, then (1 + scale) as fp32 pairs [4][nvec];
+  // after the loop the stages hold the row groups' modulation-gradient partials [RG][2][D]
   extern __shared__ __align__(128) uint4 sbuf[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ float red[2][kWarps];
@@ -262,17 +282,29 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
   };
   if (tid == 0)
     for (int c = 0; c < st.NS && c < nchunk; ++c) issue(c);
+  // the column-sum kernel may be scheduled once every CTA of this grid has started; it waits
+  // for this grid's completion before reading anything
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // the column-sum kernel's tickets start at zero (it runs after this kernel on the stream)
+  if (blockIdx.x == 0)
+    for (int i = tid; i < tickets_n; i += kThreads) tickets[i] = 0u;
+
+  float2* mod_s = reinterpret_cast<float2*>(sbuf + st.NS * 2 * half_vecs);   // 1 + scale
+  for (int v = tid; v < g.nvec; v += kThreads) {
+    const uint4 a = __ldg(scale + b * g.nvec + v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mod_s[j * g.nvec + v] = add2(pair(word(a, j)), bcast(1.f));
+  }
+  __syncthreads();
 
   int vec[VPL];
   bool valid[VPL];
-  uint4 s1[VPL];
   float2 acc_s[VPL][4], acc_b[VPL][4];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int local = lane + 32 * i;
     vec[i] = part * g.slab + local;
     valid[i] = local < g.slab && vec[i] < g.nvec;
-    s1[i] = valid[i] ? __ldg(scale + b * g.nvec + vec[i]) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc_s[i][j] = acc_b[i][j] = make_float2(0.f, 0.f);
   }
@@ -295,7 +327,7 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
         cd[i] = (active && valid[i]) ? sd[o] : make_uint4(0, 0, 0, 0);
       }
       float mean, rstd;
-      row_stats<VPL>(cx, valid, red[0], red[1], g, rg, warp, lane, Df, eps, mean, rstd);
+      row_stats<VPL>(cx, valid, red[0], red[1], g, rg, warp, lane, Df, invD, eps, mean, rstd);
       // a padding row (not active) has x = dy = 0; its rstd may be inf when eps = 0, so it enters
       // through rs2 = 0 and nothing below multiplies an inf
       const float2 rs2 = bcast(active ? rstd : 0.f), nmr = bcast(active ? -mean * rstd : 0.f);
@@ -307,7 +339,7 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
         for (int j = 0; j < 4; ++j) {
           const float2 d = pair(word(cd[i], j));
           const float2 xh = fma2(pair(word(cx[i], j)), rs2, nmr);
-          const float2 gg = fma2(d, pair(word(s1[i], j)), d);     // dy * (1 + scale)
+          const float2 gg = mul2(d, mod_s[j * g.nvec + vec[i]]);     // dy * (1 + scale)
           sg = add2(sg, gg);
           sgx = fma2(gg, xh, sgx);
           acc_s[i][j] = fma2(d, xh, acc_s[i][j]);
@@ -317,7 +349,7 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
       const float2 m = row_sum2(make_float2(sg.x + sg.y, sgx.x + sgx.y), red2, g.W, rg, warp, lane);
       if (active) {
         // dx = rstd (g - mean g - xhat mean(g xhat)) = fma(rstd, g, fma(-rstd mean(g xhat), xhat, -rstd mean g))
-        const float mg = m.x / Df, mgx = m.y / Df;
+        const float mg = m.x * invD, mgx = m.y * invD;
         const float2 a2 = bcast(rstd), b2 = bcast(-rstd * mgx), c2 = bcast(-rstd * mg);
         uint4* dxr = dx + (b * N + row) * g.nvec;
 #pragma unroll
@@ -328,7 +360,7 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
           for (int j = 0; j < 4; ++j) {
             const float2 d = pair(word(cd[i], j));
             const float2 xh = fma2(pair(word(cx[i], j)), rs2, nmr);
-            const float2 gg = fma2(d, pair(word(s1[i], j)), d);
+            const float2 gg = mul2(d, mod_s[j * g.nvec + vec[i]]);
             const float2 v = fma2(a2, gg, fma2(b2, xh, c2));
             o[j] = pack_bf16x2(v.x, v.y);
           }
@@ -365,27 +397,38 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
 }
 
 // ---------------------------------------------------------------- backward: sum of the tiles
-// One 1024-thread CTA per (sample, 32 consecutive entries of the [2][D] partial row): warp w
-// sums tiles w, w + 32, ... for its 32 entries (one per lane, coalesced; eight loads issued
-// before their in-order adds), then the 32 warp sums are added in warp order.
-constexpr int kColsumWarps = 32;
-__global__ void __launch_bounds__(kColsumWarps * 32)
-adaln_colsum_kernel(const float* __restrict__ part, float* __restrict__ d_scale, float* __restrict__ d_shift, int D,
-                    int64_t tiles_per_b) {
-  __shared__ float red[kColsumWarps][33];
+// One 256-thread CTA per (sample, 32 consecutive entries of the [2][D] partial row, group of
+// tiles): warp w sums the group's tiles w, w + 8, ... for its 32 entries (one per lane,
+// coalesced; eight loads issued before their in-order adds), the 8 warp sums are added in warp
+// order and the group's sum is stored.  The group CTAs of an entry slab then take an integer
+// ticket; the last to arrive (all groups' sums are visible to it) adds the kColGroups sums in
+// group order and resets the ticket.  The order of every addition is fixed: the result does
+// not depend on which CTA finishes last.
+constexpr int kColGroups = 8;
+__global__ void __launch_bounds__(kThreads)
+adaln_colsum_kernel(const float* __restrict__ part, float* __restrict__ group_sums, unsigned int* __restrict__ tickets,
+                    float* __restrict__ d_scale, float* __restrict__ d_shift, int D, int64_t tiles_per_b) {
+  __shared__ float red[kWarps][33];
+  __shared__ bool last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t slabs = (2 * D + 31) / 32;
-  const int64_t b = blockIdx.x / slabs;
-  const int f = static_cast<int>(blockIdx.x % slabs) * 32 + lane;
+  const int64_t grp = blockIdx.x % kColGroups;
+  const int64_t bs = blockIdx.x / kColGroups;          // (sample, slab)
+  const int64_t b = bs / slabs;
+  const int f = static_cast<int>(bs % slabs) * 32 + lane;
+  const int64_t t_lo = grp * tiles_per_b / kColGroups, t_hi = (grp + 1) * tiles_per_b / kColGroups;
+  // launched early (programmatic dependent launch): wait until the backward grid has finished
+  // and its partial rows are visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   float t = 0.f;
   if (f < 2 * D) {
     const float* p = part + static_cast<size_t>(b) * tiles_per_b * 2 * D + f;
-    for (int64_t t0 = warp; t0 < tiles_per_b; t0 += 8 * kColsumWarps) {
+    for (int64_t t0 = t_lo + warp; t0 < t_hi; t0 += 8 * kWarps) {
       float v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int64_t tl = t0 + static_cast<int64_t>(u) * kColsumWarps;
-        v[u] = tl < tiles_per_b ? p[static_cast<size_t>(tl) * 2 * D] : 0.f;
+        const int64_t tl = t0 + static_cast<int64_t>(u) * kWarps;
+        v[u] = tl < t_hi ? p[static_cast<size_t>(tl) * 2 * D] : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) t += v[u];
@@ -393,13 +436,27 @@ adaln_colsum_kernel(const float* __restrict__ part, float* __restrict__ d_scale,
   }
   red[warp][lane] = t;
   __syncthreads();
-  if (warp == 0 && f < 2 * D) {
+  float* gs = group_sums + (static_cast<size_t>(b) * kColGroups) * 2 * D;
+  if (warp == 0) {
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kColsumWarps; ++w) s += red[w][lane];
+    for (int w = 0; w < kWarps; ++w) s += red[w][lane];
+    if (f < 2 * D) gs[grp * 2 * D + f] = s;
+    __threadfence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(tickets + bs, 1u) == kColGroups - 1;
+  __syncthreads();
+  if (!last || warp != 0) return;
+  __threadfence();
+  if (f < 2 * D) {
+    float s = 0.f;
+#pragma unroll
+    for (int g2 = 0; g2 < kColGroups; ++g2) s += __ldcg(gs + g2 * 2 * D + f);
     if (f < D) d_scale[b * D + f] = s;
     else d_shift[b * D + (f - D)] = s;
   }
+  if (lane == 0) tickets[bs] = 0u;
 }
 
 RowGeom geom_for(int64_t D) {
@@ -447,7 +504,11 @@ AdalnTiling adaln_tiling(int64_t B, int64_t N, int64_t D, bool backward) {
   if (per_b < 1) per_b = 1;
   t.rows_per_tile = (N + per_b - 1) / per_b;
   t.tiles_per_b = (N + t.rows_per_tile - 1) / t.rows_per_tile;
-  t.partial_bytes = backward ? static_cast<size_t>(B * t.tiles_per_b) * 2 * D * sizeof(float) : 0;
+  // backward workspace: per-tile partial rows, per-group sums, one ticket per (sample, slab)
+  t.partial_bytes = static_cast<size_t>(B * t.tiles_per_b) * 2 * D * sizeof(float);
+  t.group_bytes = static_cast<size_t>(B * kColGroups) * 2 * D * sizeof(float);
+  t.tickets = B * ((2 * D + 31) / 32);
+  t.workspace_bytes = backward ? t.partial_bytes + t.group_bytes + static_cast<size_t>(t.tickets) * 4 : 0;
   return t;
 }
 
@@ -456,19 +517,20 @@ cudaError_t launch_adaln_fwd(const AdalnParams& p, cudaStream_t stream) {
   const AdalnTiling t = adaln_tiling(p.B, p.N, p.D, false);
   const Staging st = staging_for(g, 2 * p.D, t.rows_per_tile, kFwdStageBytes, kFwdStages);
   using Kern = void (*)(const uint4*, const uint4*, const uint4*, uint4*, int64_t, RowGeom, Staging, float, float,
-                        int64_t, int64_t, unsigned int*);
+                        float, int64_t, int64_t, unsigned int*);
   Kern k = nullptr;
   cudaError_t e = pick_vpl<Kern>(g.slab, adaln_fwd_kernel<1>, adaln_fwd_kernel<2>, adaln_fwd_kernel<3>,
                                  adaln_fwd_kernel<4>, &k);
   if (e != cudaSuccess) return e;
-  const size_t smem = static_cast<size_t>(st.NS) * st.R * 2 * p.D;
+  const size_t smem = static_cast<size_t>(st.NS) * st.R * 2 * p.D + 2 * static_cast<size_t>(p.D) * sizeof(float);
   if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
       cudaSuccess)
     return e;
   ProfScope prof("adaln_fwd", stream);
   k<<<static_cast<unsigned>(p.B * t.tiles_per_b), kThreads, smem, stream>>>(
       static_cast<const uint4*>(p.x), static_cast<const uint4*>(p.scale), static_cast<const uint4*>(p.shift),
-      static_cast<uint4*>(p.y), p.N, g, st, static_cast<float>(p.D), p.eps, t.rows_per_tile, t.tiles_per_b, p.status);
+      static_cast<uint4*>(p.y), p.N, g, st, static_cast<float>(p.D), 1.0f / static_cast<float>(p.D), p.eps,
+      t.rows_per_tile, t.tiles_per_b, p.status);
   return cudaGetLastError();
 }
 
@@ -476,8 +538,8 @@ cudaError_t launch_adaln_bwd(const AdalnParams& p, cudaStream_t stream) {
   const RowGeom g = geom_for(p.D);
   const AdalnTiling t = adaln_tiling(p.B, p.N, p.D, true);
   const Staging st = staging_for(g, 4 * p.D, t.rows_per_tile, kBwdStageBytes, kBwdStages);
-  using Kern = void (*)(const uint4*, const uint4*, const uint4*, uint4*, float*, int64_t, RowGeom, Staging, int, float,
-                        float, int64_t, int64_t, unsigned int*);
+  using Kern = void (*)(const uint4*, const uint4*, const uint4*, uint4*, float*, unsigned int*, int, int64_t, RowGeom,
+                        Staging, int, float, float, float, int64_t, int64_t, unsigned int*);
   Kern k = nullptr;
   cudaError_t e = pick_vpl<Kern>(g.slab, adaln_bwd_kernel<1>, adaln_bwd_kernel<2>, adaln_bwd_kernel<3>,
                                  adaln_bwd_kernel<4>, &k);
@@ -485,20 +547,33 @@ cudaError_t launch_adaln_bwd(const AdalnParams& p, cudaStream_t stream) {
   // the stages (x and dy) also hold the row groups' partials after the loop: NS R >= 2 RG
   const size_t stages = static_cast<size_t>(st.NS) * st.R * 4 * p.D;
   const size_t partials = static_cast<size_t>(g.RG) * 2 * p.D * sizeof(float);
-  const size_t smem = stages > partials ? stages : partials;
+  const size_t smem = (stages > partials ? stages : partials) + static_cast<size_t>(p.D) * sizeof(float);
+  float* group_sums = p.partial + t.partial_bytes / sizeof(float);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(group_sums + t.group_bytes / sizeof(float));
   if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
       cudaSuccess)
     return e;
   { ProfScope prof("adaln_bwd", stream);
   k<<<static_cast<unsigned>(p.B * t.tiles_per_b), kThreads, smem, stream>>>(
       static_cast<const uint4*>(p.x), static_cast<const uint4*>(p.scale), static_cast<const uint4*>(p.dy),
-      static_cast<uint4*>(p.dx), p.partial, p.N, g, st, static_cast<int>(p.D), static_cast<float>(p.D), p.eps,
-      t.rows_per_tile, t.tiles_per_b, p.status); }
+      static_cast<uint4*>(p.dx), p.partial, tickets, static_cast<int>(t.tickets), p.N, g, st, static_cast<int>(p.D),
+      static_cast<float>(p.D), 1.0f / static_cast<float>(p.D), p.eps, t.rows_per_tile, t.tiles_per_b, p.status); }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t slabs = (2 * p.D + 31) / 32;
   { ProfScope prof("adaln_colsum", stream);
-  adaln_colsum_kernel<<<static_cast<unsigned>(p.B * slabs), kColsumWarps * 32, 0, stream>>>(
-      p.partial, p.d_scale, p.d_shift, static_cast<int>(p.D), t.tiles_per_b); }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * slabs * kColGroups));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, adaln_colsum_kernel, static_cast<const float*>(p.partial), group_sums, tickets,
+                         p.d_scale, p.d_shift, static_cast<int>(p.D), t.tiles_per_b);
+  if (e != cudaSuccess) return e; }
   return cudaGetLastError();
 }
 

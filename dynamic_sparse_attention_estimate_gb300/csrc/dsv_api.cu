@@ -569,7 +569,7 @@ dsv_status dsv_adaln_fwd(const dsv_adaln_dims* dims, const void* x, const void* 
 
 size_t dsv_adaln_bwd_workspace(const dsv_adaln_dims* dims) {
   if (check_adaln(dims) != DSV_OK) return 0;
-  return up(dsv::adaln_tiling(dims->B, dims->N, dims->D, true).partial_bytes);
+  return up(dsv::adaln_tiling(dims->B, dims->N, dims->D, true).workspace_bytes);
 }
 
 dsv_status dsv_adaln_bwd(const dsv_adaln_dims* dims, const void* x, const void* scale, const void* dy, void* dx,
@@ -582,7 +582,7 @@ dsv_status dsv_adaln_bwd(const dsv_adaln_dims* dims, const void* x, const void* 
   DSV_NEED_PTR(dx);
   DSV_NEED_PTR(d_scale);
   DSV_NEED_PTR(d_shift);
-  const size_t need = dsv::adaln_tiling(dims->B, dims->N, dims->D, true).partial_bytes;
+  const size_t need = dsv::adaln_tiling(dims->B, dims->N, dims->D, true).workspace_bytes;
   if (!ws) return fail(DSV_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   if (ws_bytes < need) return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the %zu needed", ws_bytes, need);

@@ -111,17 +111,20 @@ struct AdalnParams {
   void* dx;              // bf16 [B][N][D] (backward)
   float* d_scale;        // fp32 [B][D] (backward)
   float* d_shift;        // fp32 [B][D] (backward)
-  float* partial;        // fp32 [B * tiles][2][D] workspace (backward)
+  float* partial;        // backward workspace: fp32 [B * tiles][2][D] partials, fp32 [B * 8][2][D]
+                         // group sums, u32 tickets (see adaln_tiling)
   int64_t B, N, D;
   float eps;
   unsigned int* status;  // device status word (timeout bit)
 };
-// Tokens per CTA tile: about this many tiles over all samples (two CTAs on each of the 152 SMs).
-constexpr int64_t kAdalnFwdTiles = 2 * 152;
+// Tokens per CTA tile: about this many tiles over all samples (three forward or two backward
+// CTAs on each of the 152 SMs).
+constexpr int64_t kAdalnFwdTiles = 3 * 152;
 constexpr int64_t kAdalnBwdTiles = 2 * 152;
 struct AdalnTiling {
   int64_t rows_per_tile, tiles_per_b;
-  size_t partial_bytes;
+  size_t partial_bytes, group_bytes, workspace_bytes;   // backward workspace layout
+  int64_t tickets;
 };
 AdalnTiling adaln_tiling(int64_t B, int64_t N, int64_t D, bool backward);
 cudaError_t launch_adaln_fwd(const AdalnParams& p, cudaStream_t stream);
