@@ -43,14 +43,20 @@ DSV_DEVICE float warp_sum(float v) {
   return v;
 }
 
+// Barrier of the W warps that share a row (named barrier 1 + row group; barrier 0 is the
+// CTA-wide one that releases a stage).
+DSV_DEVICE void row_group_sync(int W, int rg) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + rg), "r"(32 * W) : "memory");
+}
+
 // Sum of v over the W warps of this warp's row: a warp shuffle, then (W > 1) the row's W
-// warp totals from shared memory in warp order.  Called by every warp of the CTA the same
-// number of times (it contains a CTA barrier when W > 1).
+// warp totals from shared memory in warp order.  Called by every warp of a row group the same
+// number of times (it contains the row group's barrier when W > 1).
 DSV_DEVICE float row_sum(float v, float* slot, int W, int rg, int warp, int lane) {
   v = warp_sum(v);
   if (W == 1) return v;
   if (lane == 0) slot[warp] = v;
-  __syncthreads();
+  row_group_sync(W, rg);
   float t = 0.f;
   for (int p = 0; p < W; ++p) t += slot[rg * W + p];
   return t;
@@ -89,7 +95,7 @@ DSV_DEVICE float2 row_sum2(float2 v, float2* slot, int W, int rg, int warp, int 
   }
   if (W == 1) return v;
   if (lane == 0) slot[warp] = v;
-  __syncthreads();
+  row_group_sync(W, rg);
   float2 t = make_float2(0.f, 0.f);
   for (int p = 0; p < W; ++p) {
     t.x += slot[rg * W + p].x;
