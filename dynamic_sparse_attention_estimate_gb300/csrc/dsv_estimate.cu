@@ -18,13 +18,16 @@
 //           (ties go to the lower key index).
 // q_hat is held as hi + lo bf16 (an exact split for |q_hat| < 2^16), so with
 // integer-valued factors every fp32 score is the exact integer.
+#include <stdint.h>
+
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 
 namespace dsv {
 namespace {
 
-constexpr int kRows = 16;                       // query blocks per CTA
+constexpr int kRows = 16;                       // query blocks per m16 row tile of the MMA
+constexpr int kMaxRows2 = 27;                   // query blocks per CTA with two row tiles (shared memory)
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileKeys = kWarps * 32;          // keys per CTA-wide tile (32 per warp)
@@ -121,6 +124,25 @@ DSV_DEVICE void scores(const Frags<R>& A, const KeyFrags<R>& f, float (&sc)[4][4
 
 // Visit this warp's key groups in [k_begin, k_end) (32 keys each, tile stride), with the
 // next group's K_lr fragments prefetched while the current one is consumed.
+template <int R, int MT, typename F>
+DSV_DEVICE void for_each_group(const Frags<R> (&A)[MT], const bf16* __restrict__ kh, int N, int k_begin, int k_end,
+                               int warp, int g, int t, F&& body) {
+  int kbase = k_begin + warp * 32;
+  if (kbase >= k_end) return;
+  KeyFrags<R> cur, nxt;
+  load_keys<R>(cur, kh, kbase, N, g, t);
+  for (; kbase < k_end; kbase += kTileKeys) {
+    const int knext = kbase + kTileKeys;
+    if (knext < k_end) load_keys<R>(nxt, kh, knext, N, g, t);
+    float sc[MT][4][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) scores<R>(A[mt], cur, sc[mt]);
+    body(kbase, sc);
+    cur = nxt;
+  }
+}
+
+// One row tile (the mass kernel): sc[j][e] as above.
 template <int R, typename F>
 DSV_DEVICE void for_each_group(const Frags<R>& A, const bf16* __restrict__ kh, int N, int k_begin, int k_end, int warp,
                                int g, int t, F&& body) {
@@ -138,57 +160,64 @@ DSV_DEVICE void for_each_group(const Frags<R>& A, const bf16* __restrict__ kh, i
   }
 }
 
-template <int LEVEL, int R>
-DSV_DEVICE void hist_pass(const Frags<R>& A, const bf16* __restrict__ kh, int N, uint32_t* hist, RowState* rs,
+template <int LEVEL, int R, int MT>
+DSV_DEVICE void hist_pass(const Frags<R> (&A)[MT], const bf16* __restrict__ kh, int N, uint32_t* hist, RowState* rs,
                           int nrows, int warp, int g, int t) {
-  bool act[2];
-  uint32_t pre[2];
-  uint32_t* hrow[2];
+  bool act[MT][2];
+  uint32_t pre[MT][2];
+  uint32_t* hrow[MT][2];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int row = g + 8 * h;
-    act[h] = row < nrows && rs[row].level == LEVEL;
-    pre[h] = rs[row].prefix;
-    hrow[h] = hist + row * kBins;
-  }
-  for_each_group<R>(A, kh, N, 0, N, warp, g, t, [&](int kbase, const float (&sc)[4][4]) {
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = kRows * mt + g + 8 * h;
+      act[mt][h] = row < nrows && rs[row].level == LEVEL;
+      pre[mt][h] = rs[row].prefix;
+      hrow[mt][h] = hist + row * kBins;
+    }
+  for_each_group<R, MT>(A, kh, N, 0, N, warp, g, t, [&](int kbase, const float (&sc)[MT][4][4]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int h = e >> 1;
-        if (!act[h]) continue;
-        const uint32_t key = order_key(sc[j][e]);
+        if (!act[mt][h]) continue;
+        const uint32_t key = order_key(sc[mt][j][e]);
         if (LEVEL == 0) {
-          atomicAdd(hrow[h] + (key >> 21), 1u);
+          atomicAdd(hrow[mt][h] + (key >> 21), 1u);
         } else if (LEVEL == 1) {
-          if ((key >> 21) == pre[h]) {
-            atomicAdd(hrow[h] + ((key >> 10) & 2047u), 1u);
-            if (key & 1023u) atomicOr(&rs[g + 8 * h].orbits, key & 1023u);
+          if ((key >> 21) == pre[mt][h]) {
+            atomicAdd(hrow[mt][h] + ((key >> 10) & 2047u), 1u);
+            if (key & 1023u) atomicOr(&rs[kRows * mt + g + 8 * h].orbits, key & 1023u);
           }
         } else {
-          if ((key >> 10) == pre[h]) atomicAdd(hrow[h] + (key & 1023u), 1u);
+          if ((key >> 10) == pre[mt][h]) atomicAdd(hrow[mt][h] + (key & 1023u), 1u);
         }
       }
     }
   });
 }
 
-template <int R>
+// MT m16 row tiles of the MMA: `rows` query blocks per CTA (<= 16 MT; shared memory holds
+// `rows` histograms), so that the grid can be sized to fill the GPU in whole waves.
+template <int R, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
 estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_lr, int32_t* __restrict__ idx,
-                     int N, int NB, int k, const int32_t* __restrict__ krow, const int64_t* __restrict__ rowptr,
-                     unsigned int* status) {
-  extern __shared__ uint32_t hist[];  // [kRows][kBins]; in the emit phase: gt / eq bitmaps
-  __shared__ float qhat[kRows][R];
-  __shared__ RowState rs[kRows];
+                     int N, int NB, int k, int rows, const int32_t* __restrict__ krow,
+                     const int64_t* __restrict__ rowptr, unsigned int* status) {
+  constexpr int kMax = kRows * MT;
+  extern __shared__ uint32_t hist[];  // [rows][kBins]; in the emit phase: gt / eq bitmaps
+  __shared__ float qhat[kMax][R];
+  __shared__ RowState rs[kMax];
   __shared__ int pending;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int64_t bh = blockIdx.y;
-  const int row0 = blockIdx.x * kRows;
-  const int nrows = NB - row0 < kRows ? NB - row0 : kRows;
+  const int row0 = blockIdx.x * rows;
+  const int nrows = NB - row0 < rows ? NB - row0 : rows;
   const bf16* qh = q_lr + bh * static_cast<int64_t>(N) * R;
   const bf16* kh = k_lr + bh * static_cast<int64_t>(N) * R;
   // per row: its k (krow, or the uniform k) and where its indices go (CSR offsets, or row * k)
@@ -199,7 +228,7 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
   };
 
   // ---- query grouping: q_hat[row] = sum of the block's 64 Q_lr rows (fp32, exact for integers)
-  for (int p = tid; p < kRows * R; p += kThreads) {
+  for (int p = tid; p < kMax * R; p += kThreads) {
     const int row = p / R, c = p % R;
     float acc = 0.f;
     if (row < nrows) {
@@ -208,49 +237,56 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     }
     qhat[row][c] = acc;
   }
-  for (int i = tid; i < kRows * kBins; i += kThreads) hist[i] = 0u;
-  if (tid < kRows) rs[tid] = RowState{0u, 0, tid < nrows ? row_k(tid) : k, 0u, 0, 0u};
+  for (int i = tid; i < rows * kBins; i += kThreads) hist[i] = 0u;
+  if (tid < kMax) rs[tid] = RowState{0u, 0, tid < nrows ? row_k(tid) : k, 0u, 0, 0u};
   __syncthreads();
 
   // ---- A fragments: q_hat = hi + lo (bf16), with the k order permuted so each thread's
   // four k positions {2t, 2t+1, 2t+8, 2t+9} map to the contiguous channels 4t..4t+3.
-  Frags<R> A;
+  Frags<R> A[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
   for (int ks = 0; ks < Frags<R>::KS; ++ks) {
     const int c0 = ks * 16 + 4 * t;
-    const float x[4][2] = {{qhat[g][c0], qhat[g][c0 + 1]}, {qhat[g + 8][c0], qhat[g + 8][c0 + 1]},
-                           {qhat[g][c0 + 2], qhat[g][c0 + 3]}, {qhat[g + 8][c0 + 2], qhat[g + 8][c0 + 3]}};
+    const int r0 = kRows * mt + g, r1 = r0 + 8;
+    const float x[4][2] = {{qhat[r0][c0], qhat[r0][c0 + 1]}, {qhat[r1][c0], qhat[r1][c0 + 1]},
+                           {qhat[r0][c0 + 2], qhat[r0][c0 + 3]}, {qhat[r1][c0 + 2], qhat[r1][c0 + 3]}};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float h0 = __bfloat162float(__float2bfloat16_rn(x[i][0]));
       const float h1 = __bfloat162float(__float2bfloat16_rn(x[i][1]));
-      A.hi[ks][i] = pack_bf16x2(h0, h1);
-      A.lo[ks][i] = pack_bf16x2(x[i][0] - h0, x[i][1] - h1);
+      A[mt].hi[ks][i] = pack_bf16x2(h0, h1);
+      A[mt].lo[ks][i] = pack_bf16x2(x[i][0] - h0, x[i][1] - h1);
     }
   }
 
-  // ---- histogram passes; warp w resolves row w after each
+  // ---- histogram passes; warp w resolves rows w and w + 16 after each
   auto resolve = [&](int level) {
-    if (warp < nrows && rs[warp].level == level) {
-      RowState s = rs[warp];
-      int bin, above, cnt;
-      warp_find_bin(hist + warp * kBins, level == 2 ? 1024 : kBins, s.rem, lane, bin, above, cnt);
-      const int rem = s.rem - above;  // 1 <= rem <= cnt
-      if (level == 0) {
-        if (rem == cnt) { s.T = static_cast<uint32_t>(bin) << 21; s.n_tie = kTieAll; s.level = 3; }
-        else { s.prefix = bin; s.rem = rem; s.level = 1; }
-      } else if (level == 1) {
-        const uint32_t p = (s.prefix << 11) | static_cast<uint32_t>(bin);
-        if (rem == cnt) { s.T = p << 10; s.n_tie = kTieAll; s.level = 3; }
-        else if (s.orbits == 0) { s.T = p << 10; s.n_tie = rem; s.level = 3; }
-        else { s.prefix = p; s.rem = rem; s.level = 2; }
-      } else {
-        s.T = (s.prefix << 10) | static_cast<uint32_t>(bin);
-        s.n_tie = rem;
-        s.level = 3;
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      const int row = warp + kWarps * q;
+      if (row < nrows && rs[row].level == level) {
+        RowState s = rs[row];
+        int bin, above, cnt;
+        warp_find_bin(hist + row * kBins, level == 2 ? 1024 : kBins, s.rem, lane, bin, above, cnt);
+        const int rem = s.rem - above;  // 1 <= rem <= cnt
+        if (level == 0) {
+          if (rem == cnt) { s.T = static_cast<uint32_t>(bin) << 21; s.n_tie = kTieAll; s.level = 3; }
+          else { s.prefix = bin; s.rem = rem; s.level = 1; }
+        } else if (level == 1) {
+          const uint32_t p = (s.prefix << 11) | static_cast<uint32_t>(bin);
+          if (rem == cnt) { s.T = p << 10; s.n_tie = kTieAll; s.level = 3; }
+          else if (s.orbits == 0) { s.T = p << 10; s.n_tie = rem; s.level = 3; }
+          else { s.prefix = p; s.rem = rem; s.level = 2; }
+        } else {
+          s.T = (s.prefix << 10) | static_cast<uint32_t>(bin);
+          s.n_tie = rem;
+          s.level = 3;
+        }
+        __syncwarp();
+        if (lane == 0) rs[row] = s;
       }
-      __syncwarp();
-      if (lane == 0) rs[warp] = s;
     }
   };
   auto next_level_pending = [&](int level) -> bool {
@@ -260,20 +296,20 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     __syncthreads();
     const bool any = pending != 0;
     if (any)
-      for (int i = tid; i < kRows * kBins; i += kThreads) hist[i] = 0u;
+      for (int i = tid; i < rows * kBins; i += kThreads) hist[i] = 0u;
     __syncthreads();
     return any;
   };
 
-  hist_pass<0, R>(A, kh, N, hist, rs, nrows, warp, g, t);
+  hist_pass<0, R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
   __syncthreads();
   resolve(0);
   if (next_level_pending(1)) {
-    hist_pass<1, R>(A, kh, N, hist, rs, nrows, warp, g, t);
+    hist_pass<1, R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
     __syncthreads();
     resolve(1);
     if (next_level_pending(2)) {
-      hist_pass<2, R>(A, kh, N, hist, rs, nrows, warp, g, t);
+      hist_pass<2, R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
       __syncthreads();
       resolve(2);
     }
@@ -281,49 +317,69 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
   __syncthreads();
 
   // ---- emit, one segment of keys at a time
-  uint32_t* gtb = hist;                        // [kRows][kSegWords]
-  uint32_t* eqb = hist + kRows * kSegWords;    // [kRows][kSegWords]
-  const uint32_t T0 = rs[g].T, T1 = rs[g + 8].T;
-  int out_pos = 0, tie_seen = 0;               // row `warp`'s running counts (every lane holds them)
-  const int n_tie = warp < nrows ? rs[warp].n_tie : 0;
+  uint32_t* gtb = hist;                      // [rows][kSegWords]
+  uint32_t* eqb = hist + rows * kSegWords;   // [rows][kSegWords]
+  uint32_t T[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    T[mt][0] = rs[kRows * mt + g].T;
+    T[mt][1] = rs[kRows * mt + g + 8].T;
+  }
+  // rows warp and warp + 16: running counts (every lane holds them)
+  int out_pos[MT], tie_seen[MT], n_tie[MT];
+#pragma unroll
+  for (int q = 0; q < MT; ++q) {
+    const int row = warp + kWarps * q;
+    out_pos[q] = tie_seen[q] = 0;
+    n_tie[q] = row < nrows ? rs[row].n_tie : 0;
+  }
   for (int seg = 0; seg < N; seg += kSegKeys) {
     const int seg_end = seg + kSegKeys < N ? seg + kSegKeys : N;
-    for_each_group<R>(A, kh, N, seg, seg_end, warp, g, t, [&](int kbase, const float (&sc)[4][4]) {
-      uint32_t gtm[2] = {0u, 0u}, eqm[2] = {0u, 0u};
+    for_each_group<R, MT>(A, kh, N, seg, seg_end, warp, g, t, [&](int kbase, const float (&sc)[MT][4][4]) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t gtm[2] = {0u, 0u}, eqm[2] = {0u, 0u};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = e >> 1;
-          const int pos = 8 * j + 2 * t + (e & 1);
-          const uint32_t key = order_key(sc[j][e]);
-          const uint32_t T = h ? T1 : T0;
-          gtm[h] |= static_cast<uint32_t>(key > T) << pos;
-          eqm[h] |= static_cast<uint32_t>(key == T) << pos;
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int h = e >> 1;
+            const int pos = 8 * j + 2 * t + (e & 1);
+            const uint32_t key = order_key(sc[mt][j][e]);
+            gtm[h] |= static_cast<uint32_t>(key > T[mt][h]) << pos;
+            eqm[h] |= static_cast<uint32_t>(key == T[mt][h]) << pos;
+          }
         }
-      }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        gtm[h] |= __shfl_xor_sync(0xffffffffu, gtm[h], 1);
-        gtm[h] |= __shfl_xor_sync(0xffffffffu, gtm[h], 2);
-        eqm[h] |= __shfl_xor_sync(0xffffffffu, eqm[h], 1);
-        eqm[h] |= __shfl_xor_sync(0xffffffffu, eqm[h], 2);
-      }
-      if (t == 0) {
-        const int w = (kbase - seg) >> 5;
-        gtb[g * kSegWords + w] = gtm[0];
-        eqb[g * kSegWords + w] = eqm[0];
-        gtb[(g + 8) * kSegWords + w] = gtm[1];
-        eqb[(g + 8) * kSegWords + w] = eqm[1];
+        for (int h = 0; h < 2; ++h) {
+          gtm[h] |= __shfl_xor_sync(0xffffffffu, gtm[h], 1);
+          gtm[h] |= __shfl_xor_sync(0xffffffffu, gtm[h], 2);
+          eqm[h] |= __shfl_xor_sync(0xffffffffu, eqm[h], 1);
+          eqm[h] |= __shfl_xor_sync(0xffffffffu, eqm[h], 2);
+        }
+        if (t == 0) {
+          const int w = (kbase - seg) >> 5;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = kRows * mt + g + 8 * h;
+            if (row < nrows) {  // the bitmaps hold `rows` rows
+              gtb[row * kSegWords + w] = gtm[h];
+              eqb[row * kSegWords + w] = eqm[h];
+            }
+          }
+        }
       }
     });
     __syncthreads();
-    if (warp < nrows) {
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      const int row = warp + kWarps * q;
+      if (row >= nrows) continue;
       const int nwords = (seg_end - seg) >> 5;
-      const uint32_t* gw = gtb + warp * kSegWords;
-      const uint32_t* ew = eqb + warp * kSegWords;
-      int32_t* orow = row_out(warp);
-      const int kw = row_k(warp);
+      const uint32_t* gw = gtb + row * kSegWords;
+      const uint32_t* ew = eqb + row * kSegWords;
+      int32_t* orow = row_out(row);
+      const int kw = row_k(row);
       for (int w0 = 0; w0 < nwords; w0 += 32) {
         const int w = w0 + lane;
         const uint32_t gv = w < nwords ? gw[w] : 0u;
@@ -336,7 +392,7 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
           const int v = __shfl_up_sync(0xffffffffu, e_incl, o);
           if (lane >= o) e_incl += v;
         }
-        const int avail = n_tie - tie_seen - (e_incl - ne);
+        const int avail = n_tie[q] - tie_seen[q] - (e_incl - ne);
         const int m = avail <= 0 ? 0 : (avail < ne ? avail : ne);
         uint32_t take = ev;
         if (m < ne) {
@@ -356,7 +412,7 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
           const int v = __shfl_up_sync(0xffffffffu, s_incl, o);
           if (lane >= o) s_incl += v;
         }
-        int o = out_pos + s_incl - ns;
+        int o = out_pos[q] + s_incl - ns;
         const int key0 = seg + (w << 5);
         while (sel) {
           const int b = __ffs(sel) - 1;
@@ -365,8 +421,8 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
           else flag_status(status, kStatusBadIndex);
           ++o;
         }
-        out_pos += __shfl_sync(0xffffffffu, s_incl, 31);
-        tie_seen += __shfl_sync(0xffffffffu, e_incl, 31);
+        out_pos[q] += __shfl_sync(0xffffffffu, s_incl, 31);
+        tie_seen[q] += __shfl_sync(0xffffffffu, e_incl, 31);
       }
     }
     __syncthreads();
@@ -728,6 +784,26 @@ cudaError_t launch_mass_r(const MassParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Query blocks per CTA.  One CTA runs per SM and the grid has ceil(NB / rows) CTAs per head.
+// Measured on the short clip (12 heads x 256 blocks, r = 16): a CTA's time hardly depends on its
+// rows (8..16 rows: 103 us a wave; the per-key work -- streaming the head's K_lr, the MMA tile,
+// the compares -- dominates), and a CTA with two row tiles (17..27 rows) takes about 1.75 times
+// as long as one with a single tile.  So: with one tile, the most rows (fewest CTAs, fewest
+// waves); with two tiles, the fewest rows that reach their fewest waves; two tiles only when
+// that saves at least 10 % (waves x 175 against waves x 100), and only when the low-rank dim
+// leaves room in registers.
+int estimate_rows_per_cta(int64_t BH, int64_t NB, bool two_tiles_ok) {
+  constexpr int64_t kSMs = 152;
+  auto waves = [&](int r) { return (BH * ((NB + r - 1) / r) + kSMs - 1) / kSMs; };
+  const int one = NB < kRows ? static_cast<int>(NB < 1 ? 1 : NB) : kRows;
+  if (!two_tiles_ok || NB <= kRows) return one;
+  const int64_t w1 = waves(one);
+  int two = kMaxRows2;
+  for (int r = kMaxRows2; r > kRows; --r)
+    if (waves(r) == waves(kMaxRows2)) two = r;   // the fewest rows with the fewest waves
+  return waves(two) * 175 * 10 <= w1 * 100 * 9 ? two : one;
+}
+
 // k == N: every key of every block, ascending.
 __global__ void arange_kernel(int32_t* __restrict__ idx, int64_t rows, int64_t k) {
   const int64_t total = rows * k;
@@ -736,18 +812,24 @@ __global__ void arange_kernel(int32_t* __restrict__ idx, int64_t rows, int64_t k
     idx[i] = static_cast<int32_t>(i % k);
 }
 
-template <int R>
-cudaError_t launch_r(const EstimateParams& p, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(kRows) * kBins * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(estimate_topk_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int R, int MT>
+cudaError_t launch_rt(const EstimateParams& p, int rows, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(rows) * kBins * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(estimate_topk_kernel<R, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((p.NB + kRows - 1) / kRows), static_cast<unsigned>(p.BH));
+  dim3 grid(static_cast<unsigned>((p.NB + rows - 1) / rows), static_cast<unsigned>(p.BH));
   ProfScope prof("estimate_topk", stream);
-  estimate_topk_kernel<R><<<grid, kThreads, smem, stream>>>(p.q_lr, p.k_lr, p.idx, static_cast<int>(p.N),
-                                                             static_cast<int>(p.NB), static_cast<int>(p.topk), p.krow,
-                                                             p.rowptr, p.status);
+  estimate_topk_kernel<R, MT><<<grid, kThreads, smem, stream>>>(p.q_lr, p.k_lr, p.idx, static_cast<int>(p.N),
+                                                                 static_cast<int>(p.NB), static_cast<int>(p.topk), rows,
+                                                                 p.krow, p.rowptr, p.status);
   return cudaGetLastError();
+}
+
+template <int R>
+cudaError_t launch_r(const EstimateParams& p, cudaStream_t stream) {
+  const int rows = estimate_rows_per_cta(p.BH, p.NB, R <= 32);
+  return rows > kRows ? launch_rt<R, (R <= 32 ? 2 : 1)>(p, rows, stream) : launch_rt<R, 1>(p, rows, stream);
 }
 
 }  // namespace
