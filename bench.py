@@ -73,7 +73,7 @@ def config_of(wl):
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} latent {t}x{h}x{w} -> N={wl.N}, d={wl.d}, r={wl.r}, "
                         f"k={wl.k} ({100 * wl.density:.1f}% density), query blocks of 64",
             "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "r": wl.r, "k": wl.k, "block": 64,
-            "density": round(wl.density, 4), "l2": "512 MiB memset between timed steps (outside the timed events)"}
+            "density": round(wl.density, 4), "l2": "flushed between timed steps (outside the timed events): 512 MiB memset, then a read of another 512 MiB"}
 
 
 def flops_per_step(wl):
@@ -428,15 +428,19 @@ def dsv_arm(args):
                                               out=(dq, dk, dv)), n_stage)
     BH = wl.B * wl.H
 
-    # ---- e2e through the public API with host buffers
+    # ---- e2e through the public API with host buffers: every step copies its inputs host->device
+    # from pinned memory and its outputs (O, LSE, dQ, dK, dV) back.  Measured two ways: serial (copy
+    # in, step, copy out, synchronise) and pipelined (three streams, device inputs and outputs
+    # double-buffered: step i+1's inputs go in and step i-1's outputs come back while step i
+    # computes), which is what a training loop that prefetches its batches sees.
     e2e = None
     if not args.no_e2e:
         pinned = {n: host[n].pin_memory() for n in names}
         outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-        back = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
         h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-        d2h = sum(t.numel() * t.element_size() for t in back.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
         n_e2e = max(3, min(args.steps, 50))
+        back = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
         for i in range(n_e2e + 2):                 # two untimed passes first
             a, b = ev[max(i - 2, 0)]
@@ -450,9 +454,75 @@ def dsv_arm(args):
             if i >= 2:
                 b.record()
             torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev, world)
-        e2e = {"value": job_tflops(world, n_e2e, fl, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / n_e2e, "steps": n_e2e}
+        serial_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev, world) / n_e2e
+
+        slots = []
+        for _ in range(2):
+            gi = {n: torch.empty_like(g[n]) for n in names}
+            go = {n: torch.empty_like(t) for n, t in outs.items()}
+            hb = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+            slots.append((gi, go, hb, torch.empty_like(idx)))
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        in_done = [torch.cuda.Event() for _ in range(2)]
+        cmp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+
+        def pipelined(n_steps, t0=None, t1=None):
+            for i in range(n_steps):
+                si = i % 2
+                gi, go, hb, idx_s = slots[si]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(cmp_done[si])      # step i-2 has consumed this slot's inputs
+                    if i == 0 and t0 is not None:
+                        t0.record(s_in)
+                    for n in names:
+                        gi[n].copy_(pinned[n], non_blocking=True)
+                    in_done[si].record(s_in)
+                with torch.cuda.stream(s_cmp):
+                    s_cmp.wait_event(in_done[si])
+                    if i >= 2:
+                        s_cmp.wait_event(out_done[si])     # step i-2's outputs have left this slot
+                    dsv_estimate_topk(gi["q_lr"], gi["k_lr"], wl.k, idx=idx_s)
+                    dsv_sparse_attn_fwd(gi["q"], gi["k"], gi["v"], idx_s, out=(go["o"], go["lse"]))
+                    dsv_sparse_attn_bwd(gi["do"], gi["q"], gi["k"], gi["v"], go["o"], go["lse"], idx_s, workspace=ws,
+                                        out=(go["dq"], go["dk"], go["dv"]))
+                    cmp_done[si].record(s_cmp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(cmp_done[si])
+                    for n in outs:
+                        hb[n].copy_(go[n], non_blocking=True)
+                    out_done[si].record(s_out)
+            if t1 is not None:
+                with torch.cuda.stream(s_out):
+                    t1.record(s_out)
+            torch.cuda.synchronize()
+
+        # the copies alone (every step's H2D then D2H, no compute), to show what the pipeline hides
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        c0.record()
+        for i in range(n_e2e):
+            gi, go, hb, _ = slots[i % 2]
+            for n in names:
+                gi[n].copy_(pinned[n], non_blocking=True)
+            for n in outs:
+                hb[n].copy_(go[n], non_blocking=True)
+        c1.record()
+        torch.cuda.synchronize()
+        copy_ms = max_over_ranks(c0.elapsed_time(c1), dev, world) / n_e2e
+
+        pipelined(2)                                # untimed
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # the start event waits for nothing queued before it: every stream is idle here
+        pipelined(n_e2e, t0, t1)
+        pipe_ms = max_over_ranks(t0.elapsed_time(t1), dev, world) / n_e2e
+        e2e = {"value": job_tflops(world, n_e2e, fl, pipe_ms * n_e2e), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms, "steps": n_e2e,
+               "pipelined": "3 streams; device inputs and outputs double-buffered; step i+1's H2D and step i-1's "
+                            "D2H overlap step i",
+               "copies_alone_ms_per_step": copy_ms,
+               "serial": {"value": job_tflops(world, n_e2e, fl, serial_ms * n_e2e), "ms_per_step": serial_ms}}
 
     # ---- dense comparator (PyTorch SDPA fwd+bwd on the same shape)
     dense = None
