@@ -265,7 +265,11 @@ dsv_status dsv_adaln_fwd(const dsv_adaln_dims* dims, const void* x, const void* 
                          void* y, void* stream);
 /* Bytes of workspace dsv_adaln_bwd needs (per-tile partial sums of the modulation gradients). */
 size_t dsv_adaln_bwd_workspace(const dsv_adaln_dims* dims);
-/* ws: at least dsv_adaln_bwd_workspace(dims) bytes, 256-byte aligned (DSV_ERR_WORKSPACE otherwise). */
+/* ws: at least dsv_adaln_bwd_workspace(dims) bytes, 256-byte aligned (DSV_ERR_WORKSPACE otherwise).
+ * It holds per-tile partial sums and the tickets that order their final sum, so one workspace
+ * must not serve two backward calls that can run at the same time (other streams); calls in
+ * order on one stream may share it.  The call runs two kernels, the second launched as a
+ * programmatic dependent of the first (it waits for the first to finish before reading). */
 dsv_status dsv_adaln_bwd(const dsv_adaln_dims* dims, const void* x, const void* scale, const void* dy, void* dx,
                          float* d_scale, float* d_shift, void* ws, size_t ws_bytes, void* stream);
 
