@@ -17,6 +17,8 @@ from .binding import (  # noqa: F401
     dsv_estimate_topk_workspace,
     dsv_sparse_attn_bwd,
     dsv_sparse_attn_bwd_csr,
+    dsv_sparse_attn_bwd_prepare,
+    dsv_sparse_attn_bwd_prepared,
     dsv_sparse_attn_bwd_workspace,
     dsv_sparse_attn_fwd,
     dsv_sparse_attn_fwd_csr,

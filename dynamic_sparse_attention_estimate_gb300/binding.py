@@ -29,6 +29,7 @@ EXPORTED = (
     "dsv_estimate_mass_k", "dsv_estimate_topk_csr", "dsv_sparse_attn_fwd_csr",
     "dsv_sparse_attn_bwd_csr_workspace", "dsv_sparse_attn_bwd_csr", "dsv_csr_launch_order",
     "dsv_adaln_fwd", "dsv_adaln_bwd_workspace", "dsv_adaln_bwd",
+    "dsv_sparse_attn_bwd_prepare", "dsv_sparse_attn_bwd_prepared",
 )
 
 
@@ -96,6 +97,10 @@ def load_library(path: Optional[str] = None):
     lib.dsv_sparse_attn_bwd_csr.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp, vp, vp, sz,
                                             vp]
     lib.dsv_sparse_attn_bwd_csr.restype = st
+    lib.dsv_sparse_attn_bwd_prepare.argtypes = [dp, vp, vp, sz, vp]
+    lib.dsv_sparse_attn_bwd_prepare.restype = st
+    lib.dsv_sparse_attn_bwd_prepared.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.dsv_sparse_attn_bwd_prepared.restype = st
     ap = ctypes.POINTER(AdalnDims)
     lib.dsv_adaln_fwd.argtypes = [ap, vp, vp, vp, vp, vp]
     lib.dsv_adaln_fwd.restype = st
@@ -266,6 +271,40 @@ def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: t
     _check(lib.dsv_sparse_attn_bwd(ctypes.byref(dims), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                    _ptr(idx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
                                    _stream_ptr(q)), "dsv_sparse_attn_bwd")
+    return dq, dk, dv
+
+
+def dsv_sparse_attn_bwd_prepare(idx: torch.Tensor, d: int, workspace: torch.Tensor, block: int = 64) -> None:
+    """First half of a split backward: the key-major rank structure of idx, written into `workspace`
+    (which must hold every head in one wave: dsv_sparse_attn_bwd_workspace).  Reads idx only, so it
+    may run on another stream beside the forward; order dsv_sparse_attn_bwd_prepared after it."""
+    _need(idx, "idx", torch.int32, 4)
+    B, H, NB, kk = idx.shape
+    dims = make_dims(B, H, NB * block, d, 0, kk, block)
+    _check(load_library().dsv_sparse_attn_bwd_prepare(ctypes.byref(dims), _ptr(idx), _ptr(workspace),
+                                                      workspace.numel(), _stream_ptr(idx)),
+           "dsv_sparse_attn_bwd_prepare")
+
+
+def dsv_sparse_attn_bwd_prepared(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                 o: torch.Tensor, lse: torch.Tensor, idx: torch.Tensor, workspace: torch.Tensor,
+                                 block: int = 64, scale: Optional[float] = None, out=None):
+    """Second half of a split backward, on the workspace dsv_sparse_attn_bwd_prepare filled: the same
+    (dQ, dK, dV) as dsv_sparse_attn_bwd, bit for bit."""
+    for t, n in ((do, "do"), (q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    _need(idx, "idx", torch.int32, 4)
+    B, H, N, d = q.shape
+    dims = make_dims(B, H, N, d, 0, idx.shape[3], block, scale)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    _check(load_library().dsv_sparse_attn_bwd_prepared(ctypes.byref(dims), _ptr(do), _ptr(q), _ptr(k), _ptr(v),
+                                                       _ptr(o), _ptr(lse), _ptr(idx), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                       _ptr(workspace), workspace.numel(), _stream_ptr(q)),
+           "dsv_sparse_attn_bwd_prepared")
     return dq, dk, dv
 
 

@@ -365,22 +365,26 @@ size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims) {
 
 // rowptr == nullptr: k keys per block, waves planned from the workspace; otherwise CSR rows
 // with total_pairs keys in all, one wave over every head (the workspace must hold it).
+// parts: dsv::kBwdAll, or one of the two halves of a split backward (kBwdPrep reads idx only;
+// kBwdFinish expects the workspace a kBwdPrep call filled); the halves need a single wave.
 dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const void* k, const void* v,
                     const void* o, const float* lse, const int32_t* idx, const int64_t* rowptr,
                     const int32_t* order, int64_t total_pairs, void* dq, void* dk, void* dv, void* ws,
-                    size_t ws_bytes, void* stream) {
+                    size_t ws_bytes, void* stream, int parts = dsv::kBwdAll) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
-  DSV_NEED_PTR(d_o);
-  DSV_NEED_PTR(q);
-  DSV_NEED_PTR(k);
-  DSV_NEED_PTR(v);
-  DSV_NEED_PTR(o);
-  DSV_NEED_PTR(lse);
   DSV_NEED_PTR(idx);
-  DSV_NEED_PTR(dq);
-  DSV_NEED_PTR(dk);
-  DSV_NEED_PTR(dv);
+  if (parts & dsv::kBwdFinish) {
+    DSV_NEED_PTR(d_o);
+    DSV_NEED_PTR(q);
+    DSV_NEED_PTR(k);
+    DSV_NEED_PTR(v);
+    DSV_NEED_PTR(o);
+    DSV_NEED_PTR(lse);
+    DSV_NEED_PTR(dq);
+    DSV_NEED_PTR(dk);
+    DSV_NEED_PTR(dv);
+  }
   if (!ws) return fail(DSV_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   WavePlan plan;
@@ -393,6 +397,9 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
     return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the minimum %zu", ws_bytes,
                 dsv_sparse_attn_bwd_workspace_min(dims));
   }
+  if (parts != dsv::kBwdAll && (plan.sub || plan.nh < dims->B * dims->H))
+    return fail(DSV_ERR_WORKSPACE, "a split backward needs a workspace that holds every head in one wave "
+                "(dsv_sparse_attn_bwd_workspace)");
   unsigned int* status = nullptr;
   if ((s = status_word(&status)) != DSV_OK) return s;
 
@@ -431,7 +438,7 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
   if (!plan.sub) {
     for (int64_t bh0 = 0; bh0 < p.BH; bh0 += plan.nh) {
       dsv::BwdWave w{bh0, plan.nh < p.BH - bh0 ? plan.nh : p.BH - bh0, 0, p.NB, true, true};
-      cudaError_t e = dsv::launch_bwd_wave(p, w, st);
+      cudaError_t e = dsv::launch_bwd_wave(p, w, st, parts);
       if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
     }
   } else {
@@ -451,6 +458,19 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
                                const void* o, const float* lse, const int32_t* idx, void* dq, void* dk, void* dv,
                                void* ws, size_t ws_bytes, void* stream) {
   return bwd_impl(dims, d_o, q, k, v, o, lse, idx, nullptr, nullptr, 0, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+dsv_status dsv_sparse_attn_bwd_prepare(const dsv_dims* dims, const int32_t* idx, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  return bwd_impl(dims, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, idx, nullptr, nullptr, 0, nullptr,
+                  nullptr, nullptr, ws, ws_bytes, stream, dsv::kBwdPrep);
+}
+
+dsv_status dsv_sparse_attn_bwd_prepared(const dsv_dims* dims, const void* d_o, const void* q, const void* k,
+                                        const void* v, const void* o, const float* lse, const int32_t* idx, void* dq,
+                                        void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(dims, d_o, q, k, v, o, lse, idx, nullptr, nullptr, 0, dq, dk, dv, ws, ws_bytes, stream,
+                  dsv::kBwdFinish);
 }
 
 size_t dsv_sparse_attn_bwd_csr_workspace(const dsv_dims* dims, int64_t total_pairs) {

@@ -276,8 +276,9 @@ inline unsigned grid_for(int64_t work, int threads, int64_t cap = 152 * 16) {
   return static_cast<unsigned>(b);
 }
 
-template <int D>
-cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t stream) {
+// Steps 1-3 (the key-major rank structure): they read only idx (and rowptr), so they may run
+// as soon as the selection exists, e.g. beside the forward on another stream.
+cudaError_t launch_wave_prep(const BwdParams& p, const BwdWave& w, cudaStream_t stream) {
   const int64_t W32 = (w.nblk + 31) / 32;
   const int64_t N = p.N;
   const int64_t ntile = (N + kBitsTile - 1) / kBitsTile;
@@ -299,8 +300,15 @@ cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t str
     scan_kernel<<<dim3(static_cast<unsigned>(nscan), nh), kScanThreads, 0, stream>>>(
         p.count, p.tsum, p.offsets, N, w.nblk * p.topk, p.rowptr, p.NB, w.bh0, w.blk0, hs0); }
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
+// Steps 4-5 on a prepared workspace.
+template <int D>
+cudaError_t launch_wave_finish(const BwdParams& p, const BwdWave& w, cudaStream_t stream) {
+  const int64_t W32 = (w.nblk + 31) / 32;
+  const int64_t N = p.N;
+  cudaError_t e;
   if ((e = launch_bwd_main_tc(p, w, W32, stream)) != cudaSuccess) return e;
 
   int mode = 0;
@@ -312,12 +320,12 @@ cudaError_t launch_wave_d(const BwdParams& p, const BwdWave& w, cudaStream_t str
 
 }  // namespace
 
-cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream) {
-  switch (p.d) {
-    case 64: return launch_wave_d<64>(p, w, stream);
-    case 128: return launch_wave_d<128>(p, w, stream);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream, int parts) {
+  if (p.d != 64 && p.d != 128) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((parts & kBwdPrep) && (e = launch_wave_prep(p, w, stream)) != cudaSuccess) return e;
+  if (parts & kBwdFinish) return p.d == 64 ? launch_wave_finish<64>(p, w, stream) : launch_wave_finish<128>(p, w, stream);
+  return cudaSuccess;
 }
 
 }  // namespace dsv

@@ -99,7 +99,10 @@ struct BwdParams {
                        //                16-byte chunks of row n are stored XOR (n & 7)
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
 };
-cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream);
+// parts: kBwdPrep (bitmaps, prefix, scan: reads idx only), kBwdFinish (main kernel and reduce on
+// a workspace the prep filled), or both
+constexpr int kBwdPrep = 1, kBwdFinish = 2, kBwdAll = 3;
+cudaError_t launch_bwd_wave(const BwdParams& p, const BwdWave& w, cudaStream_t stream, int parts = kBwdAll);
 
 // ---------------------------------------------------------------- fused AdaLN (adaln.cu)
 struct AdalnParams {

@@ -163,6 +163,25 @@ dsv_status dsv_sparse_attn_bwd(const dsv_dims* dims, const void* d_o, const void
                                void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The backward in two calls, so that its first part can run beside the forward.  The first part
+ * (dsv_sparse_attn_bwd_prepare) builds the backward's key-major rank structure of idx in the
+ * workspace -- which query blocks selected each key, and where each key's partial rows go -- and
+ * reads nothing but idx; the second (dsv_sparse_attn_bwd_prepared) runs the rest of
+ * dsv_sparse_attn_bwd on that workspace and gives bitwise the same dQ, dK, dV.  A training step
+ * can call prepare on a second stream as soon as idx exists, after the forward is enqueued, so
+ * that it fills the SMs the forward leaves idle, and order prepared after it with an event.
+ *   - Both calls take the same dims, idx, ws and ws_bytes; ws must hold every head in one wave
+ *     (dsv_sparse_attn_bwd_workspace(dims) does when it fits; otherwise DSV_ERR_WORKSPACE).
+ *   - prepared must run after prepare has finished (same stream, or an event), and nothing may
+ *     write the workspace in between.  Arguments as dsv_sparse_attn_bwd.
+ */
+dsv_status dsv_sparse_attn_bwd_prepare(const dsv_dims* dims, const int32_t* idx, void* ws, size_t ws_bytes,
+                                       void* stream);
+dsv_status dsv_sparse_attn_bwd_prepared(const dsv_dims* dims, const void* d_o, const void* q, const void* k,
+                                        const void* v, const void* o, const float* lse, const int32_t* idx, void* dq,
+                                        void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Backward without a caller workspace.  Some callers cannot allocate device memory
  * themselves: a host framework that owns every byte of the GPU through its own pool and
  * forbids outside allocations during a step, a plug-in whose memory budget is fixed when

@@ -119,3 +119,14 @@ def test_adaln_arguments_rejected_before_launch(lib):
     assert lib.dsv_adaln_bwd(*args, None, 0, None) == 3
     assert lib.dsv_adaln_bwd(*args, p, need - 256, None) == 3
     assert lib.dsv_adaln_bwd(*args, ctypes.c_void_p(0x1010), need, None) == 3
+
+
+def test_split_backward_needs_a_single_wave_workspace(lib):
+    dims = make_dims(1, 12, 16384, 64, 16, 1638)
+    p = ctypes.c_void_p(0x1000)
+    mn = lib.dsv_sparse_attn_bwd_workspace_min(ctypes.byref(dims))
+    assert lib.dsv_sparse_attn_bwd_prepare(ctypes.byref(dims), p, p, mn, None) == 3      # several waves
+    assert b"one wave" in lib.dsv_last_error_message()
+    assert lib.dsv_sparse_attn_bwd_prepare(ctypes.byref(dims), None, p, mn, None) == 1   # no idx
+    args = [ctypes.byref(dims)] + [p] * 10
+    assert lib.dsv_sparse_attn_bwd_prepared(*args, p, mn, None) == 3
