@@ -2,22 +2,25 @@
 // summary section 2B).  y = (x - mean) * rstd * (1 + scale[b]) + shift[b] per token, with
 // mean and the biased variance over the D features and rstd = 1 / sqrt(var + eps).
 //
-// The row means are correctly rounded divisions by D (exact for a constant row, whose
-// normalised row is then exactly 0 and whose output is exactly the shift).
+// The row mean is sum * (1/D) corrected once by its exact FMA residual, which makes it exact for
+// a constant row (whose normalised row is then exactly 0 and whose output is exactly the shift).
 //
-// Layout: a 256-thread CTA owns a tile of consecutive tokens of one sample.  A token's D
-// features are D / 8 16-byte vectors spread over W warps (W = 1 while D <= 1024, up to 8 at
-// D = 8192); the CTA's 8 warps form 8 / W row groups that take the tile's tokens in turn.  A
-// row is read from HBM once and kept in registers for the three passes (mean, variance,
-// output); the reductions are warp shuffles plus, when W > 1, a shared-memory level across the
-// row's warps.
+// Layout: a 256-thread CTA owns a tile of consecutive tokens of one sample.  The tile is
+// contiguous in HBM and streams through shared-memory stages filled by bulk copies of the tensor
+// memory accelerator (mbarrier completion, bounded waits).  A token's D features are D / 8
+// 16-byte vectors spread over W warps (W = 1 while D <= 1024, up to 8 at D = 8192); the CTA's 8
+// warps form 8 / W row groups that take the stage's tokens in turn (two at a time in the
+// forward).  A token is read from shared memory once into registers for its passes (mean,
+// variance, output); the reductions are warp shuffles plus, when W > 1, a shared-memory level
+// across the row's warps behind a named barrier of that row group.  Elementwise arithmetic runs
+// on packed fp32 pairs; the modulation is held as fp32 in shared memory.
 //
 // Backward: the statistics are recomputed from x (nothing is saved between the passes).  Per
 // token dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) with g = dy * (1 + scale); the
 // modulation gradients d_scale = sum_n dy * xhat and d_shift = sum_n dy are accumulated per
 // feature in registers by the lanes that own that feature over the CTA's tile (the (D tile,
 // N tile) blocking: loads stay coalesced along D), reduced across the row groups in a fixed
-// order, and written as one partial row per tile; a second kernel sums the tiles in tile
+// order, and written as one partial row per tile; a second kernel sums the tiles in a fixed
 // order.  No float atomics: the results are bitwise reproducible.
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
