@@ -155,8 +155,7 @@ def reference_arm(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(wl),
-        "step": "estimate; forward; the backward's rank structure of idx on a second stream beside the forward; "
-                "the rest of the backward",
+            "step": "estimate, forward and backward of sampled query blocks by the fp64 oracle on the host cores",
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"{blocks} query blocks of head 0 (estimate + forward + backward), "
                                        f"~{per_step:.2f} s per step, numpy fp64"},
