@@ -89,6 +89,17 @@ def test_mass_selection_short_clip_two_heads():
         _check_head(x, 0, h, k_row, rowptr, cols, 1 / 64, 0.9)
 
 
+def test_mass_selection_short_clip_every_head():
+    """All 12 heads at once: the CSR top-k runs 22 query blocks per CTA on two m16 row tiles."""
+    need_gpu()
+    wl = WORKLOADS["short"]
+    x = make_inputs(wl)
+    g = {k: v.cuda() for k, v in x.items()}
+    k_row, rowptr, cols = _select(g, 1 / 64, 0.9)
+    for h in range(wl.H):
+        _check_head(x, 0, h, k_row, rowptr, cols, 1 / 64, 0.9)
+
+
 def _abs_contributions(c, lists, blocks):
     """Per key, the sum over blocks of |that block's contribution| to dK and dV: each block's
     contribution is one bf16 partial row, rounded once, so the rounding scales with these."""

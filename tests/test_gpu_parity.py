@@ -114,6 +114,22 @@ def test_short_clip_selection_every_head_bit_exact():
         assert np.array_equal(idx[0, h].cpu().numpy(), want), f"head {h}"
 
 
+def test_short_clip_selection_r32_two_row_tiles():
+    """12 heads x 256 query blocks with r = 32: the estimate runs 22 query blocks per CTA on two m16
+    row tiles (one wave over the SMs); every head's selection equals the oracle's."""
+    import dataclasses
+    dev = need_gpu()
+    wl = dataclasses.replace(WORKLOADS["short"], r=32)
+    x = make_inputs(wl)
+    g = _to(dev, x)
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    torch.cuda.synchronize()
+    check_idx_invariants(idx, wl.N)
+    for h in range(wl.H):
+        want = oracle.estimate_topk(x["q_lr"][0, h], x["k_lr"][0, h], 64, wl.k)
+        assert np.array_equal(idx[0, h].cpu().numpy(), want), f"head {h}"
+
+
 def test_short_clip_attention():
     dev = need_gpu()
     wl = WORKLOADS["short"]
