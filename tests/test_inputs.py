@@ -66,3 +66,20 @@ def test_k_from_density_is_floor():
 def test_sample_blocks_sorted_distinct():
     s = sample_blocks(8128, 64)
     assert s.size == 64 and np.all(np.diff(s) > 0) and s.max() < 8128
+
+
+def test_adaln_draws_are_seeded_shaped_and_spread_per_token():
+    from dynamic_sparse_attention_estimate_gb300.inputs import ADALN_WORKLOADS, make_adaln_inputs
+    a, b = make_adaln_inputs(2, 300, 64), make_adaln_inputs(2, 300, 64)
+    for n in ("x", "scale", "shift", "dy"):
+        assert a[n].dtype == torch.bfloat16 and a[n].is_contiguous()
+        assert torch.equal(a[n], b[n])                        # same seed, same draws
+    assert a["x"].shape == a["dy"].shape == (2, 300, 64) and a["scale"].shape == a["shift"].shape == (2, 64)
+    assert not torch.equal(make_adaln_inputs(2, 300, 64, seed=1)["x"], a["x"])
+    # tokens differ in mean and spread (offset N(0,1), spread U(0.5, 3)), as hidden states do
+    x = a["x"].float()
+    sd = x.std(dim=-1)
+    assert float(sd.min()) > 0.3 and float(sd.max()) < 4.0 and float(sd.max() / sd.min()) > 2.0
+    assert float(x.mean(dim=-1).std()) > 0.5
+    assert set(ADALN_WORKLOADS) == {"short", "wide"}
+    assert all(D % 8 == 0 for (_, _, D) in ADALN_WORKLOADS.values())
