@@ -181,7 +181,7 @@ DSV_DEVICE void row_stats_pair(const uint4 (&ra)[VPL], const uint4 (&rb)[VPL], c
 // rows each, filled by bulk copies that complete on one mbarrier per stage.  Thread 0 issues the
 // copies; after every warp has finished a stage (a CTA barrier) it refills that stage with the
 // chunk NS ahead.  Waits are bounded: a copy that never lands sets the timeout status bit and
-// the CTA winds down without storing.
+// the CTA winds down without storing, after a second bounded wait for its copies in flight.
 DSV_DEVICE void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
@@ -220,7 +220,9 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
+  int issued = 0, waited = 0;   // chunks issued (thread 0) and chunks whose copy this thread saw land
   auto issue = [&](int c) {
+    issued = c + 1;
     const int s = c % st.NS;
     const int64_t rs = r0 + static_cast<int64_t>(c) * st.R;
     const int64_t nr = r1 - rs < st.R ? r1 - rs : st.R;
@@ -256,6 +258,7 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
   for (int c = 0; c < nchunk; ++c) {
     const int s = c % st.NS;
     if (ok) ok = tc::mbar_wait(smem_u32(&full[s]), (c / st.NS) & 1);
+    if (ok) waited = c + 1;
     const uint4* stage = sbuf + s * stage_vecs;
     const int64_t rs = r0 + static_cast<int64_t>(c) * st.R;
     // two tokens per warp: local rows lr and lr + RG of the stage (the same trip count for every
@@ -300,6 +303,10 @@ adaln_fwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
     if (tid == 0 && ok && c + st.NS < nchunk) issue(c + st.NS);
   }
   if (!ok && lane == 0) flag_status(status, kStatusTimeout);
+  // error path: before this CTA's shared memory can go away, wait (again bounded) for the copies
+  // thread 0 issued that nobody saw land
+  if (!ok && tid == 0)
+    for (int cc = waited; cc < issued; ++cc) tc::mbar_wait(smem_u32(&full[cc % st.NS]), (cc / st.NS) & 1);
 }
 
 // ---------------------------------------------------------------- backward: dx + per-tile partials
@@ -329,7 +336,9 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
+  int issued = 0, waited = 0;   // chunks issued (thread 0) and chunks whose copy this thread saw land
   auto issue = [&](int c) {
+    issued = c + 1;
     const int s = c % st.NS;
     const int64_t rs = r0 + static_cast<int64_t>(c) * st.R;
     const int64_t nr = r1 - rs < st.R ? r1 - rs : st.R;
@@ -372,6 +381,7 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
   for (int c = 0; c < nchunk; ++c) {
     const int s = c % st.NS;
     if (ok) ok = tc::mbar_wait(smem_u32(&full[s]), (c / st.NS) & 1);
+    if (ok) waited = c + 1;
     const uint4* sx = sbuf + (2 * s) * half_vecs;
     const uint4* sd = sbuf + (2 * s + 1) * half_vecs;
     const int64_t rs = r0 + static_cast<int64_t>(c) * st.R;
@@ -431,6 +441,10 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
     if (tid == 0 && ok && c + st.NS < nchunk) issue(c + st.NS);
   }
   if (!ok && lane == 0) flag_status(status, kStatusTimeout);
+  // error path: before this CTA's shared memory can go away, wait (again bounded) for the copies
+  // thread 0 issued that nobody saw land
+  if (!ok && tid == 0)
+    for (int cc = waited; cc < issued; ++cc) tc::mbar_wait(smem_u32(&full[cc % st.NS]), (cc / st.NS) & 1);
 
   // row groups' partials -> shared memory (the stages are free: every copy has landed and every
   // warp passed the last barrier) -> one fixed-order sum per feature
