@@ -441,10 +441,16 @@ adaln_bwd_kernel(const uint4* __restrict__ x, const uint4* __restrict__ scale, c
     if (tid == 0 && ok && c + st.NS < nchunk) issue(c + st.NS);
   }
   if (!ok && lane == 0) flag_status(status, kStatusTimeout);
-  // error path: before this CTA's shared memory can go away, wait (again bounded) for the copies
-  // thread 0 issued that nobody saw land
-  if (!ok && tid == 0)
-    for (int cc = waited; cc < issued; ++cc) tc::mbar_wait(smem_u32(&full[cc % st.NS]), (cc / st.NS) & 1);
+  // Error path (any thread of the CTA gave up on a stage): the tile's results are invalid and
+  // the status word says so.  Thread 0 waits (again bounded) for the copies it issued that it
+  // has not seen land, so that none can still write into the stages; then the CTA leaves
+  // without reusing the stages for the partial sums (shared memory lives until its last thread
+  // exits).
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0)
+      for (int cc = waited; cc < issued; ++cc) tc::mbar_wait(smem_u32(&full[cc % st.NS]), (cc / st.NS) & 1);
+    return;
+  }
 
   // row groups' partials -> shared memory (the stages are free: every copy has landed and every
   // warp passed the last barrier) -> one fixed-order sum per feature

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <map>
 #include <string>
 #include <vector>
@@ -36,20 +37,24 @@ dsv_status ok() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int kMaxDevices = 64;
-unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
+// Per-device address of g_dsv_status, looked up on first use with that device current (host
+// threads racing on the first look-up all find the same address).
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
 
 dsv_status status_word(unsigned int** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(DSV_ERR_CUDA, "device ordinal %d out of range", dev);
-  if (!g_status_ptr[dev]) {
+  unsigned int* ptr = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_dsv_status);
     if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    ptr = static_cast<unsigned int*>(p);
+    g_status_ptr[dev].store(ptr, std::memory_order_release);
   }
-  *out = g_status_ptr[dev];
+  *out = ptr;
   return DSV_OK;
 }
 
@@ -631,7 +636,10 @@ dsv_status dsv_adaln_bwd(const dsv_adaln_dims* dims, const void* x, const void* 
 
 namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DSV_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_ptr[kMaxDevices] = {nullptr};   // per-device address of g_noalloc_scratch
+// Per-device address of g_noalloc_scratch, looked up once per device.  Several host threads may
+// race on the first look-up; they all find the same address, and the atomic makes the store and
+// the loads well defined.
+std::atomic<void*> g_noalloc_ptr[kMaxDevices];
 }  // namespace
 
 extern "C" {
@@ -651,16 +659,18 @@ dsv_status dsv_sparse_attn_bwd_noalloc(const dsv_dims* dims, const void* d_o, co
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(DSV_ERR_CUDA, "device ordinal %d out of range", dev);
-  if (!g_noalloc_ptr[dev]) {  // set-up, once per device, with that device current
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  void* scratch = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!scratch) {  // set-up, once per device, with that device current
+    e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
     if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = p;
+    g_noalloc_ptr[dev].store(scratch, std::memory_order_release);
   }
-  // The backward clears its bitmaps at the start of every wave and writes every other
-  // scratch region before reading it, so what an earlier call left behind is never used.
-  return dsv_sparse_attn_bwd(dims, d_o, q, k, v, o, lse, idx, dq, dk, dv, g_noalloc_ptr[dev],
-                             DSV_NOALLOC_SCRATCH_BYTES, stream);
+  // Every word of the scratch that the backward reads in a wave is written earlier in the same
+  // wave (the bitmap kernel writes all of its words, zeros included; the scans, lists, partial
+  // rows and the accumulator are written before they are read), so what an earlier call left
+  // there is never used and nothing needs clearing.
+  return dsv_sparse_attn_bwd(dims, d_o, q, k, v, o, lse, idx, dq, dk, dv, scratch, DSV_NOALLOC_SCRATCH_BYTES,
+                             stream);
 }
 
 }  // extern "C"

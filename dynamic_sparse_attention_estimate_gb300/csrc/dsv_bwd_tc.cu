@@ -68,6 +68,7 @@ struct Bars {
   uint64_t dvk_full[2], dvk_empty[2];  // per buffer: dV_c, dK_c in TMEM ready / read
   uint64_t dq_full;                // last dQ^T update done
   uint64_t st_full[2], st_empty[2];  // per staging buffer: rows written / copied out (d = 64)
+  uint64_t drain;                  // MMA commit at the end: every MMA issued is done
 };
 
 DSV_DEVICE void sync_group(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
@@ -178,6 +179,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::mbar_init(bar(bars.dvk_empty[s]), 128);
     }
     tc::mbar_init(bar(bars.dq_full), 1);
+    tc::mbar_init(bar(bars.drain), 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(bars.st_full[s]), 128);
       tc::mbar_init(bar(bars.st_empty[s]), 1);
@@ -330,6 +332,10 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         issue_grads(c);
       }
       if (!ok_run) atomicOr(&fail_s, 1);
+      // Every MMA issued here must be done before the CTA frees its tensor and shared memory,
+      // also when a wait gave up with MMAs still in flight: one more commit tracks them all.
+      tc::mma_commit(bar(bars.drain));
+      if (!tc::mbar_wait(bar(bars.drain), 0, kWaitLimit)) atomicOr(&fail_s, 1);
     }
   } else if (warp < 8) {
     // ================================================================ P and dS (threads 0..255)

@@ -65,6 +65,7 @@ struct Bars {
   uint64_t p_full[2];       // softmax: P^T tile b written
   uint64_t pv_done[2];      // MMA commit: PV with P^T tile b done
   uint64_t o_full;          // MMA commit: last PV done
+  uint64_t drain;           // MMA commit at the end: every MMA the issuing thread started is done
 };
 
 DSV_DEVICE void named_sync_softmax() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
@@ -194,6 +195,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       tc::mbar_init(bar(bars.pv_done[b]), 1);
     }
     tc::mbar_init(bar(bars.o_full), 1);
+    tc::mbar_init(bar(bars.drain), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     flag_s[0] = flag_s[1] = 0;
     fail_s = 0;
@@ -315,6 +317,11 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         }
       }
       if (!ok_run) atomicOr(&fail_s, 1);
+      // Before the CTA frees its tensor memory and shared memory, every MMA issued here must
+      // have finished, also after a wait gave up with MMAs still in flight: one more commit
+      // tracks all of them.
+      tc::mma_commit(bar(bars.drain));
+      if (!tc::mbar_wait(bar(bars.drain), 0, kWaitLimit)) atomicOr(&fail_s, 1);
     }
   } else {
     // ================================================================ softmax (threads 0..127)

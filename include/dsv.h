@@ -192,7 +192,12 @@ dsv_status dsv_sparse_attn_bwd_prepared(const dsv_dims* dims, const void* d_o, c
  * nothing.  (The DSV pages have no counterpart: this is a deployment convenience.)
  *   - Problems whose smallest backward workspace (dsv_sparse_attn_bwd_workspace_min) is
  *     above DSV_NOALLOC_SCRATCH_BYTES are rejected with DSV_ERR_WORKSPACE before anything
- *     runs; larger problems that fit are processed in several waves.
+ *     runs; larger problems that fit are processed in several waves.  The smallest plan takes
+ *     one query block per wave and chains a head's waves through an fp32 accumulator of
+ *     8 d N bytes, next to k bf16 partial rows of 4 d bytes, so at d = 128 and k = N the limit
+ *     is about N = 21,000 tokens per head (about N = 43,000 at d = 64); a head whose partial
+ *     rows all fit (N/64 * k * 4 d bytes plus its rank structure) needs no accumulator.  The
+ *     long-video shape (N = 520,192) is rejected: use dsv_sparse_attn_bwd there.
  *   - The first call on a device looks up that device's address of the array (with the
  *     device current); make that first call before any stream capture.
  *   - All calls share the one array, which keeps whatever the last call left there (every

@@ -18,7 +18,7 @@ from dynamic_sparse_attention_estimate_gb300 import dsv_estimate_topk, dsv_spars
 from dynamic_sparse_attention_estimate_gb300.binding import dsv_last_device_status, load_library, make_dims
 from dynamic_sparse_attention_estimate_gb300.inputs import WORKLOADS, Workload, make_inputs
 
-from gpu_helpers import assert_close, need_gpu
+from gpu_helpers import need_gpu
 
 
 def _noalloc(lib, dims, g, o, lse, idx, out):
@@ -46,16 +46,8 @@ def test_noalloc_backward_matches_the_workspace_backward_on_two_calls(wl):
         assert status == 0, lib.dsv_last_error_message()
         torch.cuda.synchronize()
         assert dsv_last_device_status() == 0
+        # the backward gives bitwise the same gradients whatever its wave plan, so the outputs
+        # must be equal, not just close
         for name, got, want in zip(("dQ", "dK", "dV"), out, ref):
-            assert_close(f"{name} (call {call + 1})", got, want.float().cpu().numpy())
+            assert torch.equal(got, want), f"{name} (call {call + 1}) differs from the workspace backward"
 
-
-def test_noalloc_rejects_a_problem_larger_than_its_scratch():
-    """The long-clip shape needs 53 MB of partial rows for a single query block: rejected
-    on the host, before any device work, with the reason in the error message."""
-    lib = load_library()
-    wl = WORKLOADS["long"]
-    dims = make_dims(1, 4, wl.N, wl.d, wl.r, wl.k)
-    p = ctypes.c_void_p(0x1000)   # never dereferenced: the size check comes first
-    assert lib.dsv_sparse_attn_bwd_noalloc(ctypes.byref(dims), p, p, p, p, p, p, p, p, p, p, None) == 3
-    assert b"no-allocation" in lib.dsv_last_error_message()
