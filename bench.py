@@ -1,21 +1,23 @@
 #!/usr/bin/env python
 """Benchmark one DSV sparse-attention layer step on GB300.
 
-A step is one pass of the whole hot path over one batch of synthetic input:
-low-rank estimate + top-k per query block -> sparse attention forward -> sparse
-attention backward (dQ, dK, dV), all through the C ABI (libdsv.so).
+A step is one pass of the whole hot path over one batch of synthetic input, for every head
+of the layer: low-rank estimate + top-k per query block -> sparse attention forward ->
+sparse attention backward (dQ, dK, dV), all through the C ABI (libdsv.so).  The default
+workload is the long video: 24 heads of N = 520,192 tokens at d = 128, k = 52,019 (10 %),
+run as 6 calls of 4 heads (the selection of 4 heads takes 6.8 GB).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload short] [--impl dsv|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long] [--impl dsv|reference]
 
 Prints ONE JSON line (rank 0).  `value` is the effective TFLOP/s of the whole job:
 14 * B * H * N * k * d flops per step (4 N k d forward + 10 N k d backward, only the
 selected query-key pairs counted) divided by the step time, which includes the
-estimate/top-k.  Inputs are resident in HBM when the timed region starts; between timed
-steps (outside the timed events) a 512 MiB memset flushes L2 and a read of another 512 MiB
-buffer leaves it holding clean lines.  `e2e` is the same
-metric when every step also copies its inputs host->device from pinned memory and
-its outputs (O, LSE, dQ, dK, dV) back.  Under torchrun each rank runs an independent
-replica (weak scaling, no collective on the data path).
+estimate/top-k.  Inputs are resident in HBM when the timed region starts (drawn there by a
+seeded device generator); between timed steps (outside the timed events) a 512 MiB memset
+flushes L2 and a read of another 512 MiB buffer leaves it holding clean lines.  `e2e` is the
+same metric when every head group's inputs are also copied host->device from pinned memory
+and its outputs (O, LSE, dQ, dK, dV) back, inside the timed region.  Under torchrun each rank
+runs an independent replica (weak scaling, no collective on the data path).
 """
 from __future__ import annotations
 
@@ -36,24 +38,28 @@ sys.path.insert(0, REPO)
 METRIC = "sparse attn fwd+bwd effective TFLOP/s and tokens/s at 10% density; % of bf16 peak"
 CSRC = os.path.join(REPO, "dynamic_sparse_attention_estimate_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(REPO, "profiles", "kernel_traffic.json")
+GIB = 1 << 30
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="short")
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="long", help="tiny, short, mid, sweep or long (default: long)")
     ap.add_argument("--density", type=float, default=None)
     ap.add_argument("--impl", default="dsv", choices=["dsv", "reference"])
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads (small cases for profiler captures)")
+    ap.add_argument("--ws-gib", type=float, default=64.0,
+                    help="backward workspace cap in GiB when a head group's partial rows do not fit one wave")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adaptive", action="store_true", help="skip the mass-based selection measurement")
     ap.add_argument("--no-adaln", action="store_true", help="skip the fused AdaLN measurement")
-    ap.add_argument("--heads", type=int, default=None,
-                    help="run the workload with this many heads (small cases for profiler captures)")
-    return ap.parse_args()
+    ap.add_argument("--no-side", action="store_true", help="skip every side measurement (dense, adaptive, AdaLN)")
+    return ap.parse_args(argv)
 
 
 def workload(args):
@@ -61,19 +67,33 @@ def workload(args):
     wl = WORKLOADS[args.workload]
     if args.density is not None:
         wl = wl.with_density(args.density)
-    if wl.heads_per_call:
-        wl = wl.with_heads(wl.heads_per_call)   # the long clip runs 4 heads per call
     if args.heads is not None:
         wl = wl.with_heads(args.heads)
     return wl
 
 
+def heads_per_call(wl):
+    """Heads per library call: the long clip runs its heads 4 at a time (its idx for 4 heads is
+    6.8 GB); the other workloads run all heads in one call."""
+    return min(wl.heads_per_call or wl.H, wl.H)
+
+
 def config_of(wl):
     t, h, w = wl.latent
-    return {"workload": f"{wl.name}: B={wl.B} H={wl.H} latent {t}x{h}x{w} -> N={wl.N}, d={wl.d}, r={wl.r}, "
-                        f"k={wl.k} ({100 * wl.density:.1f}% density), query blocks of 64",
-            "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "r": wl.r, "k": wl.k, "block": 64,
-            "density": round(wl.density, 4), "l2": "flushed between timed steps (outside the timed events): 512 MiB memset, then a read of another 512 MiB"}
+    hpc = heads_per_call(wl)
+    calls = (wl.H + hpc - 1) // hpc
+    per_call = f" ({calls} calls of {hpc} heads)" if calls > 1 else ""
+    return {"workload": f"{wl.name}: B={wl.B} H={wl.H}{per_call} latent {t}x{h}x{w} -> N={wl.N}, d={wl.d}, "
+                        f"r={wl.r}, k={wl.k} ({100 * wl.density:.1f}% density), query blocks of 64",
+            "B": wl.B, "H": wl.H, "heads_per_call": hpc, "N": wl.N, "d": wl.d, "r": wl.r, "k": wl.k, "block": 64,
+            "density": round(wl.density, 4),
+            "l2": "flushed between timed steps (outside the timed events): 512 MiB memset, then a read of another "
+                  "512 MiB; a step's inputs (%.1f GB) %s L2" % (step_input_bytes(wl) / 1e9,
+                                                              "exceed" if step_input_bytes(wl) > 129e6 else "fit in")}
+
+
+def step_input_bytes(wl):
+    return wl.B * wl.H * wl.N * (4 * wl.d + 2 * wl.r) * 2
 
 
 def flops_per_step(wl):
@@ -108,9 +128,9 @@ def oracle_sample(wl, budget_s, cache={}):
     return 14.0 * 64 * nblocks * wl.k * wl.d, dt, nblocks
 
 
-def dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs):
+def dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs, H=None):
     from dynamic_sparse_attention_estimate_gb300.binding import dsv_sparse_attn_bwd_csr_workspace, make_dims
-    return dsv_sparse_attn_bwd_csr_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, wl.k), pairs)
+    return dsv_sparse_attn_bwd_csr_workspace(make_dims(wl.B, H or wl.H, wl.N, wl.d, wl.r, wl.k), pairs)
 
 
 def max_over_ranks(ms, dev, world):
@@ -246,8 +266,11 @@ def kernel_source_hash(kernel):
 
 
 def algorithmic(kernel, wl, launches_per_step):
-    """(bound, amount per launch, unit) for a kernel of the step."""
+    """(bound, amount per launch, unit) for a kernel of the step: flops of the selected pairs for the
+    attention kernels; for the HBM-bound kernels the bytes they must move (the reduce: every bf16
+    partial row and its list entry read, dK and dV written)."""
     BH = wl.B * wl.H
+    pairs = BH * wl.NB * wl.k
     if kernel == "sparse_fwd":
         return "tensor", 4.0 * BH * wl.N * wl.k * wl.d / launches_per_step, "flop"
     if kernel == "bwd_main":
@@ -255,22 +278,18 @@ def algorithmic(kernel, wl, launches_per_step):
     if kernel == "estimate_topk":
         return "hbm", (2.0 * BH * wl.N * wl.r * 2 + 4.0 * BH * wl.NB * wl.k) / launches_per_step, "byte"
     if kernel == "bwd_reduce":
-        pairs = BH * wl.NB * wl.k
-        return "hbm", (pairs * 2 * wl.d * 4 + 2.0 * BH * wl.N * wl.d * 2) / launches_per_step, "byte"
+        return "hbm", (pairs * (2 * wl.d * 2 + 4) + 2.0 * BH * wl.N * wl.d * 2) / launches_per_step, "byte"
     return None, None, None
 
 
-def roofline(prof, steps, wl):
+def kernel_roofline(name, launches, total_ms, steps, wl):
     hbm, bf16, src = measured_peaks()
-    kern = {k: v for k, v in prof.items() if k != "dropped"}
-    name, (launches, total_ms) = max(kern.items(), key=lambda kv: kv[1][1])
     bound, amount, unit = algorithmic(name, wl, launches / steps)
-    avg_s = total_ms / launches / 1e3
-    out = {"kernel": name, "launches": launches, "avg_ms": total_ms / launches,
-           "share_of_kernel_time": total_ms / sum(v[1] for v in kern.values())}
+    out = {"kernel": name, "launches": launches, "avg_ms": total_ms / launches}
     if bound is None:
-        out.update({"bound": None, "achieved": None, "peak": None, "unit": None, "frac": None, "traffic": None})
+        out.update({"bound": None, "achieved": None, "peak": None, "unit": None, "frac": None})
         return out
+    avg_s = total_ms / launches / 1e3
     if bound == "tensor":
         achieved = amount / avg_s / 1e12
         out.update({"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
@@ -280,16 +299,32 @@ def roofline(prof, steps, wl):
         out.update({"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "peak_source": f"hbm_gbs, of {src}"})
     out["algorithmic_per_launch"] = amount
+    return out
+
+
+def roofline(prof, steps, wl):
+    kern = {k: v for k, v in prof.items() if k != "dropped"}
+    name, (launches, total_ms) = max(kern.items(), key=lambda kv: kv[1][1])
+    out = kernel_roofline(name, launches, total_ms, steps, wl)
+    out["share_of_kernel_time"] = total_ms / sum(v[1] for v in kern.values())
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         t = json.load(open(TRAFFIC_FILE)).get(name)
         if t and t.get("source_hash") == kernel_source_hash(name) and t.get("workload") == wl.name:
             traffic = t["bytes_per_launch"]
     out["traffic"] = traffic
+    if name == "bwd_main":
+        # the same launches seen from HBM: every pair writes its bf16 partial row (4 d bytes) and list
+        # entry, and gathers its K and V rows (4 d bytes, from L2 or HBM)
+        pairs = wl.B * wl.H * wl.NB * wl.k / (launches / steps)
+        hbm = measured_peaks()[0]
+        w = pairs * (4 * wl.d + 4) / (out["avg_ms"] / 1e3) / 1e9
+        out["hbm_view"] = {"partial_row_write_gbs": w, "frac_of_hbm": w / hbm,
+                           "gather_gbs": pairs * 4 * wl.d / (out["avg_ms"] / 1e3) / 1e9}
     return out
 
 
-# ---------------------------------------------------------------- the DSV arm
+# ---------------------------------------------------------------- side measurements
 
 def adaln_measurements(dev, timed):
     """Fused AdaLN on its two workloads: forward and backward times (L2 flushed before each call),
@@ -329,6 +364,135 @@ def adaln_measurements(dev, timed):
     return out
 
 
+def dense_comparator(g, wl, timed, ms_per_step):
+    """PyTorch SDPA forward + backward (a library timing comparator, not this library) on the same
+    per-head shape, every backend that runs here, one head, scaled to the step's heads; the speedup
+    is quoted against the fastest backend."""
+    import torch
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    heads = 1 if wl.N > 65536 else heads_per_call(wl)
+    scale_to = wl.H / heads
+    qf, kf, vf = [g[n][:, :heads].detach().clone().requires_grad_(True) for n in ("q", "k", "v")]
+    do = g["do"][:, :heads].contiguous()
+    dense_flop = 14.0 * wl.B * wl.H * wl.N * wl.N * wl.d
+    reps = 2 if wl.N > 65536 else 5
+    backends = {}
+    for name, be in (("cudnn", SDPBackend.CUDNN_ATTENTION), ("flash", SDPBackend.FLASH_ATTENTION),
+                     ("efficient", SDPBackend.EFFICIENT_ATTENTION)):
+        try:
+            def dense_step():
+                with sdpa_kernel([be]):
+                    out = torch.nn.functional.scaled_dot_product_attention(qf, kf, vf)
+                    out.backward(do)
+            dense_step()
+            torch.cuda.synchronize()
+            ms = timed(dense_step, reps) * scale_to
+            backends[name] = {"ms": ms, "tflops": dense_flop / (ms / 1e3) / 1e12}
+        except Exception as exc:  # a backend that does not run on this GPU / shape
+            backends[name] = {"error": str(exc).splitlines()[0][:160]}
+        torch.cuda.synchronize()
+    ok = {k: v for k, v in backends.items() if "ms" in v}
+    out = {"impl": "torch SDPA (library), fwd+bwd", "heads_timed": heads,
+           "scaled": f"x{scale_to:g} to the step's {wl.H} heads" if scale_to != 1 else None, "backends": backends}
+    if ok:
+        best = min(ok, key=lambda k: ok[k]["ms"])
+        out.update({"fastest": best, "ms": ok[best]["ms"], "tflops": ok[best]["tflops"],
+                    "speedup_of_sparse_step": ok[best]["ms"] / ms_per_step})
+    del qf, kf, vf, do
+    return out
+
+
+def adaptive_measurement(dev, timed):
+    """The mass-based selection (per block the keys carrying 90 % of the estimated mass, tau = 1/64)
+    on the short clip: selection, then forward + backward over the CSR key lists."""
+    import torch
+    from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_mass_k, dsv_estimate_topk_csr,
+                                                          dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr)
+    from dynamic_sparse_attention_estimate_gb300.inputs import WORKLOADS, make_inputs_on_device
+    wl = WORKLOADS["short"]
+    g = make_inputs_on_device(wl, dev)
+    o = torch.empty_like(g["q"])
+    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
+    k_row, rowptr, order = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9)
+    cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr)
+    pairs = cols.numel()
+    ws_a = torch.empty(dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs), dtype=torch.uint8, device=dev)
+    t_sel = timed(lambda: (dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9, out=(k_row, rowptr, order)),
+                           dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr, cols=cols)), 5)
+    t_af = timed(lambda: dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rowptr, cols, out=(o, lse), order=order), 5)
+    t_ab = timed(lambda: dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rowptr, cols,
+                                                 workspace=ws_a, out=(dq, dk, dv), order=order), 5)
+    fl_a = 14.0 * 64 * pairs * wl.d
+    kr = k_row.float()
+    return {"workload": "short clip (12 heads, N=16384, d=64)", "tau": 1.0 / 64, "mass": 0.9,
+            "mean_k": float(kr.mean()), "min_k": int(k_row.min()), "max_k": int(k_row.max()),
+            "density": pairs / (wl.B * wl.H * wl.NB * wl.N), "selection_ms": t_sel, "fwd_ms": t_af, "bwd_ms": t_ab,
+            "attn_tflops": fl_a / ((t_af + t_ab) / 1e3) / 1e12,
+            "step_tflops": fl_a / ((t_sel + t_af + t_ab) / 1e3) / 1e12}
+
+
+# ---------------------------------------------------------------- the DSV arm
+
+class LayerStep:
+    """One step over every head of the layer, head group by head group: estimate -> forward ->
+    backward.  When a group's backward fits one wave of the workspace, its first part (the key-major
+    rank structure of idx) runs on a second stream beside the forward."""
+
+    def __init__(self, wl, dev, ws_cap):
+        import torch
+        from dynamic_sparse_attention_estimate_gb300.binding import dsv_sparse_attn_bwd_workspace, make_dims
+        self.wl, self.dev = wl, dev
+        self.hpc = heads_per_call(wl)
+        self.groups = [(h0, min(self.hpc, wl.H - h0)) for h0 in range(0, wl.H, self.hpc)]
+        self.idx = torch.empty((wl.B, self.hpc, wl.NB, wl.k), dtype=torch.int32, device=dev)
+        dims = make_dims(wl.B, self.hpc, wl.N, wl.d, wl.r, wl.k)
+        one_wave = dsv_sparse_attn_bwd_csr_workspace_bytes(wl, wl.B * self.hpc * wl.NB * wl.k, self.hpc)
+        ws_bytes = one_wave if one_wave <= ws_cap else max(dsv_sparse_attn_bwd_workspace(dims), int(ws_cap))
+        self.split = ws_bytes >= one_wave
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        self.side = torch.cuda.Stream()
+        self.have_idx, self.prepared = torch.cuda.Event(), torch.cuda.Event()
+
+    def group(self, x, out, h0, nh, idx=None):
+        """Estimate, forward and backward of heads [h0, h0 + nh) of the tensors in x, writing the
+        matching heads of out (o, lse, dq, dk, dv), on the current stream."""
+        import torch
+        from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_topk, dsv_sparse_attn_bwd,
+                                                             dsv_sparse_attn_bwd_prepare, dsv_sparse_attn_bwd_prepared,
+                                                             dsv_sparse_attn_fwd)
+        wl = self.wl
+        sl = lambda t: t[:, h0:h0 + nh]
+        idx = self.idx[:, :nh] if idx is None else idx
+        q, k, v, do = sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"])
+        o, lse, dq, dk, dv = (sl(out[n]) for n in ("o", "lse", "dq", "dk", "dv"))
+        dsv_estimate_topk(sl(x["q_lr"]), sl(x["k_lr"]), wl.k, idx=idx)
+        if self.split:
+            cur = torch.cuda.current_stream()
+            self.have_idx.record(cur)
+            dsv_sparse_attn_fwd(q, k, v, idx, out=(o, lse))
+            with torch.cuda.stream(self.side):
+                self.side.wait_event(self.have_idx)
+                dsv_sparse_attn_bwd_prepare(idx, wl.d, self.ws)
+                self.prepared.record(self.side)
+            cur.wait_event(self.prepared)
+            dsv_sparse_attn_bwd_prepared(do, q, k, v, o, lse, idx, self.ws, out=(dq, dk, dv))
+        else:
+            dsv_sparse_attn_fwd(q, k, v, idx, out=(o, lse))
+            dsv_sparse_attn_bwd(do, q, k, v, o, lse, idx, workspace=self.ws, out=(dq, dk, dv))
+
+    def __call__(self, x, out):
+        for h0, nh in self.groups:
+            self.group(x, out, h0, nh)
+
+
+def check_status(where):
+    from dynamic_sparse_attention_estimate_gb300.binding import dsv_last_device_status
+    st = dsv_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status word set during {where} (status {st}): the run is not valid")
+
+
 def dsv_arm(args):
     import torch
     import torch.distributed as dist
@@ -343,24 +507,19 @@ def dsv_arm(args):
     dev = torch.device("cuda", local)
 
     from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_topk, dsv_sparse_attn_bwd,
-                                                         dsv_sparse_attn_bwd_prepare, dsv_sparse_attn_bwd_prepared,
                                                          dsv_sparse_attn_fwd, load_library)
-    from dynamic_sparse_attention_estimate_gb300.binding import (dsv_last_device_status, dsv_profile_enable,
-                                                                 dsv_profile_read, dsv_sparse_attn_bwd_workspace,
-                                                                 make_dims)
-    from dynamic_sparse_attention_estimate_gb300.inputs import make_inputs
+    from dynamic_sparse_attention_estimate_gb300.binding import (dsv_profile_enable, dsv_profile_read,
+                                                                 dsv_sparse_attn_bwd_workspace, make_dims)
+    from dynamic_sparse_attention_estimate_gb300.inputs import make_inputs_on_device
     load_library()
 
     wl = workload(args)
-    host = make_inputs(wl)
+    BH = wl.B * wl.H
     names = ("q", "k", "v", "do", "q_lr", "k_lr")
-    g = {n: host[n].to(dev) for n in names}
-    idx = torch.empty((wl.B, wl.H, wl.NB, wl.k), dtype=torch.int32, device=dev)
-    o = torch.empty_like(g["q"])
-    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
-    ws = torch.empty(dsv_sparse_attn_bwd_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, wl.k)),
-                     dtype=torch.uint8, device=dev)
+    g = make_inputs_on_device(wl, dev)
+    outs = {"o": torch.empty_like(g["q"]), "lse": torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev),
+            "dq": torch.empty_like(g["q"]), "dk": torch.empty_like(g["q"]), "dv": torch.empty_like(g["q"])}
+    step = LayerStep(wl, dev, args.ws_gib * GIB)
     # L2 flush between timed calls: write a 512 MiB buffer (4x the 129 MB L2), then read another
     # one, so that the lines left in L2 are clean and the next timed kernel does not pay for
     # writing the flush's dirty lines back to HBM
@@ -371,28 +530,10 @@ def dsv_arm(args):
         flush.zero_()
         flush_rd.sum()
 
-    # One step: the estimate; the forward; the backward's rank structure of idx built on a second
-    # stream beside the forward (enqueued after it, so it takes the SMs the forward's last wave
-    # leaves idle); then the rest of the backward once both are done.
-    side = torch.cuda.Stream()
-    have_idx, prepared = torch.cuda.Event(), torch.cuda.Event()
-
-    def step():
-        dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k, idx=idx)
-        have_idx.record()
-        dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx, out=(o, lse))
-        with torch.cuda.stream(side):
-            side.wait_event(have_idx)
-            dsv_sparse_attn_bwd_prepare(idx, wl.d, ws)
-            prepared.record(side)
-        torch.cuda.current_stream().wait_event(prepared)
-        dsv_sparse_attn_bwd_prepared(g["do"], g["q"], g["k"], g["v"], o, lse, idx, ws, out=(dq, dk, dv))
-
     for _ in range(args.warmup):
-        step()
+        step(g, outs)
     torch.cuda.synchronize()
-    if dsv_last_device_status() != 0:
-        raise RuntimeError("device status set during warm-up")
+    check_status("warm-up")
 
     # ---- timed region (device-resident inputs)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -406,13 +547,14 @@ def dsv_arm(args):
         for i in range(args.steps):
             flush_l2()
             starts[i].record()
-            step()
+            step(g, outs)
             ends[i].record()
         torch.cuda.synchronize()
         t_wall1 = time.time()
         prof = dsv_profile_read()
         dsv_profile_enable(False)
     clocks = clk.summary(t_wall0, t_wall1)
+    check_status("the timed steps")
     total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     if world > 1:
         dist.barrier()
@@ -420,8 +562,8 @@ def dsv_arm(args):
     fl = flops_per_step(wl)
     value = job_tflops(world, args.steps, fl, total_ms)
     ms_per_step = total_ms / args.steps
+    heavy = ms_per_step > 300.0
 
-    # ---- stage breakdown (separately timed, same inputs)
     def timed(fn, n):
         """Median device time of fn over n calls, each after an L2 flush.  All n calls are
         enqueued before one synchronisation, so the host's launch latency stays outside the
@@ -435,192 +577,213 @@ def dsv_arm(args):
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ev)
 
-    n_stage = max(3, min(20, args.steps))
-    t_est = timed(lambda: dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k, idx=idx), n_stage)
-    t_fwd = timed(lambda: dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx, out=(o, lse)), n_stage)
-    t_bwd = timed(lambda: dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws,
-                                              out=(dq, dk, dv)), n_stage)
-    BH = wl.B * wl.H
+    # ---- stage breakdown: each stage over every head group, timed alone (same inputs)
+    n_stage = 2 if heavy else max(3, min(20, args.steps))
+    sl = lambda t, h0, nh: t[:, h0:h0 + nh]
+    idx_all = [step.idx[:, :nh] for _, nh in step.groups]
 
-    # ---- e2e through the public API with host buffers: every step copies its inputs host->device
-    # from pinned memory and its outputs (O, LSE, dQ, dK, dV) back.  Measured two ways: serial (copy
-    # in, step, copy out, synchronise) and pipelined (three streams, device inputs and outputs
-    # double-buffered: step i+1's inputs go in and step i-1's outputs come back while step i
-    # computes), which is what a training loop that prefetches its batches sees.
+    def est_all():
+        for (h0, nh), idx in zip(step.groups, idx_all):
+            dsv_estimate_topk(sl(g["q_lr"], h0, nh), sl(g["k_lr"], h0, nh), wl.k, idx=idx)
+
+    def fwd_all():
+        for (h0, nh), idx in zip(step.groups, idx_all):
+            dsv_sparse_attn_fwd(sl(g["q"], h0, nh), sl(g["k"], h0, nh), sl(g["v"], h0, nh), idx,
+                                out=(sl(outs["o"], h0, nh), sl(outs["lse"], h0, nh)))
+
+    def bwd_all():
+        for (h0, nh), idx in zip(step.groups, idx_all):
+            dsv_sparse_attn_bwd(*(sl(g[n], h0, nh) for n in ("do", "q", "k", "v")), sl(outs["o"], h0, nh),
+                                sl(outs["lse"], h0, nh), idx, workspace=step.ws,
+                                out=tuple(sl(outs[n], h0, nh) for n in ("dq", "dk", "dv")))
+
+    if len(step.groups) == 1:
+        t_est, t_fwd, t_bwd = timed(est_all, n_stage), timed(fwd_all, n_stage), timed(bwd_all, n_stage)
+    else:   # the selection of a group is overwritten by the next: time each group's stages in turn
+        t_est = t_fwd = t_bwd = 0.0
+        for gi in range(len(step.groups)):
+            h0, nh = step.groups[gi]
+            idx = idx_all[gi]
+            t_est += timed(lambda: dsv_estimate_topk(sl(g["q_lr"], h0, nh), sl(g["k_lr"], h0, nh), wl.k, idx=idx),
+                           n_stage)
+            t_fwd += timed(lambda: dsv_sparse_attn_fwd(sl(g["q"], h0, nh), sl(g["k"], h0, nh), sl(g["v"], h0, nh),
+                                                       idx, out=(sl(outs["o"], h0, nh), sl(outs["lse"], h0, nh))),
+                           n_stage)
+            t_bwd += timed(lambda: dsv_sparse_attn_bwd(*(sl(g[n], h0, nh) for n in ("do", "q", "k", "v")),
+                                                       sl(outs["o"], h0, nh), sl(outs["lse"], h0, nh), idx,
+                                                       workspace=step.ws,
+                                                       out=tuple(sl(outs[n], h0, nh) for n in ("dq", "dk", "dv"))),
+                           n_stage)
+    check_status("the stage timings")
+
+    # ---- e2e through the public API with host buffers: every head group's inputs are copied
+    # host->device from pinned memory and its outputs (O, LSE, dQ, dK, dV) back, inside the timed
+    # region.  Measured two ways: serial (copy in, compute, copy out, synchronise, group by group)
+    # and pipelined (three streams, device buffers for two groups: group i+1's inputs go in and
+    # group i-1's outputs come back while group i computes), which is what a training loop that
+    # prefetches its batches sees.
     e2e = None
     if not args.no_e2e:
-        pinned = {n: host[n].pin_memory() for n in names}
-        outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-        d2h = sum(t.numel() * t.element_size() for t in outs.values())
-        n_e2e = max(3, min(args.steps, 50))
+        pinned = {n: torch.empty(g[n].shape, dtype=g[n].dtype, pin_memory=True) for n in names}
+        for n in names:
+            pinned[n].copy_(g[n])
         back = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
-        for i in range(n_e2e + 2):                 # two untimed passes first
-            a, b = ev[max(i - 2, 0)]
-            if i >= 2:
-                a.record()
-            for n in names:
-                g[n].copy_(pinned[n], non_blocking=True)
-            step()
-            for n, t in outs.items():
-                back[n].copy_(t, non_blocking=True)
-            if i >= 2:
-                b.record()
-            torch.cuda.synchronize()
-        serial_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev, world) / n_e2e
-
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in back.values())
+        n_e2e = 2 if heavy else max(3, min(args.steps, 50))
+        hpc = step.hpc
         slots = []
         for _ in range(2):
-            gi = {n: torch.empty_like(g[n]) for n in names}
-            go = {n: torch.empty_like(t) for n, t in outs.items()}
-            hb = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
-            slots.append((gi, go, hb, torch.empty_like(idx)))
+            gi = {n: torch.empty((wl.B, hpc) + tuple(g[n].shape[2:]), dtype=g[n].dtype, device=dev) for n in names}
+            go = {n: torch.empty((wl.B, hpc) + tuple(t.shape[2:]), dtype=t.dtype, device=dev)
+                  for n, t in outs.items()}
+            slots.append((gi, go, torch.empty_like(step.idx)))
+        units = [(s, h0, nh) for s in range(n_e2e) for (h0, nh) in step.groups]
+
+        def copy_in(gi, h0, nh):
+            for n in names:
+                gi[n][:, :nh].copy_(sl(pinned[n], h0, nh), non_blocking=True)
+
+        def copy_out(go, h0, nh):
+            for n in outs:
+                sl(back[n], h0, nh).copy_(go[n][:, :nh], non_blocking=True)
+
+        def compute(gi, go, idx_s, nh):
+            step.group(gi, go, 0, nh, idx=idx_s[:, :nh])
+
+        def serial(n_units):
+            for i in range(n_units):
+                _, h0, nh = units[i % len(units)]
+                gi, go, idx_s = slots[0]
+                copy_in(gi, h0, nh)
+                compute(gi, go, idx_s, nh)
+                copy_out(go, h0, nh)
+                torch.cuda.synchronize()
+
+        serial(len(step.groups))   # untimed
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        serial(len(units))
+        b.record()
+        torch.cuda.synchronize()
+        serial_ms = max_over_ranks(a.elapsed_time(b), dev, world) / n_e2e
+
         s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
         in_done = [torch.cuda.Event() for _ in range(2)]
         cmp_done = [torch.cuda.Event() for _ in range(2)]
         out_done = [torch.cuda.Event() for _ in range(2)]
 
-        def pipelined(n_steps, t0=None, t1=None):
-            for i in range(n_steps):
+        def pipelined(n_units, t0=None, t1=None):
+            for i in range(n_units):
+                _, h0, nh = units[i % len(units)]
                 si = i % 2
-                gi, go, hb, idx_s = slots[si]
+                gi, go, idx_s = slots[si]
                 with torch.cuda.stream(s_in):
                     if i >= 2:
-                        s_in.wait_event(cmp_done[si])      # step i-2 has consumed this slot's inputs
+                        s_in.wait_event(cmp_done[si])      # unit i-2 has consumed this slot's inputs
                     if i == 0 and t0 is not None:
                         t0.record(s_in)
-                    for n in names:
-                        gi[n].copy_(pinned[n], non_blocking=True)
+                    copy_in(gi, h0, nh)
                     in_done[si].record(s_in)
                 with torch.cuda.stream(s_cmp):
                     s_cmp.wait_event(in_done[si])
                     if i >= 2:
-                        s_cmp.wait_event(out_done[si])     # step i-2's outputs have left this slot
-                    dsv_estimate_topk(gi["q_lr"], gi["k_lr"], wl.k, idx=idx_s)
-                    have_idx.record(s_cmp)
-                    dsv_sparse_attn_fwd(gi["q"], gi["k"], gi["v"], idx_s, out=(go["o"], go["lse"]))
-                with torch.cuda.stream(side):
-                    side.wait_event(have_idx)
-                    dsv_sparse_attn_bwd_prepare(idx_s, wl.d, ws)
-                    prepared.record(side)
-                with torch.cuda.stream(s_cmp):
-                    s_cmp.wait_event(prepared)
-                    dsv_sparse_attn_bwd_prepared(gi["do"], gi["q"], gi["k"], gi["v"], go["o"], go["lse"], idx_s, ws,
-                                                 out=(go["dq"], go["dk"], go["dv"]))
+                        s_cmp.wait_event(out_done[si])     # unit i-2's outputs have left this slot
+                    compute(gi, go, idx_s, nh)
                     cmp_done[si].record(s_cmp)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(cmp_done[si])
-                    for n in outs:
-                        hb[n].copy_(go[n], non_blocking=True)
+                    copy_out(go, h0, nh)
                     out_done[si].record(s_out)
             if t1 is not None:
                 with torch.cuda.stream(s_out):
                     t1.record(s_out)
             torch.cuda.synchronize()
 
-        # the copies alone (every step's H2D then D2H, no compute), to show what the pipeline hides
+        # the copies alone (every unit's H2D then D2H, no compute), to show what the pipeline hides
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         c0.record()
-        for i in range(n_e2e):
-            gi, go, hb, _ = slots[i % 2]
-            for n in names:
-                gi[n].copy_(pinned[n], non_blocking=True)
-            for n in outs:
-                hb[n].copy_(go[n], non_blocking=True)
+        for i, (_, h0, nh) in enumerate(units):
+            gi, go, _ = slots[i % 2]
+            copy_in(gi, h0, nh)
+            copy_out(go, h0, nh)
         c1.record()
         torch.cuda.synchronize()
         copy_ms = max_over_ranks(c0.elapsed_time(c1), dev, world) / n_e2e
 
-        pipelined(2)                                # untimed
+        pipelined(min(2, len(units)))               # untimed
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         # the start event waits for nothing queued before it: every stream is idle here
-        pipelined(n_e2e, t0, t1)
+        pipelined(len(units), t0, t1)
         pipe_ms = max_over_ranks(t0.elapsed_time(t1), dev, world) / n_e2e
+        check_status("the end-to-end steps")
         e2e = {"value": job_tflops(world, n_e2e, fl, pipe_ms * n_e2e), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms, "steps": n_e2e,
-               "pipelined": "4 streams; device inputs and outputs double-buffered; step i+1's H2D and step i-1's "
-                            "D2H overlap step i; the backward's rank structure beside the forward",
+               "pipelined": "3 streams; device buffers for two head groups; group i+1's H2D and group i-1's D2H "
+                            "overlap group i's estimate, forward and backward",
                "copies_alone_ms_per_step": copy_ms,
                "serial": {"value": job_tflops(world, n_e2e, fl, serial_ms * n_e2e), "ms_per_step": serial_ms}}
+        del pinned, back, slots
 
-    # ---- dense comparator (PyTorch SDPA fwd+bwd on the same shape)
+    side = not args.no_side
     dense = None
-    if not args.no_dense:
+    if side and not args.no_dense:
         try:
-            qf, kf, vf = [g[n].detach().clone().requires_grad_(True) for n in ("q", "k", "v")]
-
-            def dense_step():
-                out = torch.nn.functional.scaled_dot_product_attention(qf, kf, vf)
-                out.backward(g["do"])
-            for _ in range(2):
-                dense_step()
-            t_dense = timed(dense_step, 5)
-            dense = {"ms": t_dense, "tflops": 14.0 * BH * wl.N * wl.N * wl.d / (t_dense / 1e3) / 1e12,
-                     "speedup_of_sparse_step": t_dense / ms_per_step, "impl": "torch SDPA (library)"}
+            dense = dense_comparator(g, wl, timed, ms_per_step)
         except Exception as exc:  # a comparator only
             dense = {"error": str(exc)[:200]}
 
     # ---- this library at density 100 % (k = N: idx = every key, ascending) on the same shape: the
-    # sparse kernels run as a dense attention
+    # sparse kernels run as a dense attention (only where k = N fits: idx and partial rows grow as N^2)
     own_dense = None
-    if not args.no_dense:
-        try:
-            kd = wl.N
-            idx_d = torch.empty((wl.B, wl.H, wl.NB, kd), dtype=torch.int32, device=dev)
-            ws_d = torch.empty(dsv_sparse_attn_bwd_workspace(make_dims(wl.B, wl.H, wl.N, wl.d, wl.r, kd)),
-                               dtype=torch.uint8, device=dev)
+    if side and not args.no_dense:
+        if wl.N > 131072:
+            own_dense = {"skipped": f"k = N at N = {wl.N} needs {4 * wl.NB * wl.N / 1e9:.0f} GB of idx and "
+                                    f"{4 * wl.d * wl.NB * wl.N / 1e12:.1f} TB of partial rows per head"}
+        else:
+            try:
+                kd = wl.N
+                hpc = step.hpc
+                idx_d = torch.empty((wl.B, hpc, wl.NB, kd), dtype=torch.int32, device=dev)
+                dims_d = make_dims(wl.B, hpc, wl.N, wl.d, wl.r, kd)
+                ws_d = torch.empty(min(dsv_sparse_attn_bwd_workspace(dims_d), int(args.ws_gib * GIB)),
+                                   dtype=torch.uint8, device=dev)
+                h0, nh = step.groups[0]
 
-            def own_dense_step():
-                dsv_estimate_topk(g["q_lr"], g["k_lr"], kd, idx=idx_d)
-                dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx_d, out=(o, lse))
-                dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx_d, workspace=ws_d, out=(dq, dk, dv))
-            for _ in range(2):
+                def own_dense_step():
+                    dsv_estimate_topk(sl(g["q_lr"], h0, nh), sl(g["k_lr"], h0, nh), kd, idx=idx_d)
+                    dsv_sparse_attn_fwd(sl(g["q"], h0, nh), sl(g["k"], h0, nh), sl(g["v"], h0, nh), idx_d,
+                                        out=(sl(outs["o"], h0, nh), sl(outs["lse"], h0, nh)))
+                    dsv_sparse_attn_bwd(*(sl(g[n], h0, nh) for n in ("do", "q", "k", "v")), sl(outs["o"], h0, nh),
+                                        sl(outs["lse"], h0, nh), idx_d, workspace=ws_d,
+                                        out=tuple(sl(outs[n], h0, nh) for n in ("dq", "dk", "dv")))
                 own_dense_step()
-            t_od = timed(own_dense_step, 5)
-            own_dense = {"ms": t_od, "tflops": 14.0 * BH * wl.N * wl.N * wl.d / (t_od / 1e3) / 1e12,
-                         "impl": "this library with k = N (idx = arange), estimate + forward + backward"}
-            del idx_d, ws_d
-        except Exception as exc:  # a comparator only
-            own_dense = {"error": str(exc)[:200]}
+                t_od = timed(own_dense_step, 3) * len(step.groups)
+                own_dense = {"ms": t_od, "tflops": 14.0 * BH * wl.N * wl.N * wl.d / (t_od / 1e3) / 1e12,
+                             "impl": "this library with k = N (idx = arange), estimate + forward + backward",
+                             "scaled": f"one group of {nh} heads x{len(step.groups)}" if len(step.groups) > 1 else None}
+                del idx_d, ws_d
+            except Exception as exc:  # a comparator only
+                own_dense = {"error": str(exc)[:200]}
+        check_status("the dense comparison")
 
-    # ---- the adaptive selection (per block the keys carrying 90 % of the estimated mass,
-    # tau = 1/64) on the same inputs: selection, then forward + backward over the CSR lists
     adaptive = None
-    if not args.no_adaptive:
+    if side and not args.no_adaptive:
         try:
-            from dynamic_sparse_attention_estimate_gb300 import (dsv_estimate_mass_k, dsv_estimate_topk_csr,
-                                                                  dsv_sparse_attn_bwd_csr, dsv_sparse_attn_fwd_csr)
-            k_row, rowptr, order = dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9)
-            cols = dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr)
-            pairs = cols.numel()
-            ws_a = torch.empty(dsv_sparse_attn_bwd_csr_workspace_bytes(wl, pairs), dtype=torch.uint8, device=dev)
-            t_sel = timed(lambda: (dsv_estimate_mass_k(g["q_lr"], g["k_lr"], 1.0 / 64, 0.9, out=(k_row, rowptr, order)),
-                                   dsv_estimate_topk_csr(g["q_lr"], g["k_lr"], k_row, rowptr, cols=cols)), 5)
-            t_af = timed(lambda: dsv_sparse_attn_fwd_csr(g["q"], g["k"], g["v"], rowptr, cols, out=(o, lse),
-                                                         order=order), 5)
-            t_ab = timed(lambda: dsv_sparse_attn_bwd_csr(g["do"], g["q"], g["k"], g["v"], o, lse, rowptr, cols,
-                                                         workspace=ws_a, out=(dq, dk, dv), order=order), 5)
-            fl_a = 14.0 * 64 * pairs * wl.d
-            kr = k_row.float()
-            adaptive = {"tau": 1.0 / 64, "mass": 0.9, "mean_k": float(kr.mean()), "min_k": int(k_row.min()),
-                        "max_k": int(k_row.max()), "density": pairs / (BH * wl.NB * wl.N),
-                        "selection_ms": t_sel, "fwd_ms": t_af, "bwd_ms": t_ab,
-                        "attn_tflops": fl_a / ((t_af + t_ab) / 1e3) / 1e12,
-                        "step_tflops": fl_a / ((t_sel + t_af + t_ab) / 1e3) / 1e12}
-            del ws_a
+            adaptive = adaptive_measurement(dev, timed)
         except Exception as exc:  # a side measurement only
             adaptive = {"error": str(exc)[:200]}
 
     # ---- fused AdaLN (LayerNorm + modulation) forward and backward, HBM-bound: bytes moved per
     # call (x, dy read; y, dx written; modulation vectors and gradients) over the measured time
     adaln = None
-    if not args.no_adaln:
+    if side and not args.no_adaln:
         try:
             adaln = adaln_measurements(dev, timed)
         except Exception as exc:  # a side measurement only
             adaln = {"error": str(exc)[:200]}
+    check_status("the side measurements")
 
     if rank != 0:
         if world > 1:
@@ -637,21 +800,28 @@ def dsv_arm(args):
     rl = roofline(prof, args.steps, wl)
     launches = sum(v[0] for k, v in prof.items() if k != "dropped")
     hbm, bf16, src = measured_peaks()
+    kernels = {k: kernel_roofline(k, v[0], v[1], args.steps, wl) for k, v in prof.items() if k != "dropped"}
+    for k, v in kernels.items():
+        v["ms_per_step"] = prof[k][1] / args.steps
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the short-clip workload)",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": f"synthetic (seeded; drawn on the device by torch's generator with the {wl.name} workload's "
+                f"distributions, shapes and block-major order)",
         "config": config_of(wl),
-        "step": "estimate; forward; the backward's rank structure of idx on a second stream beside the forward; "
-                "the rest of the backward",
+        "step": ("per group of %d heads: estimate; forward; %s" % (
+            step.hpc, "the backward's rank structure of idx on a second stream beside the forward, then the rest "
+                      "of the backward" if step.split else "the backward (waves of query blocks through a %.0f GiB "
+                                                            "workspace)" % (step.ws.numel() / GIB))),
         "tokens_per_s": world * wl.B * wl.N * args.steps / (total_ms / 1e3),
         "pct_of_bf16_peak": 100.0 * value / world / bf16,
         "stages_ms": {"estimate_topk": t_est, "sparse_fwd": t_fwd, "sparse_bwd": t_bwd},
         "attn_only_tflops": 14.0 * BH * wl.N * wl.k * wl.d / ((t_fwd + t_bwd) / 1e3) / 1e12,
-        "kernel_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
-        "kernel_ms_note": "bwd_set_bits, bwd_colpre and bwd_scan run on a second stream beside the forward: their "
-                          "event times include waiting for SMs the forward holds (set_bits starts as soon as idx "
-                          "exists); bwd_main is not affected",
+        "tokens_per_s_attn_only": wl.B * wl.N / ((t_fwd + t_bwd) / 1e3),
+        "kernels": kernels,
+        "kernel_ms_note": "per-kernel event times inside the timed steps; kernels on the second stream (the "
+                          "backward's set_bits, colpre, scan beside the forward) include waiting for SMs",
         "estimate": {"ms": t_est, "score_elements_per_s": BH * wl.NB * wl.N / (t_est / 1e3),
                      "mma_tflops": 2.0 * wl.r * BH * wl.NB * wl.N / (t_est / 1e3) / 1e12},
         "roofline": rl, "gpu_launches": launches, "clocks": clocks, "e2e": e2e, "dense_comparator": dense,

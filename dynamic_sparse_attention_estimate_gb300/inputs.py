@@ -223,3 +223,48 @@ def make_adaln_inputs(B: int, N: int, D: int, seed: int = 0) -> Dict[str, torch.
     shift = torch.randn(B, D, generator=g).to(torch.bfloat16)
     dy = torch.randn(B, N, D, generator=g).to(torch.bfloat16)
     return {"x": x.contiguous(), "scale": scale.contiguous(), "shift": shift.contiguous(), "dy": dy.contiguous()}
+
+
+def make_inputs_on_device(wl: Workload, device, heads: Optional[Sequence[int]] = None, b: int = 0
+                          ) -> Dict[str, torch.Tensor]:
+    """The same workload drawn directly in device memory, for timing runs whose inputs would take
+    minutes to draw on the host (the long clip's 24 heads are 6.4 G normal samples).
+
+    Same distributions, draw order, per-(batch, head) seeds, mid-clip planting and block-major
+    token order as :func:`make_head`, but the numbers come from torch's device generator
+    (Philox), so they differ from the host draw: nothing compares them with the oracle.
+    Returns stacked [1, len(heads), N, *] tensors on ``device``.
+    """
+    if heads is None:
+        heads = range(wl.H)
+    heads = list(heads)
+    N, d, r = wl.N, wl.d, wl.r
+    perm = torch.from_numpy(block_major_permutation(wl.latent, wl.block_shape)).to(device)
+    names = ("q", "k", "v", "do", "q_lr", "k_lr")
+    out = {n: torch.empty((1, len(heads), N, r if n.endswith("_lr") else d), dtype=torch.bfloat16, device=device)
+           for n in names}
+    R = projection_matrix(wl).to(device) if wl.planted_locality else None
+    nbh = torch.from_numpy(_neighbourhood_of_token(wl.latent)).to(device) if wl.planted_locality else None
+    for i, h in enumerate(heads):
+        g = torch.Generator(device=device)
+        g.manual_seed(wl.seed + 7919 * (b * wl.H + h))
+        normal = lambda shape: torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        if not wl.planted_locality:
+            x = {"q": normal((N, d)).to(torch.bfloat16), "k": normal((N, d)).to(torch.bfloat16),
+                 "v": normal((N, d)).to(torch.bfloat16), "do": normal((N, d)).to(torch.bfloat16)}
+            for n in ("q_lr", "k_lr"):
+                x[n] = torch.randint(-wl.lr_max, wl.lr_max + 1, (N, r), generator=g, device=device,
+                                     dtype=torch.int32).to(torch.bfloat16)
+        else:
+            q = normal((N, d)).to(torch.bfloat16)
+            k0 = normal((N, d))
+            e = normal((int(nbh.max()) + 1, d))
+            k = (k0 + 2.0 * e[nbh]).to(torch.bfloat16)
+            x = {"q": q, "k": k, "v": normal((N, d)).to(torch.bfloat16), "do": normal((N, d)).to(torch.bfloat16)}
+            lim = float(wl.lr_max)
+            x["q_lr"] = torch.clamp(torch.round(0.5 * (q.float() @ R)), -lim, lim).to(torch.bfloat16)
+            x["k_lr"] = torch.clamp(torch.round(0.5 * (k.float() @ R)), -lim, lim).to(torch.bfloat16)
+        for n in names:
+            torch.index_select(x[n], 0, perm, out=out[n][0, i])
+        del x
+    return out

@@ -1,5 +1,6 @@
 """Host-side input generation: token layout and seeded draws (CPU only)."""
 import numpy as np
+import pytest
 import torch
 
 from dynamic_sparse_attention_estimate_gb300.inputs import (
@@ -83,3 +84,16 @@ def test_adaln_draws_are_seeded_shaped_and_spread_per_token():
     assert float(x.mean(dim=-1).std()) > 0.5
     assert set(ADALN_WORKLOADS) == {"short", "wide"}
     assert all(D % 8 == 0 for (_, _, D) in ADALN_WORKLOADS.values())
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_device_draw_follows_the_host_recipe(name):
+    """make_inputs_on_device runs the host recipe step for step: given the host's generator it
+    reproduces make_inputs exactly (on a GPU only the generator's numbers differ)."""
+    from dynamic_sparse_attention_estimate_gb300.inputs import make_inputs_on_device
+    wl = WORKLOADS[name]
+    heads = [0, 1] if name == "tiny" else [3]
+    a = make_inputs(wl, heads=heads)
+    b = make_inputs_on_device(wl, torch.device("cpu"), heads=heads)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
