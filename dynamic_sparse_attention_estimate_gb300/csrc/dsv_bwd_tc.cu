@@ -19,11 +19,14 @@
 // end); warps 12 and 15 gather with cp.async, warp 12 Q, dO and the chunks' K rows, warp 15
 // their V rows, into separate rings (V is free after dP, K only after dQ); one thread of warp
 // 13 issues the MMAs
-// in a fixed order, each group as soon as its inputs are there; one thread of warp 14 sends
-// each chunk's staged rows out as one bulk copy (d = 64; at d = 128 the readout warps copy
-// their half rows themselves).  Buffering across chunks: dV_c / dK_c in two TMEM buffers and
-// two staging buffers (d = 64), so that readout and stores of chunk c overlap the MMAs of
-// chunk c + 1.  Every wait is bounded.
+// in a fixed order, each group as soon as its inputs are there.  Partial rows leave shared
+// memory through the tensor memory accelerator (bulk copies, no load/store-unit work): at d = 64
+// one thread of warp 14 sends each chunk's staged rows (32 KB) as one copy from two alternating
+// staging buffers; at d = 128 each readout warp sends its own 32 rows (16 KB) as soon as it has
+// staged them, and waits for that copy to have read its staging rows before it stages the next
+// chunk.  dV_c / dK_c sit in two TMEM buffers at d = 64 (one at d = 128, released as soon as the
+// readout has loaded it), so that readout and stores of chunk c overlap the MMAs of chunk c + 1.
+// Every wait is bounded.
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -43,14 +46,16 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
 template <int D>
 struct Sm {
   static constexpr int KST = D == 64 ? 4 : 2;         // K stages (held until dQ)
-  static constexpr int VST = 2;                       // V stages (held until dP)
+  static constexpr int VST = D == 64 ? 2 : 1;         // V stages (held until dP, which is issued
+                                                      // a chunk ahead of the gradients)
   static constexpr int NPDS = 1;                      // P / dS tile pairs
-  static constexpr int NST = D == 64 ? 2 : 1;         // staging buffers (d = 64: the store warps
-                                                      // drain one while the other fills)
+  static constexpr int NST = D == 64 ? 2 : 1;         // staging buffers (d = 64: the store thread
+                                                      // drains one while the other fills; d = 128:
+                                                      // each readout warp sends its own rows)
   static constexpr int NDVK = D == 64 ? 2 : 1;       // dV_c / dK_c accumulator buffers
   static constexpr uint32_t COL_DV = kColDQ + 64;     // first buffer; buffer b at + b * 2d
-  static constexpr int ROWB = 256;                    // staging bytes per key: the whole partial
-                                                      // row (d = 64) or half of it (d = 128)
+  static constexpr int ROWB = 4 * D;                  // staging bytes per key: the whole bf16
+                                                      // partial row (dK part, then dV part)
   static constexpr int BLK = D / 64;
   static constexpr int T64 = BLK * 64 * 128;          // a [64 rows][D] tile
   static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
@@ -458,16 +463,15 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       ok_run = ok_run && tc::mbar_wait(bar(bars.dvk_full[buf]), (c / NDVK) & 1, kWaitLimit);
       tc::tc_fence_after();
       // dK (times scale) then dV, as bf16, into this key's staging row (16-byte chunks XOR-
-      // swizzled by the row, so a warp's stores hit distinct banks).  d = 64: the store warps
-      // copy the chunk's rows out; d = 128: each half row is copied out here, by the warp, two
-      // rows per store instruction.  Either way every store instruction writes whole rows.
-      // The TMEM load of the next 32 columns is in flight while the current ones are converted.
+      // swizzled by the partial row index, so a warp's stores hit distinct banks; the reduction
+      // undoes it).  d = 64: the store thread copies the chunk's rows out; d = 128: the warp's
+      // elected lane copies the warp's rows out.  The TMEM load of the next 32 columns is in
+      // flight while the current ones are converted.
       const uint32_t cdv = S::COL_DV + buf * 2 * D;
       const int sb = kStoreWarps ? (c & 1) : 0;  // staging buffer
       const uint32_t srow = sbase + S::OFF_ST + sb * (kChunk * S::ROWB) + te * S::ROWB;
       const uint32_t swarp = sbase + S::OFF_ST + (te & ~31) * S::ROWB;
       constexpr int NPART = 2 * D / 32;             // 32-column parts: dK columns first, then dV
-      constexpr int PARTS_PER_COPY = S::ROWB / 64;  // parts (64 bytes each) per staging fill
       auto part_col = [&](int part) -> uint32_t {
         return part < D / 32 ? cdv + D + part * 32 : cdv + (part - D / 32) * 32;
       };
@@ -480,10 +484,14 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       const int64_t prow_index = prow0 + static_cast<int64_t>(c) * kChunk + te;
       if (pos >= 0) p.lists[pos] = static_cast<int32_t>(prow_index);
       // 16-byte chunk q of the row is staged at q ^ swz: distinct for 8 consecutive keys (no
-      // bank conflicts); d = 64 keys it on the partial row index, which the reduction undoes
-      const int swz = kStoreWarps ? static_cast<int>(prow_index & 7) : (te & 7);
+      // bank conflicts), keyed on the partial row index, which the reduction undoes
+      const int swz = static_cast<int>(prow_index & 7);
       if (kStoreWarps && c >= 2)  // the bulk copy has read this buffer's previous chunk
         ok_run = ok_run && tc::mbar_wait(bar(bars.st_empty[sb]), ((c >> 1) - 1) & 1, kWaitLimit);
+      if (!kStoreWarps && c >= 1) {  // this warp's copy of the previous chunk has read its rows
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+      }
 #pragma unroll
       for (int part = 0; part < NPART; ++part) {
         const int cur = part & 1;
@@ -497,37 +505,36 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16x2(__uint_as_float(r[cur][i >> 3][(2 * i) & 15]) * mult,
                              __uint_as_float(r[cur][i >> 3][(2 * i + 1) & 15]) * mult);
-        const int base_chunk = (part % PARTS_PER_COPY) * 4;  // 16-byte chunks within the staging row
+        const int base_chunk = part * 4;  // 16-byte chunks within the staging row
 #pragma unroll
         for (int v = 0; v < 4; ++v)
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((base_chunk + v) ^ swz) << 4)),
                        "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3]));
-        if (!kStoreWarps && part % PARTS_PER_COPY == PARTS_PER_COPY - 1) {
-          __syncwarp();
-          const int half_off = (part / PARTS_PER_COPY) * (S::ROWB / 2);  // bf16 elements into the row
-          const int chunk = lane & 15, rsel = lane >> 4;
-#pragma unroll
-          for (int rr = 0; rr < 32; rr += 2) {  // the warp's 32 rows are consecutive partial rows
-            const int row = rr + rsel;
-            const int64_t slot = static_cast<int64_t>(c) * kChunk + (te & ~31) + row;
-            uint4 val;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(swarp + row * S::ROWB + ((chunk ^ (row & 7)) << 4)));
-            if (slot < kk)
-              *reinterpret_cast<uint4*>(p.partial + (prow0 + slot) * (2 * D) +
-                                        half_off + chunk * 8) = val;
-          }
-          __syncwarp();
-        }
         if (part + 1 < NPART) tmem_wait_ld_into(r[cur ^ 1]);
+        if (part + 2 == NPART) {  // every TMEM load of this chunk has completed: release the buffer
+          tc::tc_fence_before();
+          tc::mbar_arrive(bar(bars.dvk_empty[buf]));
+        }
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(bar(bars.dvk_empty[buf]));
+      if (NPART < 2) {
+        tc::tc_fence_before();
+        tc::mbar_arrive(bar(bars.dvk_empty[buf]));
+      }
+      tc::fence_async_shared();  // staged rows visible to the bulk copy
       if (kStoreWarps) {
-        tc::fence_async_shared();  // staged rows visible to the bulk copy
         tc::mbar_arrive(bar(bars.st_full[sb]));
+      } else {
+        // the warp's 32 rows are consecutive partial rows: one bulk copy (16 KB) by one lane
+        __syncwarp();
+        const int64_t wslot = static_cast<int64_t>(c) * kChunk + (te & ~31);
+        const int64_t nr = kk - wslot < 32 ? kk - wslot : 32;
+        if (lane == 0 && nr > 0)
+          bulk_store(p.partial + (prow0 + wslot) * (2 * D), swarp, static_cast<uint32_t>(nr * S::ROWB));
       }
+    }
+    if (!kStoreWarps) {  // the rows are written before the CTA ends
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
     // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
     ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);

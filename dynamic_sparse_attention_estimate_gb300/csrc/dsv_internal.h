@@ -95,8 +95,8 @@ struct BwdParams {
   int32_t* lists;      // [pairs]        partial row of each key-major position: key j's rows in
                        //                ascending query-block order
   bf16* partial;       // [pairs][2 d]   BLOCK-major rows (CTA c's k rows at c k): dK part times the
-                       //                scale, then dV part (bf16; summed in fp32); at d = 64 the
-                       //                16-byte chunks of row n are stored XOR (n & 7)
+                       //                scale, then dV part (bf16; summed in fp32); the 16-byte
+                       //                chunks of row n are stored XOR (n & 7)
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
 };
 // parts: kBwdPrep (bitmaps, prefix, scan: reads idx only), kBwdFinish (main kernel and reduce on
