@@ -17,8 +17,10 @@
 // on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
 // dK_c out of TMEM into shared-memory staging rows and write the key lists (and dQ at the
 // end); warps 12 and 15 gather with cp.async, warp 12 Q, dO and the chunks' K rows, warp 15
-// their V rows, into separate rings (V is free after dP, K only after dQ); one thread of warp
-// 13 issues the MMAs
+// (with warp 14 at d = 128, each taking half of a chunk's rows) their V rows, into separate
+// rings (V is free after dP, K only after dQ; random-row gathers run at the rate of the loads
+// the issuing warps keep in flight, and the single V stage at d = 128 is on the critical path);
+// one thread of warp 13 issues the MMAs
 // in a fixed order, each group as soon as its inputs are there.  Partial rows leave shared
 // memory through the tensor memory accelerator (bulk copies, no load/store-unit work): at d = 64
 // one thread of warp 14 sends each chunk's staged rows (32 KB) as one copy from two alternating
@@ -42,6 +44,10 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 // TMEM columns: S^T, dP^T, dQ^T (64 each), then dV_c, dK_c (d each) in one buffer (d = 128)
 // or two (d = 64: the MMAs of the next chunk fill one while the partial rows leave the other)
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
+
+// V producer warps: 15, and 14 at d = 128 (at d = 64 warp 14 sends the partial rows)
+template <int D>
+constexpr int kVProducers = D == 128 ? 2 : 1;
 
 template <int D>
 struct Sm {
@@ -169,7 +175,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   if (tid == 0) {
     for (int s = 0; s < 4; ++s) {
       tc::mbar_init(bar(bars.full_k[s]), 32);
-      tc::mbar_init(bar(bars.full_v[s]), 32);
+      tc::mbar_init(bar(bars.full_v[s]), 32 * kVProducers<D>);
       tc::mbar_init(bar(bars.empty_k[s]), 1);
       tc::mbar_init(bar(bars.empty_v[s]), 1);
     }
@@ -222,11 +228,14 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   // d = 64: a chunk's staged partial rows leave as one bulk copy (block-major rows are
   // contiguous); d = 128 stages half rows, which the readout warps copy out themselves
   constexpr bool kStoreWarps = D == 64;
-  if (warp == 12 || warp == 15) {
+  if (warp == 12 || warp == 15 || (kVProducers<D> == 2 && warp == 14)) {
     // ================================================================ producers (cp.async)
-    // warp 12 gathers Q, dO and the chunks' K rows, warp 15 the V rows: one issuing warp
-    // cannot keep both rings fed.  Each ring's "landed" barrier counts its copies.
+    // warp 12 gathers Q, dO and the chunks' K rows; the V producers (warp 15; warps 15 and 14
+    // at d = 128) the V rows, producer v taking the 32-row groups v, v + NV, ....  Each ring's
+    // "landed" barrier counts its copies.
     const bool is_k = warp == 12;
+    const int NPR = is_k ? 1 : kVProducers<D>;
+    const int pidx = is_k || warp == 15 ? 0 : 1;
     if (is_k) {
       copy_rows<D>(sQ, 64, 64, p.q, [&](int r) -> int64_t { return row0 + r; }, lane);
       copy_rows<D>(sDO, 64, 64, p.d_o, [&](int r) -> int64_t { return row0 + r; }, lane);
@@ -239,7 +248,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
-        rr[h] = (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
+        rr[h] = (c < nchunks && slot < kk && (h % NPR) == pidx) ? __ldg(ib + slot) : -1;
       }
     };
     load_rows(0, nxt);
@@ -257,14 +266,19 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       constexpr int LPR = D / 8, RPI = 32 / LPR;
       const int sub = lane % LPR, rsub = lane / LPR;
       const uint32_t dst = ring + st * S::KV;
+      const int e = sub * 8;
 #pragma unroll
-      for (int it = 0; it < kChunk / RPI; ++it) {
-        const int row = it * RPI + rsub;
-        const int32_t j = __shfl_sync(0xffffffffu, cur[(it * RPI) >> 5], row & 31);
-        const bool ok = j >= 0 && j < N;
-        const int e = sub * 8;
-        cp_async_16(dst + (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63),
-                    src_head + (ok ? static_cast<int64_t>(j) : 0) * D + e, ok);
+      for (int h = 0; h < 4; ++h) {
+        if ((h % NPR) != pidx) continue;  // uniform over the warp
+#pragma unroll
+        for (int it = 0; it < 32 / RPI; ++it) {
+          const int rg = it * RPI + rsub;
+          const int row = 32 * h + rg;
+          const int32_t j = __shfl_sync(0xffffffffu, cur[h], rg);
+          const bool ok = j >= 0 && j < N;
+          cp_async_16(dst + (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63),
+                      src_head + (ok ? static_cast<int64_t>(j) : 0) * D + e, ok);
+        }
       }
       cp_async_arrive(bar(is_k ? bars.full_k[st] : bars.full_v[st]));
     }
