@@ -734,38 +734,32 @@ def dsv_arm(args):
         except Exception as exc:  # a comparator only
             dense = {"error": str(exc)[:200]}
 
-    # ---- this library at density 100 % (k = N: idx = every key, ascending) on the same shape: the
-    # sparse kernels run as a dense attention (only where k = N fits: idx and partial rows grow as N^2)
+    # ---- this library at density 100 % (k = N: every key selected) on the same shape: its dense path
+    # (key-stationary dK / dV, no idx, no partial rows), one head for the long shapes, scaled
     own_dense = None
     if side and not args.no_dense:
-        if wl.N > 131072:
-            own_dense = {"skipped": f"k = N at N = {wl.N} needs {4 * wl.NB * wl.N / 1e9:.0f} GB of idx and "
-                                    f"{4 * wl.d * wl.NB * wl.N / 1e12:.1f} TB of partial rows per head"}
-        else:
-            try:
-                kd = wl.N
-                hpc = step.hpc
-                idx_d = torch.empty((wl.B, hpc, wl.NB, kd), dtype=torch.int32, device=dev)
-                dims_d = make_dims(wl.B, hpc, wl.N, wl.d, wl.r, kd)
-                ws_d = torch.empty(min(dsv_sparse_attn_bwd_workspace(dims_d), int(args.ws_gib * GIB)),
-                                   dtype=torch.uint8, device=dev)
-                h0, nh = step.groups[0]
+        try:
+            heads = 1 if wl.N > 65536 else step.hpc
+            sl1 = lambda t: t[:, :heads]
+            ws_d = torch.empty(max(1, dsv_sparse_attn_bwd_workspace(make_dims(wl.B, heads, wl.N, wl.d, wl.r, wl.N))),
+                               dtype=torch.uint8, device=dev)
 
-                def own_dense_step():
-                    dsv_estimate_topk(sl(g["q_lr"], h0, nh), sl(g["k_lr"], h0, nh), kd, idx=idx_d)
-                    dsv_sparse_attn_fwd(sl(g["q"], h0, nh), sl(g["k"], h0, nh), sl(g["v"], h0, nh), idx_d,
-                                        out=(sl(outs["o"], h0, nh), sl(outs["lse"], h0, nh)))
-                    dsv_sparse_attn_bwd(*(sl(g[n], h0, nh) for n in ("do", "q", "k", "v")), sl(outs["o"], h0, nh),
-                                        sl(outs["lse"], h0, nh), idx_d, workspace=ws_d,
-                                        out=tuple(sl(outs[n], h0, nh) for n in ("dq", "dk", "dv")))
-                own_dense_step()
-                t_od = timed(own_dense_step, 3) * len(step.groups)
-                own_dense = {"ms": t_od, "tflops": 14.0 * BH * wl.N * wl.N * wl.d / (t_od / 1e3) / 1e12,
-                             "impl": "this library with k = N (idx = arange), estimate + forward + backward",
-                             "scaled": f"one group of {nh} heads x{len(step.groups)}" if len(step.groups) > 1 else None}
-                del idx_d, ws_d
-            except Exception as exc:  # a comparator only
-                own_dense = {"error": str(exc)[:200]}
+            def own_dense_step():
+                dsv_sparse_attn_fwd(sl1(g["q"]), sl1(g["k"]), sl1(g["v"]), None,
+                                    out=(sl1(outs["o"]), sl1(outs["lse"])))
+                dsv_sparse_attn_bwd(*(sl1(g[n]) for n in ("do", "q", "k", "v")), sl1(outs["o"]), sl1(outs["lse"]),
+                                    None, workspace=ws_d, out=tuple(sl1(outs[n]) for n in ("dq", "dk", "dv")))
+            own_dense_step()
+            t_od = timed(own_dense_step, 2 if wl.N > 65536 else 5) * (wl.H / heads)
+            dense_flop = 14.0 * BH * wl.N * wl.N * wl.d
+            own_dense = {"ms": t_od, "tflops": dense_flop / (t_od / 1e3) / 1e12, "heads_timed": heads,
+                         "impl": "this library at k = N: forward without idx, dense dK/dV kernel + dQ-only main kernel",
+                         "scaled": f"x{wl.H / heads:g} to the step's {wl.H} heads" if heads != wl.H else None}
+            if dense and "ms" in dense:
+                own_dense["vs_fastest_sdpa"] = dense["ms"] / t_od
+            del ws_d
+        except Exception as exc:  # a comparator only
+            own_dense = {"error": str(exc)[:200]}
         check_status("the dense comparison")
 
     adaptive = None

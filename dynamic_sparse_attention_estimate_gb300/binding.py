@@ -29,7 +29,7 @@ EXPORTED = (
     "dsv_estimate_mass_k", "dsv_estimate_topk_csr", "dsv_sparse_attn_fwd_csr",
     "dsv_sparse_attn_bwd_csr_workspace", "dsv_sparse_attn_bwd_csr", "dsv_csr_launch_order",
     "dsv_adaln_fwd", "dsv_adaln_bwd_workspace", "dsv_adaln_bwd",
-    "dsv_sparse_attn_bwd_prepare", "dsv_sparse_attn_bwd_prepared",
+    "dsv_sparse_attn_bwd_prepare", "dsv_sparse_attn_bwd_prepared", "dsv_sparse_attn_fwd_workspace",
 )
 
 
@@ -50,7 +50,7 @@ class AdalnDims(ctypes.Structure):
 
 
 def library_path() -> str:
-    return os.environ.get("DSV_LIBRARY", os.path.join(_HERE, _LIB_NAME))
+    return os.environ.get("DSV_LIBRARY") or os.path.join(_HERE, _LIB_NAME)
 
 
 def load_library(path: Optional[str] = None):
@@ -68,8 +68,10 @@ def load_library(path: Optional[str] = None):
     lib.dsv_estimate_topk_workspace.restype = sz
     lib.dsv_estimate_topk.argtypes = [dp, vp, vp, vp, vp, sz, vp]
     lib.dsv_estimate_topk.restype = st
-    lib.dsv_sparse_attn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
+    lib.dsv_sparse_attn_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.dsv_sparse_attn_fwd.restype = st
+    lib.dsv_sparse_attn_fwd_workspace.argtypes = [dp]
+    lib.dsv_sparse_attn_fwd_workspace.restype = sz
     lib.dsv_sparse_attn_bwd_workspace.argtypes = [dp]
     lib.dsv_sparse_attn_bwd_workspace.restype = sz
     lib.dsv_sparse_attn_bwd_workspace_min.argtypes = [dp]
@@ -223,14 +225,23 @@ def dsv_estimate_topk_csr(q_lr: torch.Tensor, k_lr: torch.Tensor, k_row: torch.T
     return cols
 
 
-def dsv_sparse_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, block: int = 64,
-                        scale: Optional[float] = None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
-    """(O bf16 [B,H,N,d], LSE fp32 [B,H,N]) of softmax attention over the selected keys."""
+def dsv_sparse_attn_fwd_workspace(dims: Dims) -> int:
+    return int(load_library().dsv_sparse_attn_fwd_workspace(ctypes.byref(dims)))
+
+
+def dsv_sparse_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: Optional[torch.Tensor], block: int = 64,
+                        scale: Optional[float] = None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
+                        workspace: Optional[torch.Tensor] = None):
+    """(O bf16 [B,H,N,d], LSE fp32 [B,H,N]) of softmax attention over the selected keys.  Without a
+    workspace argument the workspace the library asks for (for key passes) is allocated here."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 4)
-    _need(idx, "idx", torch.int32, 4)
     B, H, N, d = q.shape
-    kk = idx.shape[3]
+    if idx is None:   # every key selected (k = N): the dense path, which reads no idx
+        kk = N
+    else:
+        _need(idx, "idx", torch.int32, 4)
+        kk = idx.shape[3]
     dims = make_dims(B, H, N, d, 0, kk, block, scale)
     if out is None:
         o = torch.empty_like(q)
@@ -238,8 +249,12 @@ def dsv_sparse_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: 
     else:
         o, lse = out
     lib = load_library()
+    if workspace is None:
+        nbytes = int(lib.dsv_sparse_attn_fwd_workspace(ctypes.byref(dims)))
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     _check(lib.dsv_sparse_attn_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
-                                   _stream_ptr(q)), "dsv_sparse_attn_fwd")
+                                   _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream_ptr(q)),
+           "dsv_sparse_attn_fwd")
     return o, lse
 
 
@@ -250,15 +265,18 @@ def dsv_sparse_attn_bwd_workspace(dims: Dims, minimum: bool = False) -> int:
 
 
 def dsv_sparse_attn_bwd(do: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
-                        lse: torch.Tensor, idx: torch.Tensor, block: int = 64, scale: Optional[float] = None,
+                        lse: torch.Tensor, idx: Optional[torch.Tensor], block: int = 64, scale: Optional[float] = None,
                         workspace: Optional[torch.Tensor] = None, out=None):
     """(dQ, dK, dV) bf16 [B,H,N,d]; dK/dV reduced deterministically per key."""
     for t, n in ((do, "do"), (q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _need(t, n, torch.bfloat16, 4)
     _need(lse, "lse", torch.float32, 3)
-    _need(idx, "idx", torch.int32, 4)
     B, H, N, d = q.shape
-    kk = idx.shape[3]
+    if idx is None:   # every key selected (k = N): the dense backward, which reads no idx
+        kk = N
+    else:
+        _need(idx, "idx", torch.int32, 4)
+        kk = idx.shape[3]
     dims = make_dims(B, H, N, d, 0, kk, block, scale)
     lib = load_library()
     if workspace is None:

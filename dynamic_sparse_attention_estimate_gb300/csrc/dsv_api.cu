@@ -300,14 +300,19 @@ dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const v
   return ok();
 }
 
+// The forward needs no scratch at present (its workspace arguments are reserved).
+size_t fwd_workspace_bytes(const dsv_dims*) { return 0; }
+
 dsv_status fwd_impl(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
-                    const int64_t* rowptr, const int32_t* order, void* o, float* lse, void* stream) {
+                    const int64_t* rowptr, const int32_t* order, void* o, float* lse, void* ws, size_t ws_bytes,
+                    void* stream) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
+  if (ws && !aligned16(ws)) return fail(DSV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
   DSV_NEED_PTR(q);
   DSV_NEED_PTR(k);
   DSV_NEED_PTR(v);
-  DSV_NEED_PTR(idx);
+  if (rowptr || dims->k != dims->N) DSV_NEED_PTR(idx);  // k = N: every key, idx is not read
   DSV_NEED_PTR(o);
   DSV_NEED_PTR(lse);
   unsigned int* status = nullptr;
@@ -328,31 +333,43 @@ dsv_status fwd_impl(const dsv_dims* dims, const void* q, const void* k, const vo
   p.status = status;
   p.rowptr = rowptr;
   p.order = order;
+  (void)ws_bytes;
   cudaError_t e = dsv::launch_sparse_fwd_tc(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return ok();
 }
 
+size_t dsv_sparse_attn_fwd_workspace(const dsv_dims* dims) {
+  if (check_dims(dims, true, false) != DSV_OK) return 0;
+  return fwd_workspace_bytes(dims);
+}
+
 dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
-                               void* o, float* lse, void* stream) {
-  return fwd_impl(dims, q, k, v, idx, nullptr, nullptr, o, lse, stream);
+                               void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return fwd_impl(dims, q, k, v, idx, nullptr, nullptr, o, lse, ws, ws_bytes, stream);
 }
 
 dsv_status dsv_sparse_attn_fwd_csr(const dsv_dims* dims, const void* q, const void* k, const void* v,
                                    const int64_t* rowptr, const int32_t* cols, const int32_t* order, void* o,
                                    float* lse, void* stream) {
   if (!rowptr) return fail(DSV_ERR_INVALID_ARG, "rowptr is NULL");
-  return fwd_impl(dims, q, k, v, cols, rowptr, order, o, lse, stream);
+  return fwd_impl(dims, q, k, v, cols, rowptr, order, o, lse, nullptr, 0, stream);
 }
+
+// k = N (every key selected): the dense backward needs only D = rowsum(dO o O) per query row;
+// no partial rows at all.
+size_t dense_bwd_bytes(const dsv_dims* d) { return up(sizeof(float) * static_cast<size_t>(d->B * d->H * d->N)); }
 
 size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims) {
   if (check_dims(dims, true, false) != DSV_OK) return 0;
+  if (dims->k == dims->N) return dense_bwd_bytes(dims);
   WavePlan w{1, 1, dims->N / 64 > 1};
   return plan_bytes(dims, w);
 }
 
 size_t dsv_sparse_attn_bwd_workspace(const dsv_dims* dims) {
   if (check_dims(dims, true, false) != DSV_OK) return 0;
+  if (dims->k == dims->N) return dense_bwd_bytes(dims);
   // the largest plan whose partial rows stay within the recommended budget
   const size_t per_block = sizeof(uint16_t) * 2 * dims->d * dims->k;
   const int64_t BH = dims->B * dims->H, NB = dims->N / 64;
@@ -378,7 +395,7 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
                     size_t ws_bytes, void* stream, int parts = dsv::kBwdAll) {
   dsv_status s = check_dims(dims, true, false);
   if (s != DSV_OK) return s;
-  DSV_NEED_PTR(idx);
+  if (rowptr || dims->k != dims->N) DSV_NEED_PTR(idx);  // k = N: every key, idx is not read
   if (parts & dsv::kBwdFinish) {
     DSV_NEED_PTR(d_o);
     DSV_NEED_PTR(q);
@@ -392,6 +409,41 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
   }
   if (!ws) return fail(DSV_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (!rowptr && dims->k == dims->N) {
+    // every key selected: the dense backward (dK, dV key-stationary; dQ query-centric), which
+    // reads no idx and writes no partial rows; the split backward's first part has nothing to do
+    const size_t need = dense_bwd_bytes(dims);
+    if (ws_bytes < need)
+      return fail(DSV_ERR_WORKSPACE, "workspace of %zu bytes is below the %zu the dense backward needs", ws_bytes, need);
+    if (parts == dsv::kBwdPrep) return ok();
+    unsigned int* status = nullptr;
+    if ((s = status_word(&status)) != DSV_OK) return s;
+    dsv::BwdParams p{};
+    p.d_o = static_cast<const dsv::bf16*>(d_o);
+    p.q = static_cast<const dsv::bf16*>(q);
+    p.k = static_cast<const dsv::bf16*>(k);
+    p.v = static_cast<const dsv::bf16*>(v);
+    p.o = static_cast<const dsv::bf16*>(o);
+    p.lse = lse;
+    p.idx = idx;
+    p.dq = static_cast<dsv::bf16*>(dq);
+    p.dk = static_cast<dsv::bf16*>(dk);
+    p.dv = static_cast<dsv::bf16*>(dv);
+    p.BH = dims->B * dims->H;
+    p.N = dims->N;
+    p.NB = dims->N / dims->block;
+    p.topk = dims->k;
+    p.d = static_cast<int>(dims->d);
+    p.scale = eff_scale(dims);
+    p.status = status;
+    p.dense = true;
+    float* delta = static_cast<float*>(ws);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dsv::launch_dense_dkdv(p, delta, st);
+    if (e == cudaSuccess) e = dsv::launch_bwd_main_tc(p, dsv::BwdWave{0, p.BH, 0, p.NB, true, true}, 1, st);
+    if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "dense backward launch: %s", cudaGetErrorString(e));
+    return ok();
+  }
   WavePlan plan;
   if (rowptr) {
     plan = WavePlan{dims->B * dims->H, dims->N / 64, false};

@@ -16,11 +16,7 @@
 // Roles (512 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
 // on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
 // dK_c out of TMEM into shared-memory staging rows and write the key lists (and dQ at the
-// end); warps 12 and 15 gather with cp.async, warp 12 Q, dO and the chunks' K rows, warp 15
-// (with warp 14 at d = 128, each taking half of a chunk's rows) their V rows, into separate
-// rings (V is free after dP, K only after dQ; random-row gathers run at the rate of the loads
-// the issuing warps keep in flight, and the single V stage at d = 128 is on the critical path);
-// one thread of warp 13 issues the MMAs
+// end); one thread of warp 13 issues the MMAs
 // in a fixed order, each group as soon as its inputs are there.  Partial rows leave shared
 // memory through the tensor memory accelerator (bulk copies, no load/store-unit work): at d = 64
 // one thread of warp 14 sends each chunk's staged rows (32 KB) as one copy from two alternating
@@ -29,6 +25,17 @@
 // chunk.  dV_c / dK_c sit in two TMEM buffers at d = 64 (one at d = 128, released as soon as the
 // readout has loaded it), so that readout and stores of chunk c overlap the MMAs of chunk c + 1.
 // Every wait is bounded.
+// Gathers.  Random-row gathers run at the rate of the copies the issuing warps keep in flight
+// (measured here: 256-byte rows out of L2 at about 3.8 TB/s over the GPU with one issuing warp
+// per SM, 14 TB/s with four), and a stage can be refilled the moment its last reader is done.
+// So the warps that learn of that moment first issue the copies, each for its own rows: the
+// compute warps gather chunk c + 1's V rows (16 each) right after reading S^T / dP^T of chunk c
+// (dP of chunk c was the last reader of the stage), and the readout warps gather chunk
+// c + KST's K rows (32 each) as soon as dQ of chunk c has read its stage (and, before the first
+// chunk, Q, dO and the first K stages).  Each ring's "landed" barrier counts its copies.
+// Dense blocks (k = N, the DENSE instantiation): chunk c holds keys 128 c .. 128 c + 127 and
+// no idx is read; the kernel computes dQ only (no dV_c / dK_c products, no partial rows): dK and
+// dV of dense blocks come from the key-stationary kernel of dsv_dense_bwd.cu.
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 #include "dsv_tc.cuh"
@@ -44,10 +51,6 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 // TMEM columns: S^T, dP^T, dQ^T (64 each), then dV_c, dK_c (d each) in one buffer (d = 128)
 // or two (d = 64: the MMAs of the next chunk fill one while the partial rows leave the other)
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
-
-// V producer warps: 15, and 14 at d = 128 (at d = 64 warp 14 sends the partial rows)
-template <int D>
-constexpr int kVProducers = D == 128 ? 2 : 1;
 
 template <int D>
 struct Sm {
@@ -114,24 +117,28 @@ DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
-// Copy `nrows` rows of D bf16 (rows given by row_of(i)) into a 128-byte-swizzled tile of
-// `tile_rows` rows; LPR lanes per row so each warp-wide copy moves whole rows.
-template <int D, typename RowFn>
-DSV_DEVICE void copy_rows(uint32_t dst, int tile_rows, int nrows, const bf16* base, RowFn row_of, int lane) {
+// NROWS rows of a 128-byte-swizzled [TILE_ROWS][D] tile, starting at tile row row0, gathered with
+// cp.async from the head's rows: tile row row0 + i takes source row j = the key held by lane
+// key_lane0 + i of this warp (j outside [0, N): zeros).  LPR lanes per row, so each warp-wide
+// copy moves whole rows and every 32-byte sector is fetched once.
+template <int D, int NROWS, int TILE_ROWS = kChunk>
+DSV_DEVICE void gather_rows(uint32_t tile, const bf16* head, int32_t my_key, int key_lane0, int row0, int lane,
+                            int64_t N) {
   constexpr int LPR = D / 8, RPI = 32 / LPR;
-  const int sub = lane % LPR, rsub = lane / LPR;
-  for (int r0 = 0; r0 < nrows; r0 += RPI) {
-    const int row = r0 + rsub;
-    const int64_t src_row = row_of(row);
-    const int e = sub * 8;
-    cp_async_16(dst + (e >> 6) * (tile_rows * 128) + tc::sw128(row, e & 63), base + (src_row < 0 ? 0 : src_row) * D + e,
-                src_row >= 0);
+  const int sub = lane % LPR, rsub = lane / LPR, e = sub * 8;
+  const uint32_t dcol = tile + (e >> 6) * (TILE_ROWS * 128);  // 64-column blocks are TILE_ROWS rows apart
+#pragma unroll
+  for (int it = 0; it < NROWS / RPI; ++it) {
+    const int i = it * RPI + rsub;
+    const int32_t j = __shfl_sync(0xffffffffu, my_key, key_lane0 + i);
+    const bool ok = j >= 0 && j < N;
+    cp_async_16(dcol + tc::sw128(row0 + i, e & 63), head + (ok ? static_cast<int64_t>(j) : 0) * D + e, ok);
   }
 }
 
 // CSR: per-block key counts from row offsets (and an optional launch order); otherwise k for
 // every block, compiled without those loads.
-template <int D, bool CSR>
+template <int D, bool CSR, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32, float scale_log2) {
   using S = Sm<D>;
@@ -151,7 +158,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   // this block's keys: k of them (or its CSR row), and its first partial row in the wave
   const int64_t grow = bh * NB + blk;
   const int64_t kk = CSR ? p.rowptr[grow + 1] - p.rowptr[grow] : p.topk;
-  const int32_t* ib = p.idx + (CSR ? p.rowptr[grow] : grow * p.topk);
+  const int32_t* ib = DENSE ? nullptr : p.idx + (CSR ? p.rowptr[grow] : grow * p.topk);
+  // the key at slot i (dense: the key position itself)
+  auto key_at = [&](int64_t i) -> int32_t { return DENSE ? static_cast<int32_t>(i) : __ldg(ib + i); };
   const int64_t prow0 = CSR ? p.rowptr[grow] - p.rowptr[bh0 * NB + blk0] : cta_row * kk;
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
   if (CSR && nchunks == 0) {  // a block with no keys: dQ = 0 (uniform for the CTA, before any barrier)
@@ -174,8 +183,8 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   }
   if (tid == 0) {
     for (int s = 0; s < 4; ++s) {
-      tc::mbar_init(bar(bars.full_k[s]), 32);
-      tc::mbar_init(bar(bars.full_v[s]), 32 * kVProducers<D>);
+      tc::mbar_init(bar(bars.full_k[s]), 128);   // the 4 readout warps' copies
+      tc::mbar_init(bar(bars.full_v[s]), 256);   // the 8 compute warps' copies
       tc::mbar_init(bar(bars.empty_k[s]), 1);
       tc::mbar_init(bar(bars.empty_v[s]), 1);
     }
@@ -227,63 +236,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   constexpr int NDVK = S::NDVK, NPDS = S::NPDS;
   // d = 64: a chunk's staged partial rows leave as one bulk copy (block-major rows are
   // contiguous); d = 128 stages half rows, which the readout warps copy out themselves
-  constexpr bool kStoreWarps = D == 64;
-  if (warp == 12 || warp == 15 || (kVProducers<D> == 2 && warp == 14)) {
-    // ================================================================ producers (cp.async)
-    // warp 12 gathers Q, dO and the chunks' K rows; the V producers (warp 15; warps 15 and 14
-    // at d = 128) the V rows, producer v taking the 32-row groups v, v + NV, ....  Each ring's
-    // "landed" barrier counts its copies.
-    const bool is_k = warp == 12;
-    const int NPR = is_k ? 1 : kVProducers<D>;
-    const int pidx = is_k || warp == 15 ? 0 : 1;
-    if (is_k) {
-      copy_rows<D>(sQ, 64, 64, p.q, [&](int r) -> int64_t { return row0 + r; }, lane);
-      copy_rows<D>(sDO, 64, 64, p.d_o, [&](int r) -> int64_t { return row0 + r; }, lane);
-    }
-    const bf16* src_head = (is_k ? p.k : p.v) + bh * N * D;
-    const int NS = is_k ? KST : VST;
-    const uint32_t ring = is_k ? sK : sV;
-    int32_t nxt[4];
-    auto load_rows = [&](int c, int32_t (&rr)[4]) {
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
-        rr[h] = (c < nchunks && slot < kk && (h % NPR) == pidx) ? __ldg(ib + slot) : -1;
-      }
-    };
-    load_rows(0, nxt);
-    bool ok_run = true;
-    for (int c = 0; c < nchunks && ok_run; ++c) {
-      const int st = c % NS;
-      int32_t cur[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) cur[h] = nxt[h];
-      load_rows(c + 1, nxt);
-      if (c >= NS)
-        ok_run = tc::mbar_wait(bar(is_k ? bars.empty_k[st] : bars.empty_v[st]), ((c / NS) - 1) & 1, kWaitLimit);
-      ok_run = __all_sync(0xffffffffu, ok_run);
-      if (!ok_run) break;
-      constexpr int LPR = D / 8, RPI = 32 / LPR;
-      const int sub = lane % LPR, rsub = lane / LPR;
-      const uint32_t dst = ring + st * S::KV;
-      const int e = sub * 8;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        if ((h % NPR) != pidx) continue;  // uniform over the warp
-#pragma unroll
-        for (int it = 0; it < 32 / RPI; ++it) {
-          const int rg = it * RPI + rsub;
-          const int row = 32 * h + rg;
-          const int32_t j = __shfl_sync(0xffffffffu, cur[h], rg);
-          const bool ok = j >= 0 && j < N;
-          cp_async_16(dst + (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63),
-                      src_head + (ok ? static_cast<int64_t>(j) : 0) * D + e, ok);
-        }
-      }
-      cp_async_arrive(bar(is_k ? bars.full_k[st] : bars.full_v[st]));
-    }
-    cp_async_wait<0>();
-    if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
+  constexpr bool kStoreWarps = D == 64 && !DENSE;
+  if (warp == 12 || warp == 15) {
+    // idle
   } else if (warp == 13) {
     // ================================================================ MMA issue (one thread)
     if (lane == 0) {
@@ -307,26 +262,28 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         tc::mma_commit(bar(bars.s_full));
         tc::mma_commit(bar(bars.empty_v[c % VST]));
       };
-      // dV_c, dK_c, then the dQ^T update of chunk c
+      // the dQ^T update of chunk c, then dV_c, dK_c (so the K stage frees first)
       auto issue_grads = [&](int c) {
         tc::tc_fence_after();
         const uint32_t cdv = S::COL_DV + (c % NDVK) * 2 * D;
         const uint32_t sP = sPDS + (c % NPDS) * 2 * S::P, sDS = sP + S::P;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {  // K = 64 queries
-          tc::mma_ss(tmem + cdv, tc::smem_desc(sP + j * 32, 16, 1024), tc::smem_desc(sDO + j * 2048, 64 * 128, 1024),
-                     idKV, j > 0 ? 1u : 0u);
-          tc::mma_ss(tmem + cdv + D, tc::smem_desc(sDS + j * 32, 16, 1024),
-                     tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
-        }
-        tc::mma_commit(bar(bars.dvk_full[c % NDVK]));
         const uint32_t aK = sK + (c % KST) * S::KV;
 #pragma unroll
         for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
           tc::mma_ss(tmem + kColDQ, tc::smem_desc(aK + j * 2048, kChunk * 128, 1024),
                      tc::smem_desc(sDS + j * 2048, 8192, 1024), idQ, (c > 0 || j > 0) ? 1u : 0u);
+        tc::mma_commit(bar(bars.empty_k[c % KST]));  // the K stage is free once dQ^T has read it
+        if (!DENSE) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // K = 64 queries
+            tc::mma_ss(tmem + cdv, tc::smem_desc(sP + j * 32, 16, 1024), tc::smem_desc(sDO + j * 2048, 64 * 128, 1024),
+                       idKV, j > 0 ? 1u : 0u);
+            tc::mma_ss(tmem + cdv + D, tc::smem_desc(sDS + j * 32, 16, 1024),
+                       tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bars.dvk_full[c % NDVK]));
+        }
         tc::mma_commit(bar(bars.pds_empty[c % NPDS]));
-        tc::mma_commit(bar(bars.empty_k[c % KST]));
         if (c == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
       };
       // Fixed issue order S(0), then per chunk c: S(c+1), grads(c).  S(c+1) needs only the
@@ -346,7 +303,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
           issue_s(c + 1);
         }
         ok_run = tc::mbar_wait(bar(bars.p_full[c % NPDS]), (c / NPDS) & 1, kWaitLimit) &&
-                 (c < NDVK || tc::mbar_wait(bar(bars.dvk_empty[c % NDVK]), ((c / NDVK) - 1) & 1, kWaitLimit));
+                 (DENSE || c < NDVK || tc::mbar_wait(bar(bars.dvk_empty[c % NDVK]), ((c / NDVK) - 1) & 1, kWaitLimit));
         if (!ok_run) break;
         issue_grads(c);
       }
@@ -362,12 +319,17 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     const int hq = tid >> 7;          // query columns [32 hq, 32 hq + 32)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok_run = true;
-    int32_t jnext = t < kk ? __ldg(ib + t) : -1;
+    int32_t jnext = t < kk ? key_at(t) : -1;
+    // this warp's 16 V rows of each chunk: rows 32 (warp & 3) + 16 hq + i, keys in lanes 16 hq + i
+    const bf16* vhead = p.v + bh * N * D;
+    const int vrow0 = 32 * (warp & 3) + 16 * hq;
+    gather_rows<D, 16>(sV, vhead, jnext, 16 * hq, vrow0, lane, N);  // chunk 0
+    cp_async_arrive(bar(bars.full_v[0]));
     for (int c = 0; c < nchunks; ++c) {
       const bool valid = jnext >= 0 && jnext < N;
       {
         const int64_t slot = static_cast<int64_t>(c + 1) * kChunk + t;
-        jnext = slot < kk ? __ldg(ib + slot) : -1;
+        jnext = slot < kk ? key_at(slot) : -1;
       }
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full), c & 1, kWaitLimit);
       tc::tc_fence_after();
@@ -380,6 +342,12 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty));
+      if (c + 1 < nchunks) {  // chunk c + 1's V rows: its stage's last reader, dP, is done or nearly
+        const int sv = (c + 1) % VST;
+        if (c + 1 >= VST) ok_run = ok_run && tc::mbar_wait(bar(bars.empty_v[sv]), ((c + 1) / VST - 1) & 1, kWaitLimit);
+        gather_rows<D, 16>(sV + sv * S::KV, vhead, jnext, 16 * hq, vrow0, lane, N);
+        cp_async_arrive(bar(bars.full_v[sv]));
+      }
       uint32_t pw[16], dw[16];  // packed bf16 pairs of P and dS
 #pragma unroll
       for (int i4 = 0; i4 < 8; ++i4) {
@@ -416,6 +384,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.p_full[pb]));
     }
+    cp_async_wait<0>();
     if (!ok_run) atomicOr(&fail_s, 1);
   } else if (warp == 14) {
     // ================================================================ partial-row stores (d = 64)
@@ -448,7 +417,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     const uint32_t lowmask = (1u << (lb & 31)) - 1u;
     auto key_of = [&](int c) -> int32_t {
       const int64_t slot = static_cast<int64_t>(c) * kChunk + te;
-      return (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
+      return (c < nchunks && slot < kk) ? key_at(slot) : -1;
     };
     // a key's partial row: offsets[j] + (blocks of this wave before this one that selected j);
     // the three loads are issued one chunk before the row is needed
@@ -466,10 +435,30 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       return q;
     };
-    PosParts pos_next = pos_load(key_of(0));
-    int32_t j_next2 = key_of(1);
+    // Q and dO (16 rows each per warp) and the first KST K stages (32 rows per warp)
+    const int wr = warp - 8;
+    const bf16* khead = p.k + bh * N * D;
+    {
+      const int32_t qkey = static_cast<int32_t>(blk * 64) + 16 * wr + (lane & 15);
+      gather_rows<D, 16, 64>(sQ, p.q + bh * N * D, qkey, 0, 16 * wr, lane, N);  // [64 rows][D] tiles
+      gather_rows<D, 16, 64>(sDO, p.d_o + bh * N * D, qkey, 0, 16 * wr, lane, N);
+      for (int s0 = 0; s0 < KST && s0 < nchunks; ++s0) {
+        gather_rows<D, 32>(sK + s0 * S::KV, khead, key_of(s0), 0, 32 * wr, lane, N);
+        cp_async_arrive(bar(bars.full_k[s0]));
+      }
+    }
+    PosParts pos_next = pos_load(DENSE ? -1 : key_of(0));
+    int32_t j_next2 = DENSE ? -1 : key_of(1);
     bool ok_run = true;
     for (int c = 0; c < nchunks; ++c) {
+      // chunk c + KST's K rows, into chunk c's stage once dQ of chunk c has read it
+      if (c + KST < nchunks) {
+        const int32_t kkey = key_of(c + KST);
+        ok_run = ok_run && tc::mbar_wait(bar(bars.empty_k[c % KST]), (c / KST) & 1, kWaitLimit);
+        gather_rows<D, 32>(sK + (c % KST) * S::KV, khead, kkey, 0, 32 * wr, lane, N);
+        cp_async_arrive(bar(bars.full_k[c % KST]));
+      }
+      if (DENSE) continue;  // dense: no partial rows, dQ only
       const int64_t pos = pos_next.valid ? pos_next.off + pos_next.pre + __popc(pos_next.bits & lowmask) : -1;
       pos_next = pos_load(j_next2);
       j_next2 = key_of(c + 2);
@@ -550,6 +539,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       if (lane == 0) bulk_wait_all();
       __syncwarp();
     }
+    cp_async_wait<0>();  // the K copies this warp issued have landed
     // ---- dQ = scale * (dQ^T)^T, through a shared-memory transpose
     ok_run = ok_run && tc::mbar_wait(bar(bars.dq_full), 0, kWaitLimit);
     if (!ok_run) atomicOr(&fail_s, 1);
@@ -565,12 +555,14 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         tc::tmem_wait_ld();
         if (dim >= 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) stage[(h * 16 + i) * D + dim] = __float2bfloat16_rn(__uint_as_float(r[i]) * p.scale);
+          for (int i = 0; i < 16; ++i)
+            stage[(h * 16 + i) * D + dim] = __float2bfloat16_rn(__uint_as_float(r[i]) * p.scale);
         }
       }
       sync_group(2);
       bf16* dqb = p.dq + row0 * D;
-      for (int i = te; i < 64 * D / 8; i += 128) reinterpret_cast<uint4*>(dqb)[i] = reinterpret_cast<const uint4*>(stage)[i];
+      for (int i = te; i < 64 * D / 8; i += 128)
+        reinterpret_cast<uint4*>(dqb)[i] = reinterpret_cast<const uint4*>(stage)[i];
     }
   }
   tc::tc_fence_before();
@@ -585,7 +577,8 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
 template <int D>
 cudaError_t launch_d(const BwdParams& p, const BwdWave& w, int64_t W32, cudaStream_t stream) {
   const int smem = Sm<D>::TOTAL;
-  auto kern = p.rowptr ? sparse_bwd_tc_kernel<D, true> : sparse_bwd_tc_kernel<D, false>;
+  auto kern = p.rowptr ? sparse_bwd_tc_kernel<D, true, false>
+                       : (p.dense ? sparse_bwd_tc_kernel<D, false, true> : sparse_bwd_tc_kernel<D, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ProfScope prof("bwd_main", stream);

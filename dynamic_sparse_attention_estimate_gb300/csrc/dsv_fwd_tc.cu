@@ -7,16 +7,21 @@
 //     O^T[d x 64 q]        += V_c^T . P^T         (tcgen05, M=d,   N=64, K=128)
 // so both products keep M = 128 although a block has 64 queries (for d = 64 the PV operand
 // carries an extra row of ones that yields the softmax row sums; see kOnesRow).
-// Roles (192 threads):
+// Roles (192 threads at d = 64, 288 at d = 128):
 //   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
 //              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16, one 128-byte
 //              row) to shared memory as the B operand of the PV product;
-//   warp 4     producer: gathers the chunk's K and V rows with cp.async (16 bytes per
-//              copy, into 128-byte-swizzled tiles) into a ring of stages and lets the stage's
-//              mbarrier count the copies' completion (cp.async.mbarrier.arrive), so it never
-//              waits for its own copies; keys past k or out of range are zero-filled;
-//   warp 5     one thread issues every MMA as soon as its inputs are ready (it polls the
-//              stage, P and S barriers without blocking on any single one).
+//   warp 4     producer (with warps 6-8 at d = 128, each taking 32 of a chunk's rows):
+//              gathers the chunk's K and V rows with cp.async (16 bytes per copy, into
+//              128-byte-swizzled tiles) into a ring of stages and lets the stage's mbarrier
+//              count the copies' completion (cp.async.mbarrier.arrive), so it never waits for
+//              its own copies; keys past k or out of range are zero-filled;
+//   warp 5     one thread issues every MMA as soon as its inputs are ready: it waits in the
+//              hardware, for a short bounded time, on the barrier of the product that comes
+//              next in the usual order (the PV product of the oldest chunk with an S^T), and
+//              checks the other between waits, so neither order of readiness stalls it.
+// Dense blocks (every key selected, k = N): the DENSE instantiation reads no idx; chunk c holds
+// keys 128 c .. 128 c + 127 (contiguous rows, the same arithmetic otherwise).
 // The running max m_q is kept STALE: a chunk only triggers the cross-thread column max and
 // an O/L rescale when one of its logits exceeds m_q by more than 8 (in log2 units; the
 // first chunk always does).  Otherwise P <= 2^8, and softmax is invariant to the
@@ -31,10 +36,19 @@ namespace dsv {
 namespace {
 
 constexpr int kChunk = 128;
-constexpr int kThreads = 192;
+// Producer warps per CTA.  Gathers of random rows are bound by the loads a warp keeps in
+// flight: measured on this GPU, one issuing warp per SM moves about 3.8 TB/s of 256-byte rows
+// out of L2 over the whole GPU, four move about 14 TB/s.  At d = 128 (one CTA per SM) four warps
+// gather, each 32 of a chunk's 128 rows; at d = 64 (two CTAs per SM, registers for 192 threads
+// each) one warp per CTA.  Producers are warp 4 and warps 6, 7, 8.
+template <int D>
+constexpr int kProducers = D == 128 ? 4 : 1;
+template <int D>
+constexpr int kThreadsFor = 160 + 32 * kProducers<D>;
+DSV_DEVICE int producer_index(int warp) { return warp == 4 ? 0 : (warp >= 6 ? warp - 5 : -1); }
 constexpr float kStaleLimit = 8.f;  // log2 units
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kPollLimit = 1u << 28;
+constexpr uint32_t kPollLimit = 1u << 24;  // rounds of bounded waits before giving up
 
 // TMEM columns
 constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kColL = 192, kTmemCols = 256;
@@ -88,6 +102,17 @@ DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Wait for the phase with the given parity to complete, suspended in the hardware for at most
+// about `ns` nanoseconds (returns false if it has not completed by then).
+DSV_DEVICE bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Arrive on `bar` once all cp.async copies this thread issued so far have landed.
 DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
@@ -138,8 +163,8 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
 
 // CSR: per-block key counts from row offsets (and an optional launch order); otherwise k for
 // every block, compiled without those loads.
-template <int D, int NST, int MINB, bool CSR>
-__global__ void __launch_bounds__(kThreads, MINB)
+template <int D, int NST, int MINB, bool CSR, bool DENSE>
+__global__ void __launch_bounds__(kThreadsFor<D>, MINB)
 sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr,
                      const int32_t* __restrict__ order, bf16* __restrict__ o,
@@ -163,14 +188,16 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   const int64_t kk = CSR ? rowptr[grow + 1] - rowptr[grow] : k_uniform;
   const int nchunks = static_cast<int>((kk + kChunk - 1) / kChunk);
   if (CSR && nchunks == 0) {  // a block with no keys: O = 0, LSE = -inf (uniform for the CTA, before any barrier)
-    for (int i = tid; i < 64 * D / 8; i += kThreads)
+    for (int i = tid; i < 64 * D / 8; i += kThreadsFor<D>)
       reinterpret_cast<uint4*>(o + (bh * N + blk * 64) * D)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < 64) lse[bh * N + blk * 64 + tid] = -CUDART_INF_F;
     return;
   }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V, sP = sbase + S::OFF_P;
-  const int32_t* ib = idx + (CSR ? rowptr[grow] : grow * k_uniform);
+  const int32_t* ib = DENSE ? nullptr : idx + (CSR ? rowptr[grow] : grow * k_uniform);
+  // the key at slot i (dense: the key position itself)
+  auto key_at = [&](int64_t i) -> int32_t { return DENSE ? static_cast<int32_t>(i) : __ldg(ib + i); };
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
   // the 128-byte swizzle of TMA and of the MMA descriptors both follow address bits, so the
@@ -185,7 +212,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   }
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
-      tc::mbar_init(bar(bars.full[s]), 32);
+      tc::mbar_init(bar(bars.full[s]), 32 * kProducers<D>);
       tc::mbar_init(bar(bars.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -211,58 +238,67 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  if (warp == 4) {
-    // ================================================================ producer (cp.async)
-    // lane l copies rows l, l + 32, l + 64, l + 96 of each chunk (whole rows, 16 bytes a copy)
+  if (producer_index(warp) >= 0) {
+    // ================================================================ producers (cp.async)
+    // Producer p copies the row groups g = p, p + NP, ... (rows 32 g .. 32 g + 31) of each chunk;
+    // lane l holds the key index of row 32 g + l.  Whole rows, 16 bytes a copy.
+    constexpr int NP = kProducers<D>, NG = 4 / NP;  // row groups per producer
+    const int pidx = producer_index(warp);
     const bf16* qb = q + (bh * N + blk * 64) * D;
     const bf16* kh = k + bh * N * D;
     const bf16* vh = v + bh * N * D;
+    if (pidx == 0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int row = lane + 32 * h;
+      for (int h = 0; h < 2; ++h) {
+        const int row = lane + 32 * h;
 #pragma unroll
-      for (int e = 0; e < D; e += 8)
-        cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
+        for (int e = 0; e < D; e += 8)
+          cp_async_16(sQ + (e >> 6) * (64 * 128) + tc::sw128(row, e & 63), qb + row * D + e, true);
+      }
     }
     bool ok_run = true;
-    int32_t nxt[4];
-    auto load_rows = [&](int c, int32_t (&rr)[4]) {
+    int32_t nxt[NG];
+    auto load_rows = [&](int c, int32_t (&rr)[NG]) {
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
-        rr[h] = (c < nchunks && slot < kk) ? __ldg(ib + slot) : -1;
+      for (int h = 0; h < NG; ++h) {
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + 32 * (pidx + NP * h) + lane;
+        rr[h] = (c < nchunks && slot < kk) ? key_at(slot) : -1;
       }
     };
     load_rows(0, nxt);
     for (int c = 0; c < nchunks && ok_run; ++c) {
       const int st = c % NST;
-      int32_t cur[4];
+      int32_t cur[NG];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) cur[h] = nxt[h];
+      for (int h = 0; h < NG; ++h) cur[h] = nxt[h];
       load_rows(c + 1, nxt);
       if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / NST) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
       const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {  // validity of the rows this lane holds the index of
-        const int64_t slot = static_cast<int64_t>(c) * kChunk + lane + 32 * h;
+      for (int h = 0; h < NG; ++h) {  // validity of the rows this lane holds the index of
+        const int64_t slot = static_cast<int64_t>(c) * kChunk + 32 * (pidx + NP * h) + lane;
         if (slot < kk && !(cur[h] >= 0 && cur[h] < N)) flag_status(status, kStatusBadIndex);
       }
       // each warp-wide copy covers whole rows: LPR lanes per row (8 for d = 64, 16 for d = 128),
       // so every 32-byte sector is fetched once; a row's index comes from the lane holding it
       constexpr int LPR = D / 8, RPI = 32 / LPR;
       const int sub = lane % LPR, rsub = lane / LPR;
+      const int e = sub * 8;
 #pragma unroll
-      for (int it = 0; it < kChunk / RPI; ++it) {
-        const int row = it * RPI + rsub;
-        const int32_t j = __shfl_sync(0xffffffffu, cur[(it * RPI) >> 5], row & 31);
-        const bool ok = j >= 0 && j < N;
-        const int e = sub * 8;
-        const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
-        const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
-        cp_async_16(dK + off, kh + src, ok);
-        cp_async_16(dV + off, vh + src, ok);
+      for (int h = 0; h < NG; ++h) {
+#pragma unroll
+        for (int it = 0; it < 32 / RPI; ++it) {
+          const int rg = it * RPI + rsub;                       // row within the group
+          const int row = 32 * (pidx + NP * h) + rg;
+          const int32_t j = __shfl_sync(0xffffffffu, cur[h], rg);
+          const bool ok = j >= 0 && j < N;
+          const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
+          const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
+          cp_async_16(dK + off, kh + src, ok);
+          cp_async_16(dV + off, vh + src, ok);
+        }
       }
       cp_async_arrive(bar(bars.full[st]));
     }
@@ -278,7 +314,9 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       int cs = 0, cp = 0;
       uint32_t idle = 0;
       while (ok_run && cp < nchunks) {
-        if (cp < cs && mbar_test(bar(bars.p_full[cp & 1]), (cp >> 1) & 1)) {
+        // the usual next product is PV(cp) once S(cp) exists; otherwise S(cs)
+        const bool pv_next = cp < cs;
+        if (pv_next && mbar_try_wait_ns(bar(bars.p_full[cp & 1]), (cp >> 1) & 1, 64)) {
           // PV(cp): O^T += V_c^T P^T
           tc::tc_fence_after();
           const uint32_t aV = sV + (cp % NST) * S::KV_BYTES, bP = sP + (cp & 1) * S::P_BYTES;
@@ -294,7 +332,9 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
           ++cp;
           idle = 0;
-        } else if (cs < nchunks && mbar_test(bar(bars.full[cs % NST]), (cs / NST) & 1) &&
+        } else if (cs < nchunks &&
+                   (pv_next ? mbar_test(bar(bars.full[cs % NST]), (cs / NST) & 1)
+                            : mbar_try_wait_ns(bar(bars.full[cs % NST]), (cs / NST) & 1, 64)) &&
                    (cs < 2 || mbar_test(bar(bars.s_empty[cs & 1]), ((cs - 2) >> 1) & 1))) {
           // S(cs): S^T = K_c Q^T.  The stage was written with cp.async (generic proxy):
           // order those writes before the tensor core's reads.
@@ -311,9 +351,8 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           tc::mma_commit(bar(bars.s_full[cs & 1]));
           ++cs;
           idle = 0;
-        } else {
-          if (++idle > kPollLimit) ok_run = false;
-          __nanosleep(32);  // nothing ready: yield issue slots to the softmax warps
+        } else if (++idle > kPollLimit) {
+          ok_run = false;
         }
       }
       if (!ok_run) atomicOr(&fail_s, 1);
@@ -330,13 +369,13 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     const int t = tid;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok_run = true;
-    int32_t jnext = t < kk ? __ldg(ib + t) : -1;  // this lane's key index, one chunk ahead
+    int32_t jnext = t < kk ? key_at(t) : -1;  // this lane's key index, one chunk ahead
     for (int c = 0; c < nchunks; ++c) {
       const int b = c & 1;
       const bool valid = jnext >= 0 && jnext < N;
       {
         const int64_t slot = static_cast<int64_t>(c + 1) * kChunk + t;
-        jnext = slot < kk ? __ldg(ib + slot) : -1;
+        jnext = slot < kk ? key_at(slot) : -1;
       }
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full[b]), (c >> 1) & 1, kWaitLimit);
       tc::tc_fence_after();
@@ -480,6 +519,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       // O^T lane -> head dim (M = 128: lane = row; lanes 64.. of the d = 64 product are the
       // row sums and the zero rows of the ones tile)
       const int dim = t < D ? t : -1;
+      const int64_t qrow0 = bh * N + blk * 64;
       bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D]: K stage 0 is free now
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
@@ -496,12 +536,12 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         }
       }
       named_sync_softmax();
-      bf16* ob = o + (bh * N + blk * 64) * D;
+      bf16* ob = o + qrow0 * D;
       for (int i = t; i < 64 * D / 8; i += 128)
         reinterpret_cast<uint4*>(ob)[i] = reinterpret_cast<const uint4*>(stage)[i];
       if (t < 64) {
         const float l = red_s[t];
-        lse[bh * N + blk * 64 + t] = l > 0.f ? (m_s[t] + __log2f(l)) * kLn2 : -CUDART_INF_F;
+        lse[qrow0 + t] = l > 0.f ? (m_s[t] + __log2f(l)) * kLn2 : -CUDART_INF_F;
       }
     }
   }
@@ -525,13 +565,17 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 template <int D, int NST, int MINB>
 cudaError_t launch_d(const FwdParams& p, cudaStream_t stream) {
   const int smem = Smem<D, NST>::TOTAL;
-  auto kern = p.rowptr ? sparse_fwd_tc_kernel<D, NST, MINB, true> : sparse_fwd_tc_kernel<D, NST, MINB, false>;
+  // k = N without CSR rows: every block attends to every key, in key order; idx is not read
+  const bool dense = !p.rowptr && p.topk == p.N;
+  auto kern = p.rowptr ? sparse_fwd_tc_kernel<D, NST, MINB, true, false>
+                       : (dense ? sparse_fwd_tc_kernel<D, NST, MINB, false, true>
+                                : sparse_fwd_tc_kernel<D, NST, MINB, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.NB), static_cast<unsigned>(p.BH));
   ProfScope prof("sparse_fwd", stream);
-  kern<<<grid, kThreads, smem, stream>>>(p.q, p.k, p.v, p.idx, p.rowptr, p.order, p.o, p.lse, p.N, p.NB, p.topk,
-                                         p.scale * kLog2e, p.status);
+  kern<<<grid, kThreadsFor<D>, smem, stream>>>(p.q, p.k, p.v, p.idx, p.rowptr, p.order, p.o, p.lse, p.N, p.NB, p.topk,
+                                               p.scale * kLog2e, p.status);
   return cudaGetLastError();
 }
 

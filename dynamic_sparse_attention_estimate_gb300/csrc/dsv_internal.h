@@ -98,7 +98,11 @@ struct BwdParams {
                        //                scale, then dV part (bf16; summed in fp32); the 16-byte
                        //                chunks of row n are stored XOR (n & 7)
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
+  bool dense = false;       // k = N: the main kernel computes dQ only, no idx read, no partial rows
 };
+// Dense blocks (k = N): D_i = dO_i . O_i into delta [BH][N], then dK and dV of every key tile
+// accumulated over all query blocks (dsv_dense_bwd.cu); dQ from launch_bwd_main_tc with dense set.
+cudaError_t launch_dense_dkdv(const BwdParams& p, float* delta, cudaStream_t stream);
 // parts: kBwdPrep (bitmaps, prefix, scan: reads idx only), kBwdFinish (main kernel and reduce on
 // a workspace the prep filled), or both
 constexpr int kBwdPrep = 1, kBwdFinish = 2, kBwdAll = 3;

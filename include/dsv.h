@@ -126,17 +126,24 @@ dsv_status dsv_csr_launch_order(const dsv_dims* dims, const int64_t* rowptr, int
 dsv_status dsv_estimate_topk_csr(const dsv_dims* dims, const void* q_lr, const void* k_lr, const int32_t* k_row,
                                  const int64_t* rowptr, int32_t* cols, void* stream);
 
+/* Bytes of device workspace dsv_sparse_attn_fwd needs: 0 for every shape at present (the
+ * workspace arguments are reserved, so that a future forward may take scratch without an ABI
+ * change). */
+size_t dsv_sparse_attn_fwd_workspace(const dsv_dims* dims);
+
 /*
  * Sparse attention forward over the selected keys (DSV Spanish summary section 3:
  * sparse attention kernels; page 1 section 2A: only the critical KV pairs are used).
  * For query i of block b:  l_ij = scale * Q_i . K_j for j in idx[b];
  *   LSE_i = max_j l_ij + ln sum_j exp(l_ij - max_j l_ij);  O_i = sum_j exp(l_ij - LSE_i) V_j.
  * q, k, v: bf16 [B][H][N][d].  idx: int32 [B][H][N/block][k], entries in [0, N)
- * (need not be sorted here).  o: bf16 [B][H][N][d] (output).  lse: fp32 [B][H][N]
- * (output, natural log).  Accumulation in fp32.
+ * (need not be sorted here).  With k = N every key is selected and idx is not read (the
+ * dense path; idx may then be NULL).  o: bf16 [B][H][N][d] (output).  lse: fp32 [B][H][N] (output, natural log).
+ * Accumulation in fp32.  ws, ws_bytes: a device workspace of at least
+ * dsv_sparse_attn_fwd_workspace(dims) bytes (NULL and 0 while that is 0), 16-byte aligned.
  */
 dsv_status dsv_sparse_attn_fwd(const dsv_dims* dims, const void* q, const void* k, const void* v,
-                               const int32_t* idx, void* o, float* lse, void* stream);
+                               const int32_t* idx, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* Recommended / minimum device workspace for dsv_sparse_attn_bwd.  With more
  * workspace the backward processes more query blocks per wave (fewer launches). */
@@ -153,7 +160,11 @@ size_t dsv_sparse_attn_bwd_workspace_min(const dsv_dims* dims);
  * The entries of one idx row must be distinct (dsv_estimate_topk writes them strictly
  * ascending); a repeated or out-of-range entry sets the device status word.
  * dK/dV are reduced per key in ascending query-block order from per-(block, key)
- * partial rows held in the workspace: deterministic, no float atomics.
+ * partial rows held in the workspace: deterministic, no float atomics.  With k = N (every key
+ * selected: the pages' dense case) idx is not read and no partial rows exist: dK and dV of each
+ * tile of 128 keys accumulate on chip over all query blocks in block order, dQ per query block
+ * (idx may then be NULL);
+ * the workspace then holds only D = rowsum(dO o O) (4 bytes per query row).
  * d_o, q, k, v, o: bf16 [B][H][N][d]; lse fp32 [B][H][N]; idx int32 [B][H][N/block][k];
  * dq, dk, dv: bf16 [B][H][N][d] (outputs).  ws: device workspace of ws_bytes >=
  * dsv_sparse_attn_bwd_workspace_min(dims), 256-byte aligned.
@@ -194,10 +205,12 @@ dsv_status dsv_sparse_attn_bwd_prepared(const dsv_dims* dims, const void* d_o, c
  *     above DSV_NOALLOC_SCRATCH_BYTES are rejected with DSV_ERR_WORKSPACE before anything
  *     runs; larger problems that fit are processed in several waves.  The smallest plan takes
  *     one query block per wave and chains a head's waves through an fp32 accumulator of
- *     8 d N bytes, next to k bf16 partial rows of 4 d bytes, so at d = 128 and k = N the limit
- *     is about N = 21,000 tokens per head (about N = 43,000 at d = 64); a head whose partial
- *     rows all fit (N/64 * k * 4 d bytes plus its rank structure) needs no accumulator.  The
- *     long-video shape (N = 520,192) is rejected: use dsv_sparse_attn_bwd there.
+ *     8 d N bytes, next to k bf16 partial rows of 4 d bytes, so at d = 128 and the largest
+ *     sparse k (N - 1) the limit is about N = 21,000 tokens per head (about N = 43,000 at
+ *     d = 64); a head whose partial rows all fit (N/64 * k * 4 d bytes plus its rank structure)
+ *     needs no accumulator, and k = N (the dense backward) needs only 4 bytes per query row.
+ *     The long-video
+ *     shape (N = 520,192, k = 52,019) is rejected: use dsv_sparse_attn_bwd there.
  *   - The first call on a device looks up that device's address of the array (with the
  *     device current); make that first call before any stream capture.
  *   - All calls share the one array, which keeps whatever the last call left there (every

@@ -53,7 +53,7 @@ def test_status_strings(lib):
 
 def _call_fwd(lib, dims, ptr=0x1000):
     p = ctypes.c_void_p(ptr)
-    return lib.dsv_sparse_attn_fwd(ctypes.byref(dims), p, p, p, p, p, p, None)
+    return lib.dsv_sparse_attn_fwd(ctypes.byref(dims), p, p, p, p, p, p, None, 0, None)
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -68,7 +68,7 @@ def test_invalid_dims_rejected_before_launch(lib, no_gpu, field, value, status):
 
 def test_null_and_misaligned_pointers_rejected(lib, no_gpu):
     dims = make_dims(1, 2, 1024, 64, 16, 128)
-    assert lib.dsv_sparse_attn_fwd(ctypes.byref(dims), None, None, None, None, None, None, None) == 1
+    assert lib.dsv_sparse_attn_fwd(ctypes.byref(dims), None, None, None, None, None, None, None, 0, None) == 1
     assert b"NULL" in lib.dsv_last_error_message()
     assert _call_fwd(lib, dims, 0x1004) == 1
     assert b"aligned" in lib.dsv_last_error_message()
@@ -159,9 +159,12 @@ def test_noalloc_rejects_a_problem_larger_than_its_scratch(lib, no_gpu):
 
 def test_noalloc_accepts_what_fits_its_scratch(lib):
     """The shapes the no-allocation backward accepts: a smallest workspace of at most 32 MiB.
-    At d = 128 with k = N (the largest k) that holds up to about N = 21,000 tokens per head."""
+    At d = 128 with the largest sparse k (N - 1) that holds up to about N = 21,000 tokens per head.
+    With k = N (every key selected) the dense backward needs only D per row (4 N bytes a head)."""
     limit = 32 << 20
-    fits = make_dims(1, 1, 20480, 128, 16, 20480)
-    too_big = make_dims(1, 1, 22528, 128, 16, 22528)
+    fits = make_dims(1, 1, 20480, 128, 16, 20479)
+    too_big = make_dims(1, 1, 22528, 128, 16, 22527)
     assert lib.dsv_sparse_attn_bwd_workspace_min(ctypes.byref(fits)) <= limit
     assert lib.dsv_sparse_attn_bwd_workspace_min(ctypes.byref(too_big)) > limit
+    dense = make_dims(1, 1, 22528, 128, 16, 22528)
+    assert lib.dsv_sparse_attn_bwd_workspace_min(ctypes.byref(dense)) == 4 * 22528

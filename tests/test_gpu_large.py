@@ -70,3 +70,4 @@ def test_density_sweep(density):
 def test_long_video_one_call_of_four_heads():
     wl = WORKLOADS["long"]
     _sampled_check(wl, heads=[0, 1, 2, 3], n_sel_blocks=64, n_attn_blocks=64)
+

@@ -90,6 +90,28 @@ def test_full_density_equals_dense_attention():
     assert_close("O vs SDPA", o, np64(ref))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_dense_path_with_a_partial_key_tile(d):
+    """k = N runs the dense backward (key tiles of 128 accumulate dK and dV on chip; dQ per query
+    block; no idx read, no partial rows).  N = 448 leaves the last key tile half full: the keys
+    past N must get no probability and no gradient row."""
+    dev = need_gpu()
+    wl = Workload("dense448", 1, 2, (7, 8, 8), d, 16, 448, None)
+    x = make_inputs(wl)
+    out = _run(_to(dev, x), wl.N)
+    _full_check(x, out, wl.N, rel_elem=EDGE_REL_ELEM)
+
+
+def test_dense_backward_repeats_bitwise():
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(2)
+    g = _to(dev, make_inputs(wl))
+    a = _run(g, wl.N)
+    b = _run(g, wl.N)
+    for name, x, y in zip(("dQ", "dK", "dV"), a[3:], b[3:]):
+        assert torch.equal(x, y), name
+
+
 def test_ties_go_to_the_lower_key_index():
     dev = need_gpu()
     wl = WORKLOADS["tiny"].with_heads(2)
