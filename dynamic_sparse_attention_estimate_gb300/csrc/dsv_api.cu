@@ -94,7 +94,7 @@ struct WavePlan {
 };
 
 struct Carve {
-  size_t colbits, colpre, count, offsets, tsum, lists, partial, acc, total;
+  size_t colbits, colpre, count, offsets, tsum, lists, partial, partial_dv, acc, total;
 };
 
 // pairs: the (block, key) pairs of the largest wave (-1: nh * nblk * k)
@@ -109,7 +109,8 @@ Carve carve(const dsv_dims* d, int64_t nh, int64_t nblk, bool sub, int64_t pairs
   c.offsets = o; o += up(sizeof(int64_t) * nh * d->N);
   c.tsum = o;    o += up(sizeof(int64_t) * nh * ((d->N + 1023) / 1024));
   c.lists = o;   o += up(sizeof(int32_t) * pairs);
-  c.partial = o; o += up(sizeof(uint16_t) * 2 * d->d * pairs);   // bf16 rows
+  c.partial = o; o += up(sizeof(uint16_t) * d->d * pairs);       // bf16 dK half-rows
+  c.partial_dv = o; o += up(sizeof(uint16_t) * d->d * pairs);    // bf16 dV half-rows
   c.acc = o;     o += sub ? up(sizeof(float) * 2 * d->d * d->N) : 0;
   c.total = o;
   return c;
@@ -487,6 +488,7 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
   p.tsum = reinterpret_cast<int64_t*>(base + c.tsum);
   p.lists = reinterpret_cast<int32_t*>(base + c.lists);
   p.partial = reinterpret_cast<dsv::bf16*>(base + c.partial);
+  p.partial_dv = reinterpret_cast<dsv::bf16*>(base + c.partial_dv);
   p.acc = plan.sub ? reinterpret_cast<float*>(base + c.acc) : nullptr;
   p.rowptr = rowptr;
   p.order = order;

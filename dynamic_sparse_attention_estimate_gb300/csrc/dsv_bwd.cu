@@ -195,7 +195,8 @@ scan_kernel(const uint32_t* __restrict__ count, const int64_t* __restrict__ tsum
 // ---------------------------------------------------------------- 5. segmented reduction per key
 // One warp per key; lane l owns columns [4 l, 4 l + 4) (and + 128 when 2 D = 256).  The key's
 // partial rows are gathered through its list (ascending query block: a fixed order), eight
-// rows in flight; the row's 16-byte chunks sit XOR (row & 7).
+// rows in flight; a row is its dK half (columns [0, D)) and its dV half (columns [D, 2 D)), in
+// two arrays, each half's 16-byte chunks XOR (row & 7).
 template <int D>
 __global__ void reduce_kernel(BwdParams p, int64_t bh0, int64_t nh, int mode /*0: write, 1: first, 2: middle, 3: last*/) {
   constexpr int W = 2 * D;       // columns per partial row
@@ -218,8 +219,10 @@ __global__ void reduce_kernel(BwdParams p, int64_t bh0, int64_t nh, int mode /*0
     auto row_ptr = [&](int32_t row, int u) -> const uint2* {
       // element offset of this lane's 4 columns [u 128 + 4 lane, + 4) within partial row `row`
       int e = u * 128 + lane * 4;
+      const bf16* half = e < D ? p.partial : p.partial_dv;
+      e = e < D ? e : e - D;
       e = ((((e >> 3) ^ (row & 7)) << 3) | (e & 7));
-      return reinterpret_cast<const uint2*>(p.partial + static_cast<int64_t>(row) * W + e);
+      return reinterpret_cast<const uint2*>(half + static_cast<int64_t>(row) * D + e);
     };
     for (int r0 = 0; r0 < cnt; r0 += 32) {
       const int32_t mine = r0 + lane < cnt ? p.lists[first + r0 + lane] : 0;

@@ -19,10 +19,11 @@
 // end); one thread of warp 13 issues the MMAs
 // in a fixed order, each group as soon as its inputs are there.  Partial rows leave shared
 // memory through the tensor memory accelerator (bulk copies, no load/store-unit work): at d = 64
-// one thread of warp 14 sends each chunk's staged rows (32 KB) as one copy from two alternating
-// staging buffers; at d = 128 each readout warp sends its own 32 rows (16 KB) as soon as it has
-// staged them, and waits for that copy to have read its staging rows before it stages the next
-// chunk.  dV_c / dK_c sit in two TMEM buffers at d = 64 (one at d = 128, released as soon as the
+// one thread of warp 14 sends each chunk's staged rows as two copies (the dK half-rows and the
+// dV half-rows, 16 KB each: they go to two arrays) from two alternating staging buffers; at
+// d = 128 each readout warp stages its 32 dK half-rows (8 KB), sends them as one copy, waits for
+// the copy to have read them, then does the same with its dV half-rows (a half-size staging
+// area, which leaves room for a third K stage).  dV_c / dK_c sit in two TMEM buffers at d = 64 (one at d = 128, released as soon as the
 // readout has loaded it), so that readout and stores of chunk c overlap the MMAs of chunk c + 1.
 // Every wait is bounded.
 // Gathers.  Random-row gathers run at the rate of the copies the issuing warps keep in flight
@@ -55,7 +56,7 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
 template <int D>
 struct Sm {
   static constexpr int KST = D == 64 ? 4 : 2;         // K stages (held until dQ)
-  static constexpr int VST = D == 64 ? 2 : 1;         // V stages (held until dP, which is issued
+  static constexpr int VST = 2;                       // V stages (held until dP, which is issued
                                                       // a chunk ahead of the gradients)
   static constexpr int NPDS = 1;                      // P / dS tile pairs
   static constexpr int NST = D == 64 ? 2 : 1;         // staging buffers (d = 64: the store thread
@@ -63,15 +64,18 @@ struct Sm {
                                                       // each readout warp sends its own rows)
   static constexpr int NDVK = D == 64 ? 2 : 1;       // dV_c / dK_c accumulator buffers
   static constexpr uint32_t COL_DV = kColDQ + 64;     // first buffer; buffer b at + b * 2d
-  static constexpr int ROWB = 4 * D;                  // staging bytes per key: the whole bf16
-                                                      // partial row (dK part, then dV part)
+  static constexpr int ROWB = 2 * D;                  // staging bytes per key: one bf16 half-row
+                                                      // (the dK part or the dV part)
+  static constexpr int STB = D == 64 ? 2 * kChunk * ROWB : kChunk * ROWB;  // bytes per staging
+                                                      // buffer: d = 64 the chunk's dK then dV
+                                                      // half-rows; d = 128 one half at a time
   static constexpr int BLK = D / 64;
   static constexpr int T64 = BLK * 64 * 128;          // a [64 rows][D] tile
   static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
   static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16
   static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + KST * KV,
                        OFF_P = OFF_V + VST * KV, OFF_ST = OFF_P + NPDS * 2 * P,  // pair b: P, then dS
-                       TOTAL = OFF_ST + NST * kChunk * ROWB;
+                       TOTAL = OFF_ST + NST * STB;
 };
 
 struct Bars {
@@ -323,8 +327,13 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
     // this warp's 16 V rows of each chunk: rows 32 (warp & 3) + 16 hq + i, keys in lanes 16 hq + i
     const bf16* vhead = p.v + bh * N * D;
     const int vrow0 = 32 * (warp & 3) + 16 * hq;
-    gather_rows<D, 16>(sV, vhead, jnext, 16 * hq, vrow0, lane, N);  // chunk 0
-    cp_async_arrive(bar(bars.full_v[0]));
+    // chunks 0 .. VST - 1 (every V stage is free); then chunk c + VST once dP of chunk c, the last
+    // reader of its stage, is done -- which is before this warp sees S^T / dP^T of chunk c
+    for (int c0 = 0; c0 < VST && c0 < nchunks; ++c0) {
+      const int64_t slot = static_cast<int64_t>(c0) * kChunk + t;
+      gather_rows<D, 16>(sV + c0 * S::KV, vhead, slot < kk ? key_at(slot) : -1, 16 * hq, vrow0, lane, N);
+      cp_async_arrive(bar(bars.full_v[c0]));
+    }
     for (int c = 0; c < nchunks; ++c) {
       const bool valid = jnext >= 0 && jnext < N;
       {
@@ -342,10 +351,12 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty));
-      if (c + 1 < nchunks) {  // chunk c + 1's V rows: its stage's last reader, dP, is done or nearly
-        const int sv = (c + 1) % VST;
-        if (c + 1 >= VST) ok_run = ok_run && tc::mbar_wait(bar(bars.empty_v[sv]), ((c + 1) / VST - 1) & 1, kWaitLimit);
-        gather_rows<D, 16>(sV + sv * S::KV, vhead, jnext, 16 * hq, vrow0, lane, N);
+      if (c + VST < nchunks) {  // chunk c + VST's V rows, into chunk c's stage (dP of chunk c is done)
+        const int sv = c % VST;
+        const int64_t slot = static_cast<int64_t>(c + VST) * kChunk + t;
+        const int32_t vkey = slot < kk ? key_at(slot) : -1;
+        ok_run = ok_run && tc::mbar_wait(bar(bars.empty_v[sv]), (c / VST) & 1, kWaitLimit);
+        gather_rows<D, 16>(sV + sv * S::KV, vhead, vkey, 16 * hq, vrow0, lane, N);
         cp_async_arrive(bar(bars.full_v[sv]));
       }
       uint32_t pw[16], dw[16];  // packed bf16 pairs of P and dS
@@ -399,8 +410,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         if (!ok_run) break;
         const int64_t row0_c = prow0 + static_cast<int64_t>(c) * kChunk;
         const int64_t nrows = kk - static_cast<int64_t>(c) * kChunk < kChunk ? kk - static_cast<int64_t>(c) * kChunk : kChunk;
-        bulk_store(p.partial + row0_c * (2 * D), sbase + S::OFF_ST + b * (kChunk * S::ROWB),
-                   static_cast<uint32_t>(nrows * S::ROWB));
+        const uint32_t sbuf = sbase + S::OFF_ST + b * S::STB;
+        bulk_store(p.partial + row0_c * D, sbuf, static_cast<uint32_t>(nrows * S::ROWB));
+        bulk_store(p.partial_dv + row0_c * D, sbuf + kChunk * S::ROWB, static_cast<uint32_t>(nrows * S::ROWB));
         bulk_wait_read();                        // the staging buffer has been read
         tc::mbar_arrive(bar(bars.st_empty[b]));
       }
@@ -472,7 +484,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       // flight while the current ones are converted.
       const uint32_t cdv = S::COL_DV + buf * 2 * D;
       const int sb = kStoreWarps ? (c & 1) : 0;  // staging buffer
-      const uint32_t srow = sbase + S::OFF_ST + sb * (kChunk * S::ROWB) + te * S::ROWB;
+      // staging half-row of this key: d = 64 row te of buffer sb's dK area (its dV area follows);
+      // d = 128 row te of the one area, dK half first, then (after its copy has read it) dV half
+      const uint32_t srow = sbase + S::OFF_ST + sb * S::STB + te * S::ROWB;
       const uint32_t swarp = sbase + S::OFF_ST + (te & ~31) * S::ROWB;
       constexpr int NPART = 2 * D / 32;             // 32-column parts: dK columns first, then dV
       auto part_col = [&](int part) -> uint32_t {
@@ -508,31 +522,43 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16x2(__uint_as_float(r[cur][i >> 3][(2 * i) & 15]) * mult,
                              __uint_as_float(r[cur][i >> 3][(2 * i + 1) & 15]) * mult);
-        const int base_chunk = part * 4;  // 16-byte chunks within the staging row
+        const bool dv_part = part >= D / 32;
+        // 16-byte chunks within the staging half-row (d = 64: the dV half-rows follow the dK area)
+        const int base_chunk = (dv_part ? part - D / 32 : part) * 4;
+        const uint32_t hrow = srow + ((kStoreWarps && dv_part) ? kChunk * S::ROWB : 0);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + (((base_chunk + v) ^ swz) << 4)),
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(hrow + (((base_chunk + v) ^ swz) << 4)),
                        "r"(w[4 * v]), "r"(w[4 * v + 1]), "r"(w[4 * v + 2]), "r"(w[4 * v + 3]));
         if (part + 1 < NPART) tmem_wait_ld_into(r[cur ^ 1]);
         if (part + 2 == NPART) {  // every TMEM load of this chunk has completed: release the buffer
           tc::tc_fence_before();
           tc::mbar_arrive(bar(bars.dvk_empty[buf]));
         }
+        if (!kStoreWarps && (part == D / 32 - 1 || part == NPART - 1)) {
+          // d = 128: the warp's 32 half-rows are consecutive: one bulk copy (8 KB) by one lane, into
+          // the dK array after the dK parts, the dV array after the dV parts; the dV parts reuse
+          // the area once the dK copy has read it
+          tc::fence_async_shared();  // staged rows visible to the bulk copy
+          __syncwarp();
+          const int64_t wslot = static_cast<int64_t>(c) * kChunk + (te & ~31);
+          const int64_t nr = kk - wslot < 32 ? kk - wslot : 32;
+          if (lane == 0 && nr > 0)
+            bulk_store((dv_part ? p.partial_dv : p.partial) + (prow0 + wslot) * D, swarp,
+                       static_cast<uint32_t>(nr * S::ROWB));
+          if (!dv_part) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+          }
+        }
       }
       if (NPART < 2) {
         tc::tc_fence_before();
         tc::mbar_arrive(bar(bars.dvk_empty[buf]));
       }
-      tc::fence_async_shared();  // staged rows visible to the bulk copy
       if (kStoreWarps) {
+        tc::fence_async_shared();  // staged rows visible to the bulk copy
         tc::mbar_arrive(bar(bars.st_full[sb]));
-      } else {
-        // the warp's 32 rows are consecutive partial rows: one bulk copy (16 KB) by one lane
-        __syncwarp();
-        const int64_t wslot = static_cast<int64_t>(c) * kChunk + (te & ~31);
-        const int64_t nr = kk - wslot < 32 ? kk - wslot : 32;
-        if (lane == 0 && nr > 0)
-          bulk_store(p.partial + (prow0 + wslot) * (2 * D), swarp, static_cast<uint32_t>(nr * S::ROWB));
       }
     }
     if (!kStoreWarps) {  // the rows are written before the CTA ends

@@ -94,9 +94,10 @@ struct BwdParams {
   int64_t* tsum;       // [nh][N / 1024] sum of count over each 1024-key tile
   int32_t* lists;      // [pairs]        partial row of each key-major position: key j's rows in
                        //                ascending query-block order
-  bf16* partial;       // [pairs][2 d]   BLOCK-major rows (CTA c's k rows at c k): dK part times the
-                       //                scale, then dV part (bf16; summed in fp32); the 16-byte
-                       //                chunks of row n are stored XOR (n & 7)
+  bf16* partial;       // [pairs][d]     BLOCK-major dK rows (CTA c's k rows at c k), times the
+                       //                scale (bf16; summed in fp32); the 16-byte chunks of row n
+                       //                are stored XOR (n & 7)
+  bf16* partial_dv;    // [pairs][d]     the matching dV rows, laid out the same way
   float* acc;          // [N][2 d]       fp32 accumulator when a head spans several waves
   bool dense = false;       // k = N: the main kernel computes dQ only, no idx read, no partial rows
 };
