@@ -10,9 +10,10 @@
 //     S^T = K_t . Q_b^T,   dP^T = V_t . dO_b^T                   (M=128, N=64,  K=d)
 //     P = exp2(S scale log2e - LSE2_b),  dS = P (dP - D_b)       (compute warps, fp32)
 //     dV_t += P^T . dO_b,  dK_t += dS^T . Q_b                     (M=128, N=d,   K=64)
-// Roles (320 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each on 32
-// of the 64 query columns; thread = key lane); warp 8 loads the key tile once and then each
-// query block's Q, dO, LSE and D into a two-stage ring with cp.async (contiguous rows); one
+// Roles (416 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each on 32
+// of the 64 query columns; thread = key lane); warps 8, 10, 11 and 12 load the key tile once and
+// then each query block's Q, dO, LSE and D into a two-stage ring with cp.async (contiguous rows,
+// a quarter of every tile per warp: one warp alone cannot keep enough loads in flight); one
 // thread of warp 9 issues the MMAs (S / dP of block b + 1 ahead of the gradients of block b,
 // into two TMEM buffers).  At the end warps 0-3 move dK (times the scale) and dV out of tensor
 // memory through shared memory and write them row by row.  Every wait is bounded.
@@ -24,7 +25,8 @@ namespace dsv {
 namespace {
 
 constexpr int kKeys = 128;     // keys per CTA (the MMA's M)
-constexpr int kThreads = 320;
+constexpr int kProducers = 4;  // warp 8 and warps 10.. copy tiles
+constexpr int kThreads = 320 + 32 * (kProducers - 1);
 constexpr int kCompute = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;
 // TMEM columns: S^T (two buffers of 64), dP^T (two of 64), dV_t (d), dK_t (d)
@@ -55,15 +57,15 @@ DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
-// rows [row0, row0 + nrows) of a [*][D] bf16 tensor into a 128-byte-swizzled tile of tile_rows rows
-// (rows >= limit are zero-filled); whole rows per warp-wide copy
+// tile rows [r_begin, r_end) of a 128-byte-swizzled tile of tile_rows rows from rows row0 + r of a
+// [*][D] bf16 tensor (rows >= limit are zero-filled); whole rows per warp-wide copy
 template <int D>
-DSV_DEVICE void copy_tile(uint32_t dst, int tile_rows, const bf16* base, int64_t row0, int nrows, int64_t limit,
-                          int lane) {
+DSV_DEVICE void copy_tile(uint32_t dst, int tile_rows, const bf16* base, int64_t row0, int r_begin, int r_end,
+                          int64_t limit, int lane) {
   constexpr int LPR = D / 8, RPI = 32 / LPR;
   const int sub = lane % LPR, rsub = lane / LPR;
   const int e = sub * 8;
-  for (int r0 = 0; r0 < nrows; r0 += RPI) {
+  for (int r0 = r_begin; r0 < r_end; r0 += RPI) {
     const int row = r0 + rsub;
     const bool ok = row0 + row < limit;
     cp_async_16(dst + (e >> 6) * (tile_rows * 128) + tc::sw128(row, e & 63), base + (ok ? row0 + row : 0) * D + e, ok);
@@ -100,9 +102,9 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar(bars.kv_full), 32);
+    tc::mbar_init(bar(bars.kv_full), 32 * kProducers);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(bar(bars.q_full[s]), 32);
+      tc::mbar_init(bar(bars.q_full[s]), 32 * kProducers);
       tc::mbar_init(bar(bars.q_empty[s]), 1);
       tc::mbar_init(bar(bars.s_full[s]), 1);
       tc::mbar_init(bar(bars.s_empty[s]), kCompute);
@@ -120,10 +122,13 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
   const uint32_t tmem = tmem_base_s;
   const int64_t hrow = bh * N;  // first row of this head
 
-  if (warp == 8) {
-    // ================================================================ producer (cp.async)
-    copy_tile<D>(sK, kKeys, k + hrow * D, key0, kKeys, N, lane);
-    copy_tile<D>(sV, kKeys, v + hrow * D, key0, kKeys, N, lane);
+  if (warp == 8 || warp >= 10) {
+    // ================================================================ producers (cp.async), each
+    // on its own quarter of every tile's rows
+    const int pr = warp == 8 ? 0 : warp - 9;
+    const int kr0 = pr * (kKeys / kProducers), qr0 = pr * (64 / kProducers);
+    copy_tile<D>(sK, kKeys, k + hrow * D, key0, kr0, kr0 + kKeys / kProducers, N, lane);
+    copy_tile<D>(sV, kKeys, v + hrow * D, key0, kr0, kr0 + kKeys / kProducers, N, lane);
     cp_async_arrive(bar(bars.kv_full));
     bool ok_run = true;
     for (int b = 0; b < NB && ok_run; ++b) {
@@ -131,12 +136,16 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
       if (b >= 2) ok_run = tc::mbar_wait(bar(bars.q_empty[st]), ((b >> 1) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
-      copy_tile<D>(sQ + st * S::T64, 64, q + hrow * D, static_cast<int64_t>(b) * 64, 64, N, lane);
-      copy_tile<D>(sDO + st * S::T64, 64, d_o + hrow * D, static_cast<int64_t>(b) * 64, 64, N, lane);
+      copy_tile<D>(sQ + st * S::T64, 64, q + hrow * D, static_cast<int64_t>(b) * 64, qr0, qr0 + 64 / kProducers, N,
+                   lane);
+      copy_tile<D>(sDO + st * S::T64, 64, d_o + hrow * D, static_cast<int64_t>(b) * 64, qr0, qr0 + 64 / kProducers,
+                   N, lane);
       // LSE and D of the block's 64 queries: 16 lanes x 16 bytes each
       const uint32_t ldst = smem_u32(ld_s + st * 128);
-      if (lane < 16) cp_async_16(ldst + lane * 16, lse + hrow + b * 64 + lane * 4, true);
-      else cp_async_16(ldst + 256 + (lane - 16) * 16, delta + hrow + b * 64 + (lane - 16) * 4, true);
+      if (pr == 0) {
+        if (lane < 16) cp_async_16(ldst + lane * 16, lse + hrow + b * 64 + lane * 4, true);
+        else cp_async_16(ldst + 256 + (lane - 16) * 16, delta + hrow + b * 64 + (lane - 16) * 4, true);
+      }
       cp_async_arrive(bar(bars.q_full[st]));
     }
     cp_async_wait<0>();
