@@ -59,6 +59,9 @@ def parse(argv=None):
     ap.add_argument("--no-adaptive", action="store_true", help="skip the mass-based selection measurement")
     ap.add_argument("--no-adaln", action="store_true", help="skip the fused AdaLN measurement")
     ap.add_argument("--no-side", action="store_true", help="skip every side measurement (dense, adaptive, AdaLN)")
+    ap.add_argument("--profile-once", action="store_true",
+                    help="run the first head group's estimate, forward and backward once, in the launch "
+                         "configuration the timed step uses, and exit (for profiler captures)")
     return ap.parse_args(argv)
 
 
@@ -260,8 +263,11 @@ KERNEL_FILES = {"estimate_topk": ("dsv_estimate.cu",), "estimate_arange": ("dsv_
 def kernel_source_hash(kernel):
     """Hash of the sources a kernel is built from: stored DRAM traffic counts only while it matches."""
     h = hashlib.sha256()
-    for f in KERNEL_FILES.get(kernel, ("dsv_bwd.cu",)) + ("dsv_common.cuh",):
-        h.update(open(os.path.join(CSRC, f), "rb").read())
+    for f in KERNEL_FILES.get(kernel, ("dsv_bwd.cu",)) + ("dsv_common.cuh", "dsv_internal.h"):
+        for ln in open(os.path.join(CSRC, f), encoding="utf-8"):
+            code = ln.split("//", 1)[0].rstrip()  # comments do not change the kernel
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
@@ -311,7 +317,9 @@ def roofline(prof, steps, wl):
     if os.path.exists(TRAFFIC_FILE):
         t = json.load(open(TRAFFIC_FILE)).get(name)
         if t and t.get("source_hash") == kernel_source_hash(name) and t.get("workload") == wl.name:
-            traffic = t["bytes_per_launch"]
+            # DRAM bytes per selected (block, key) pair of one captured launch, times this launch's pairs
+            traffic = t["bytes_per_pair"] * wl.B * wl.H * wl.NB * wl.k / (launches / steps)
+            out["traffic_source"] = t["how"]
     out["traffic"] = traffic
     if name == "bwd_main":
         # the same launches seen from HBM: every pair writes its bf16 partial row (4 d bytes) and list
@@ -529,6 +537,14 @@ def dsv_arm(args):
     def flush_l2():
         flush.zero_()
         flush_rd.sum()
+
+    if args.profile_once:
+        step.group(g, outs, 0, step.groups[0][1])
+        torch.cuda.synchronize()
+        check_status("the profiled group")
+        print(json.dumps({"profile_once": config_of(wl)["workload"], "heads": step.groups[0][1],
+                          "workspace_gib": step.ws.numel() / GIB}), flush=True)
+        return 0
 
     for _ in range(args.warmup):
         step(g, outs)

@@ -23,7 +23,7 @@
 // dV half-rows, 16 KB each: they go to two arrays) from two alternating staging buffers; at
 // d = 128 each readout warp stages its 32 dK half-rows (8 KB), sends them as one copy, waits for
 // the copy to have read them, then does the same with its dV half-rows (a half-size staging
-// area, which leaves room for a third K stage).  dV_c / dK_c sit in two TMEM buffers at d = 64 (one at d = 128, released as soon as the
+// area, which leaves room for a second V stage).  dV_c / dK_c sit in two TMEM buffers at d = 64 (one at d = 128, released as soon as the
 // readout has loaded it), so that readout and stores of chunk c overlap the MMAs of chunk c + 1.
 // Every wait is bounded.
 // Gathers.  Random-row gathers run at the rate of the copies the issuing warps keep in flight

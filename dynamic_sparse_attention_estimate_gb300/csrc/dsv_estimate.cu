@@ -5,17 +5,23 @@
 // streams every key of that head.  Scores s[b, j] = q_hat[b] . K_lr[j] live only in
 // registers: they are recomputed on each pass and never written anywhere.
 //
-// Selection is an exact radix select on the order-preserving 32-bit image of the
-// fp32 score, per query block, in shared-memory histograms:
-//   pass 1: 2048-bin histogram of bits [31:21] -> threshold bin, count above it;
-//   pass 2: 2048-bin histogram of bits [20:10] among pass-1 bin members; if all of
-//           them have zero bits [9:0] (every integer score below 2^14 does), the
-//           threshold value is now exact;
-//   pass 3 (only if needed): 1024-bin histogram of bits [9:0];
+// Selection is an exact select on the order-preserving 32-bit image ("key") of the fp32
+// score, per query block, in shared-memory histograms of 2048 bins:
+//   sample: the scores of one 512-key tile in eight, histogrammed by key bits [31:21];
+//           the sample's order statistics a few standard deviations on either side of
+//           the k-th largest give a bracket [L, H] of keys that very likely holds it;
+//   exact:  every key: those above H are counted (a register per row and thread, no
+//           atomics), those inside the bracket histogrammed in 2048 bins of 2^sh keys.
+//           If the k-th largest key lies outside the bracket the row falls back to the
+//           whole key range; if its bin holds several distinct keys the bracket narrows
+//           to that bin and the pass repeats (with integer scores below 2^13 one exact
+//           pass suffices: their keys have zero low bits);
 //   emit:   per segment of 32768 keys, bitmaps of "key > T" and "key == T" (the
 //           histogram memory is reused), then one warp per query block turns them
 //           into ascending key indices: every key > T, and the first n_tie keys == T
 //           (ties go to the lower key index).
+// The sample only decides how much work the exact passes take; the result is the exact
+// top-k whatever it holds.
 // q_hat is held as hi + lo bf16 (an exact split for |q_hat| < 2^16), so with
 // integer-valued factors every fp32 score is the exact integer.
 #include <stdint.h>
@@ -35,15 +41,19 @@ constexpr int kBins = 2048;
 constexpr int kSegKeys = 32768;                 // keys per emit segment
 constexpr int kSegWords = kSegKeys / 32;        // bitmap words per row per segment
 constexpr int kTieAll = 0x7fffffff;
+constexpr int kSampleEvery = 8;                 // the sample: one key tile in this many
+constexpr int kMaxExactPasses = 6;              // bracket, widen, and two narrowings at most
 static_assert(2 * kRows * kSegWords <= kRows * kBins, "bitmaps reuse the histogram memory");
 
 struct RowState {
-  uint32_t prefix;  // resolved high bits of the threshold
-  int level;        // 0/1/2: pass (level + 1) pending; 3: resolved
-  int rem;          // elements still to take inside the current prefix
+  uint32_t L, H;    // the bracket of keys [L, H] the next exact pass histograms
+  int sh;           // its bins hold 2^sh keys each
+  int resolved;     // 0: an exact pass pending; 1: T and n_tie final
+  int k;            // keys to select
+  int above;        // keys > H (the exact pass counts them)
+  uint32_t orbits;  // OR of (key - L) mod 2^sh over the bracket's members
   uint32_t T;       // threshold key (resolved)
   int n_tie;        // elements equal to T to take, lowest key first
-  uint32_t orbits;  // OR of bits [9:0] over pass-1 bin members
 };
 
 DSV_DEVICE uint32_t order_key(float s) {
@@ -51,6 +61,20 @@ DSV_DEVICE uint32_t order_key(float s) {
   const uint32_t u = __float_as_uint(s);
   return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
+
+// Float bounds so that the passes compare scores directly instead of forming every score's key:
+// for every score s that is not NaN, order_key(s) >= K  <=>  s >= ge_value(K), and
+// order_key(s) > K  <=>  s >= gt_value(K).  Keys at or below that of -inf give -inf; keys above
+// that of +inf (NaN patterns) give NaN, which no comparison passes; the key just below +0's
+// (the image of -0, which order_key folds into +0) behaves like +0's; every other key is the
+// image of exactly one float.
+DSV_DEVICE float ge_value(uint32_t K) {
+  if (K <= 0x007fffffu) return -__int_as_float(0x7f800000);
+  if (K > 0xff800000u) return __int_as_float(0x7fc00000);
+  if (K == 0x7fffffffu) K = 0x80000000u;
+  return __uint_as_float((K & 0x80000000u) ? (K ^ 0x80000000u) : ~K);
+}
+DSV_DEVICE float gt_value(uint32_t K) { return K == 0xffffffffu ? __int_as_float(0x7fc00000) : ge_value(K + 1u); }
 
 // Warp-cooperative search over a histogram from the top bin down: the bin where the
 // running count first reaches `need`, the count strictly above it and its own count.
@@ -126,13 +150,13 @@ DSV_DEVICE void scores(const Frags<R>& A, const KeyFrags<R>& f, float (&sc)[4][4
 // next group's K_lr fragments prefetched while the current one is consumed.
 template <int R, int MT, typename F>
 DSV_DEVICE void for_each_group(const Frags<R> (&A)[MT], const bf16* __restrict__ kh, int N, int k_begin, int k_end,
-                               int warp, int g, int t, F&& body) {
+                               int warp, int g, int t, F&& body, int stride = kTileKeys) {
   int kbase = k_begin + warp * 32;
   if (kbase >= k_end) return;
   KeyFrags<R> cur, nxt;
   load_keys<R>(cur, kh, kbase, N, g, t);
-  for (; kbase < k_end; kbase += kTileKeys) {
-    const int knext = kbase + kTileKeys;
+  for (; kbase < k_end; kbase += stride) {
+    const int knext = kbase + stride;
     if (knext < k_end) load_keys<R>(nxt, kh, knext, N, g, t);
     float sc[MT][4][4];
 #pragma unroll
@@ -160,44 +184,95 @@ DSV_DEVICE void for_each_group(const Frags<R>& A, const bf16* __restrict__ kh, i
   }
 }
 
-template <int LEVEL, int R, int MT>
-DSV_DEVICE void hist_pass(const Frags<R> (&A)[MT], const bf16* __restrict__ kh, int N, uint32_t* hist, RowState* rs,
-                          int nrows, int warp, int g, int t) {
+// The sample: tiles 0, kSampleEvery, 2 kSampleEvery, ... of every pending row, histogrammed by
+// key bits [31:21].
+template <int R, int MT>
+DSV_DEVICE void sample_pass(const Frags<R> (&A)[MT], const bf16* __restrict__ kh, int N, uint32_t* hist,
+                            const RowState* rs, int nrows, int warp, int g, int t) {
   bool act[MT][2];
-  uint32_t pre[MT][2];
   uint32_t* hrow[MT][2];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = kRows * mt + g + 8 * h;
-      act[mt][h] = row < nrows && rs[row].level == LEVEL;
-      pre[mt][h] = rs[row].prefix;
+      act[mt][h] = row < nrows && !rs[row].resolved;
       hrow[mt][h] = hist + row * kBins;
     }
-  for_each_group<R, MT>(A, kh, N, 0, N, warp, g, t, [&](int kbase, const float (&sc)[MT][4][4]) {
+  for_each_group<R, MT>(
+      A, kh, N, 0, N, warp, g, t,
+      [&](int, const float (&sc)[MT][4][4]) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (act[mt][e >> 1]) atomicAdd(hrow[mt][e >> 1] + (order_key(sc[mt][j][e]) >> 21), 1u);
+      },
+      kSampleEvery * kTileKeys);
+}
+
+// One exact pass over every key of the pending rows: keys above the bracket are counted in
+// registers, keys inside it histogrammed.
+template <int R, int MT>
+DSV_DEVICE void exact_pass(const Frags<R> (&A)[MT], const bf16* __restrict__ kh, int N, uint32_t* hist, RowState* rs,
+                           int nrows, int warp, int g, int t) {
+  bool act[MT][2];
+  uint32_t lo[MT][2], mask[MT][2], orb[MT][2];
+  float vlo[MT][2], vhi[MT][2];  // key >= L  <=>  s >= vlo;  key > H  <=>  s >= vhi
+  int sh[MT][2], above[MT][2];
+  uint32_t* hrow[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = kRows * mt + g + 8 * h;
+      act[mt][h] = row < nrows && !rs[row].resolved;
+      lo[mt][h] = rs[row].L;
+      vlo[mt][h] = ge_value(rs[row].L);
+      vhi[mt][h] = gt_value(rs[row].H);
+      sh[mt][h] = rs[row].sh;
+      mask[mt][h] = (1u << sh[mt][h]) - 1u;
+      orb[mt][h] = 0u;
+      above[mt][h] = 0;
+      hrow[mt][h] = hist + row * kBins;
+    }
+  for_each_group<R, MT>(A, kh, N, 0, N, warp, g, t, [&](int, const float (&sc)[MT][4][4]) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = e >> 1;
-        if (!act[mt][h]) continue;
-        const uint32_t key = order_key(sc[mt][j][e]);
-        if (LEVEL == 0) {
-          atomicAdd(hrow[mt][h] + (key >> 21), 1u);
-        } else if (LEVEL == 1) {
-          if ((key >> 21) == pre[mt][h]) {
-            atomicAdd(hrow[mt][h] + ((key >> 10) & 2047u), 1u);
-            if (key & 1023u) atomicOr(&rs[kRows * mt + g + 8 * h].orbits, key & 1023u);
+        for (int e = 0; e < 4; ++e) {
+          const int h = e >> 1;
+          const float sv = sc[mt][j][e];
+          const bool over = sv >= vhi[mt][h];
+          above[mt][h] += over ? 1 : 0;
+          if (!over && sv >= vlo[mt][h] && act[mt][h]) {
+            const uint32_t off = order_key(sv) - lo[mt][h];
+            atomicAdd(hrow[mt][h] + (off >> sh[mt][h]), 1u);
+            orb[mt][h] |= off & mask[mt][h];
           }
-        } else {
-          if ((key >> 10) == pre[mt][h]) atomicAdd(hrow[mt][h] + (key & 1023u), 1u);
         }
+  });
+  // the four lanes of a row group (t = 0..3) hold the same rows
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int a = above[mt][h];
+      uint32_t o = orb[mt][h];
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      o |= __shfl_xor_sync(0xffffffffu, o, 1);
+      o |= __shfl_xor_sync(0xffffffffu, o, 2);
+      if (t == 0 && act[mt][h]) {
+        RowState& r = rs[kRows * mt + g + 8 * h];
+        if (a) atomicAdd(&r.above, a);
+        if (o) atomicOr(&r.orbits, o);
       }
     }
-  });
 }
 
 // MT m16 row tiles of the MMA: `rows` query blocks per CTA (<= 16 MT; shared memory holds
@@ -238,7 +313,14 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     qhat[row][c] = acc;
   }
   for (int i = tid; i < rows * kBins; i += kThreads) hist[i] = 0u;
-  if (tid < kMax) rs[tid] = RowState{0u, 0, tid < nrows ? row_k(tid) : k, 0u, 0, 0u};
+  if (tid < kMax) {
+    // k <= 0 selects nothing (no key is above the largest key), k >= N every key
+    const int kr = tid < nrows ? row_k(tid) : 0;
+    RowState r{0u, 0xffffffffu, 21, 0, kr, 0, 0u, 0u, 0};
+    if (kr <= 0) { r.resolved = 1; r.T = 0xffffffffu; r.n_tie = 0; }
+    else if (kr >= N) { r.resolved = 1; r.T = 0u; r.n_tie = kTieAll; }
+    rs[tid] = r;
+  }
   __syncthreads();
 
   // ---- A fragments: q_hat = hi + lo (bf16), with the k order permuted so each thread's
@@ -261,38 +343,11 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     }
   }
 
-  // ---- histogram passes; warp w resolves rows w and w + 16 after each
-  auto resolve = [&](int level) {
-#pragma unroll
-    for (int q = 0; q < MT; ++q) {
-      const int row = warp + kWarps * q;
-      if (row < nrows && rs[row].level == level) {
-        RowState s = rs[row];
-        int bin, above, cnt;
-        warp_find_bin(hist + row * kBins, level == 2 ? 1024 : kBins, s.rem, lane, bin, above, cnt);
-        const int rem = s.rem - above;  // 1 <= rem <= cnt
-        if (level == 0) {
-          if (rem == cnt) { s.T = static_cast<uint32_t>(bin) << 21; s.n_tie = kTieAll; s.level = 3; }
-          else { s.prefix = bin; s.rem = rem; s.level = 1; }
-        } else if (level == 1) {
-          const uint32_t p = (s.prefix << 11) | static_cast<uint32_t>(bin);
-          if (rem == cnt) { s.T = p << 10; s.n_tie = kTieAll; s.level = 3; }
-          else if (s.orbits == 0) { s.T = p << 10; s.n_tie = rem; s.level = 3; }
-          else { s.prefix = p; s.rem = rem; s.level = 2; }
-        } else {
-          s.T = (s.prefix << 10) | static_cast<uint32_t>(bin);
-          s.n_tie = rem;
-          s.level = 3;
-        }
-        __syncwarp();
-        if (lane == 0) rs[row] = s;
-      }
-    }
-  };
-  auto next_level_pending = [&](int level) -> bool {
+  // ---- the sample and the bracket of every row (warp w sets up rows w, w + 16, ...)
+  auto any_pending = [&]() -> bool {  // also clears the histograms when a pass follows
     if (tid == 0) pending = 0;
     __syncthreads();
-    if (tid < nrows && rs[tid].level == level) atomicOr(&pending, 1);
+    if (tid < nrows && !rs[tid].resolved) atomicOr(&pending, 1);
     __syncthreads();
     const bool any = pending != 0;
     if (any)
@@ -300,18 +355,86 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
     __syncthreads();
     return any;
   };
-
-  hist_pass<0, R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
-  __syncthreads();
-  resolve(0);
-  if (next_level_pending(1)) {
-    hist_pass<1, R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
+  if (any_pending()) {
+    sample_pass<R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
     __syncthreads();
-    resolve(1);
-    if (next_level_pending(2)) {
-      hist_pass<2, R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
+    int n_s = 0;  // sampled keys per row
+    for (int t0 = 0; t0 < N; t0 += kSampleEvery * kTileKeys) n_s += N - t0 < kTileKeys ? N - t0 : kTileKeys;
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      const int row = warp + kWarps * q;
+      if (row < nrows && !rs[row].resolved) {
+        RowState s = rs[row];
+        // the k-th largest key sits near rank rho of the sample; take ranks about four
+        // binomial standard deviations (plus a few) to either side
+        const float frac = static_cast<float>(s.k) / static_cast<float>(N);
+        const float rho = frac * static_cast<float>(n_s);
+        const float m = 4.f * sqrtf(rho * (1.f - frac)) + 4.f;
+        const int r_hi = static_cast<int>(floorf(rho - m)), r_lo = static_cast<int>(ceilf(rho + m));
+        int bin_hi = kBins - 1, bin_lo = 0, above, cnt;
+        if (r_hi >= 1) warp_find_bin(hist + row * kBins, kBins, r_hi, lane, bin_hi, above, cnt);
+        if (r_lo <= n_s) warp_find_bin(hist + row * kBins, kBins, r_lo, lane, bin_lo, above, cnt);
+        const int span = bin_hi - bin_lo + 1;  // bins of 2^21 keys
+        int sh = 10;
+        while ((1 << (sh - 10)) < span && sh < 21) ++sh;
+        s.sh = sh;
+        s.L = sh >= 21 ? 0u : static_cast<uint32_t>(bin_lo) << 21;
+        const uint64_t h64 = static_cast<uint64_t>(s.L) + (static_cast<uint64_t>(kBins) << sh) - 1u;
+        s.H = h64 > 0xffffffffull ? 0xffffffffu : static_cast<uint32_t>(h64);
+        __syncwarp();
+        if (lane == 0) rs[row] = s;
+      }
+    }
+    __syncthreads();
+    for (int pass = 0; pass < kMaxExactPasses && any_pending(); ++pass) {
+      exact_pass<R, MT>(A, kh, N, hist, rs, nrows, warp, g, t);
       __syncthreads();
-      resolve(2);
+#pragma unroll
+      for (int q = 0; q < MT; ++q) {
+        const int row = warp + kWarps * q;
+        if (row < nrows && !rs[row].resolved) {
+          RowState s = rs[row];
+          const uint32_t* hr = hist + row * kBins;
+          int inside = 0;
+          for (int b = lane; b < kBins; b += 32) inside += static_cast<int>(hr[b]);
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) inside += __shfl_xor_sync(0xffffffffu, inside, o);
+          const int rem = s.k - s.above;  // to take at or below H
+          if (rem < 1 || rem > inside) {
+            // the k-th largest key is outside the bracket: the whole key range next
+            s.L = 0u;
+            s.H = 0xffffffffu;
+            s.sh = 21;
+          } else {
+            int bin, abv, cnt;
+            warp_find_bin(hr, kBins, rem, lane, bin, abv, cnt);
+            const int rem2 = rem - abv;  // 1 <= rem2 <= cnt: to take inside the bin
+            const uint32_t base = s.L + (static_cast<uint32_t>(bin) << s.sh);
+            if (rem2 == cnt) {  // the whole bin: every key >= its lowest
+              s.T = base;
+              s.n_tie = kTieAll;
+              s.resolved = 1;
+            } else if (s.sh == 0 || s.orbits == 0u) {  // the bin holds one key value
+              s.T = base;
+              s.n_tie = rem2;
+              s.resolved = 1;
+            } else {  // narrow to the bin
+              s.L = base;
+              s.H = base + ((1u << s.sh) - 1u);
+              s.sh = s.sh > 11 ? s.sh - 11 : 0;
+            }
+          }
+          s.above = 0;
+          s.orbits = 0u;
+          __syncwarp();
+          if (lane == 0) rs[row] = s;
+        }
+      }
+    }
+    if (tid < nrows && !rs[tid].resolved) {  // unreachable: every row resolves within the passes
+      flag_status(status, kStatusBadIndex);
+      rs[tid].T = 0xffffffffu;
+      rs[tid].n_tie = 0;
     }
   }
   __syncthreads();
@@ -319,12 +442,15 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
   // ---- emit, one segment of keys at a time
   uint32_t* gtb = hist;                      // [rows][kSegWords]
   uint32_t* eqb = hist + rows * kSegWords;   // [rows][kSegWords]
-  uint32_t T[MT][2];
+  float vgt[MT][2], vge[MT][2];  // key > T  <=>  s >= vgt;  key >= T  <=>  s >= vge
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    T[mt][0] = rs[kRows * mt + g].T;
-    T[mt][1] = rs[kRows * mt + g + 8].T;
-  }
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t T = rs[kRows * mt + g + 8 * h].T;
+      vgt[mt][h] = gt_value(T);
+      vge[mt][h] = ge_value(T);
+    }
   // rows warp and warp + 16: running counts (every lane holds them)
   int out_pos[MT], tie_seen[MT], n_tie[MT];
 #pragma unroll
@@ -344,11 +470,17 @@ estimate_topk_kernel(const bf16* __restrict__ q_lr, const bf16* __restrict__ k_l
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int h = e >> 1;
-            const int pos = 8 * j + 2 * t + (e & 1);
-            const uint32_t key = order_key(sc[mt][j][e]);
-            gtm[h] |= static_cast<uint32_t>(key > T[mt][h]) << pos;
-            eqm[h] |= static_cast<uint32_t>(key == T[mt][h]) << pos;
+            const int pos = 8 * j + (e & 1);  // + 2 t, applied below
+            const float sv = sc[mt][j][e];
+            const bool gt = sv >= vgt[mt][h];
+            gtm[h] |= static_cast<uint32_t>(gt) << pos;
+            eqm[h] |= static_cast<uint32_t>(!gt && sv >= vge[mt][h]) << pos;
           }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          gtm[h] <<= 2 * t;
+          eqm[h] <<= 2 * t;
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

@@ -123,6 +123,31 @@ def test_ties_go_to_the_lower_key_index():
     _full_check(x, out, 200)
 
 
+def test_selection_signed_zero_and_negative_thresholds():
+    """Scores of a few distinct integer values with many ties, signed zeros among them (the
+    selection compares scores against float bounds equivalent to their order keys, which fold -0
+    into +0), and k cutting the ranking inside the zero group, in the negative values and near N:
+    the selected sets equal the oracle's for every block."""
+    dev = need_gpu()
+    wl = WORKLOADS["tiny"].with_heads(2)
+    x = make_inputs(wl)
+    gen = torch.Generator().manual_seed(5)
+    vals = torch.tensor([-3.0, -2.0, -1.0, -0.0, 0.0, 1.0, 2.0, 3.0], dtype=torch.bfloat16)
+    for h in range(2):
+        x["k_lr"][0, h] = vals[torch.randint(0, 8, (wl.N, wl.r), generator=gen)]
+        x["q_lr"][0, h] = torch.randint(-1, 2, (wl.N, wl.r), generator=gen).to(torch.bfloat16)
+    x["q_lr"][0, 1, :64] = 0.0
+    x["q_lr"][0, 1, 0, 0] = 1.0   # block 0 of head 1: s = K_lr[:, 0], signed zeros included
+    g = _to(dev, x)
+    for k in (1, 100, 500, 511, 512, 513, 700, 1000, 1023):
+        idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], k)
+        torch.cuda.synchronize()
+        assert dsv_last_device_status() == 0
+        for h in range(2):
+            want = oracle.estimate_topk(x["q_lr"][0, h], x["k_lr"][0, h], 64, k)
+            assert np.array_equal(idx[0, h].cpu().numpy(), want), f"k={k} head {h}"
+
+
 def test_short_clip_selection_every_head_bit_exact():
     dev = need_gpu()
     wl = WORKLOADS["short"]
