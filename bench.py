@@ -277,10 +277,15 @@ def algorithmic(kernel, wl, launches_per_step):
     partial row and its list entry read, dK and dV written)."""
     BH = wl.B * wl.H
     pairs = BH * wl.NB * wl.k
+    dense = wl.k == wl.N  # the dense path: dQ-only main kernel, key-stationary dK/dV kernel
     if kernel == "sparse_fwd":
         return "tensor", 4.0 * BH * wl.N * wl.k * wl.d / launches_per_step, "flop"
     if kernel == "bwd_main":
-        return "tensor", 10.0 * BH * wl.N * wl.k * wl.d / launches_per_step, "flop"
+        return "tensor", (6.0 if dense else 10.0) * BH * wl.N * wl.k * wl.d / launches_per_step, "flop"
+    if kernel == "dense_dkdv":
+        return "tensor", 8.0 * BH * wl.N * wl.N * wl.d / launches_per_step, "flop"
+    if kernel == "dense_delta":
+        return "hbm", (2.0 * BH * wl.N * wl.d * 2 + 4.0 * BH * wl.N) / launches_per_step, "byte"
     if kernel == "estimate_topk":
         return "hbm", (2.0 * BH * wl.N * wl.r * 2 + 4.0 * BH * wl.NB * wl.k) / launches_per_step, "byte"
     if kernel == "bwd_reduce":
