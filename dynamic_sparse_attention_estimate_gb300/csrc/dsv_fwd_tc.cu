@@ -13,9 +13,12 @@
 //              row) to shared memory as the B operand of the PV product;
 //   warp 4     producer (with warps 6-8 at d = 128, each taking 32 of a chunk's rows):
 //              gathers the chunk's K and V rows with cp.async (16 bytes per copy, into
-//              128-byte-swizzled tiles) into a ring of stages and lets the stage's mbarrier
+//              128-byte-swizzled tiles) into a ring of stages and lets the stage's mbarriers
 //              count the copies' completion (cp.async.mbarrier.arrive), so it never waits for
-//              its own copies; keys past k or out of range are zero-filled;
+//              its own copies; K and V of a stage have barriers of their own, so a chunk's K
+//              rows are gathered as soon as the S^T product two chunks back has read the
+//              stage's K, while its V rows wait for that chunk's PV product; keys past k or
+//              out of range are zero-filled;
 //   warp 5     one thread issues every MMA as soon as its inputs are ready: it waits in the
 //              hardware, for a short bounded time, on the barrier of the product that comes
 //              next in the usual order (the PV product of the oldest chunk with an S^T), and
@@ -72,8 +75,10 @@ struct Smem {
 
 template <int NST>
 struct Bars {
-  uint64_t full[NST];       // cp.async completion: K and V of a stage (and Q, with stage 0) landed
-  uint64_t empty[NST];      // MMA commit: the PV product that last read a stage is done
+  uint64_t full_k[NST];     // cp.async completion: K rows of a stage (and Q, with stage 0) landed
+  uint64_t full_v[NST];     // cp.async completion: V rows of a stage landed
+  uint64_t empty_k[NST];    // MMA commit: the S^T product that read a stage's K rows is done
+  uint64_t empty_v[NST];    // MMA commit: the PV product that read a stage's V rows is done
   uint64_t s_full[2];       // MMA commit: S^T in TMEM buffer b is ready
   uint64_t s_empty[2];      // softmax: S^T buffer b has been read
   uint64_t p_full[2];       // softmax: P^T tile b written
@@ -212,8 +217,10 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   }
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
-      tc::mbar_init(bar(bars.full[s]), 32 * kProducers<D>);
-      tc::mbar_init(bar(bars.empty[s]), 1);
+      tc::mbar_init(bar(bars.full_k[s]), 32 * kProducers<D>);
+      tc::mbar_init(bar(bars.full_v[s]), 32 * kProducers<D>);
+      tc::mbar_init(bar(bars.empty_k[s]), 1);
+      tc::mbar_init(bar(bars.empty_v[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(bar(bars.s_full[b]), 1);
@@ -272,7 +279,9 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 #pragma unroll
       for (int h = 0; h < NG; ++h) cur[h] = nxt[h];
       load_rows(c + 1, nxt);
-      if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty[st]), ((c / NST) - 1) & 1, kWaitLimit);
+      // K rows as soon as the S^T product two chunks back has read the stage's K, V rows once the
+      // PV product has read its V (later: the softmax and P^T lie between them)
+      if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty_k[st]), ((c / NST) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
       const uint32_t dK = sK + st * S::KV_BYTES, dV = sV + st * S::KV_BYTES;
@@ -286,21 +295,27 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       constexpr int LPR = D / 8, RPI = 32 / LPR;
       const int sub = lane % LPR, rsub = lane / LPR;
       const int e = sub * 8;
+      auto copy_rows = [&](uint32_t dst, const bf16* src_head) {
 #pragma unroll
-      for (int h = 0; h < NG; ++h) {
+        for (int h = 0; h < NG; ++h) {
 #pragma unroll
-        for (int it = 0; it < 32 / RPI; ++it) {
-          const int rg = it * RPI + rsub;                       // row within the group
-          const int row = 32 * (pidx + NP * h) + rg;
-          const int32_t j = __shfl_sync(0xffffffffu, cur[h], rg);
-          const bool ok = j >= 0 && j < N;
-          const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
-          const uint32_t off = (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63);
-          cp_async_16(dK + off, kh + src, ok);
-          cp_async_16(dV + off, vh + src, ok);
+          for (int it = 0; it < 32 / RPI; ++it) {
+            const int rg = it * RPI + rsub;                       // row within the group
+            const int row = 32 * (pidx + NP * h) + rg;
+            const int32_t j = __shfl_sync(0xffffffffu, cur[h], rg);
+            const bool ok = j >= 0 && j < N;
+            const int64_t src = (ok ? static_cast<int64_t>(j) : 0) * D + e;
+            cp_async_16(dst + (e >> 6) * (kChunk * 128) + tc::sw128(row, e & 63), src_head + src, ok);
+          }
         }
-      }
-      cp_async_arrive(bar(bars.full[st]));
+      };
+      copy_rows(dK, kh);
+      cp_async_arrive(bar(bars.full_k[st]));
+      if (c >= NST) ok_run = tc::mbar_wait(bar(bars.empty_v[st]), ((c / NST) - 1) & 1, kWaitLimit);
+      ok_run = __all_sync(0xffffffffu, ok_run);
+      if (!ok_run) break;
+      copy_rows(dV, vh);
+      cp_async_arrive(bar(bars.full_v[st]));
     }
     cp_async_wait<0>();
     if (!ok_run && lane == 0) atomicOr(&fail_s, 1);
@@ -316,7 +331,8 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       while (ok_run && cp < nchunks) {
         // the usual next product is PV(cp) once S(cp) exists; otherwise S(cs)
         const bool pv_next = cp < cs;
-        if (pv_next && mbar_try_wait_ns(bar(bars.p_full[cp & 1]), (cp >> 1) & 1, 64)) {
+        if (pv_next && mbar_try_wait_ns(bar(bars.p_full[cp & 1]), (cp >> 1) & 1, 64) &&
+            mbar_try_wait_ns(bar(bars.full_v[cp % NST]), (cp / NST) & 1, 64)) {
           // PV(cp): O^T += V_c^T P^T
           tc::tc_fence_after();
           const uint32_t aV = sV + (cp % NST) * S::KV_BYTES, bP = sP + (cp & 1) * S::P_BYTES;
@@ -328,13 +344,13 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
                        (cp > 0 || j > 0) ? 1u : 0u);
           }
           tc::mma_commit(bar(bars.pv_done[cp & 1]));
-          tc::mma_commit(bar(bars.empty[cp % NST]));
+          tc::mma_commit(bar(bars.empty_v[cp % NST]));
           if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
           ++cp;
           idle = 0;
         } else if (cs < nchunks &&
-                   (pv_next ? mbar_test(bar(bars.full[cs % NST]), (cs / NST) & 1)
-                            : mbar_try_wait_ns(bar(bars.full[cs % NST]), (cs / NST) & 1, 64)) &&
+                   (pv_next ? mbar_test(bar(bars.full_k[cs % NST]), (cs / NST) & 1)
+                            : mbar_try_wait_ns(bar(bars.full_k[cs % NST]), (cs / NST) & 1, 64)) &&
                    (cs < 2 || mbar_test(bar(bars.s_empty[cs & 1]), ((cs - 2) >> 1) & 1))) {
           // S(cs): S^T = K_c Q^T.  The stage was written with cp.async (generic proxy):
           // order those writes before the tensor core's reads.
@@ -349,6 +365,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
                        tc::smem_desc(sQ + off_b, 16, 1024), idS, j > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(bars.s_full[cs & 1]));
+          tc::mma_commit(bar(bars.empty_k[cs % NST]));
           ++cs;
           idle = 0;
         } else if (++idle > kPollLimit) {
