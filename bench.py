@@ -377,10 +377,10 @@ def adaln_measurements(dev, timed):
     return out
 
 
-def dense_comparator(g, wl, timed, ms_per_step):
+def dense_comparator(g, wl, flush_l2, ms_per_step):
     """PyTorch SDPA forward + backward (a library timing comparator, not this library) on the same
-    per-head shape, every backend that runs here, one head, scaled to the step's heads; the speedup
-    is quoted against the fastest backend."""
+    per-head shape, every backend that runs here, one head, scaled to the step's heads; each
+    backend's fastest call is kept and the speedup is quoted against the fastest backend."""
     import torch
     from torch.nn.attention import SDPBackend, sdpa_kernel
     heads = 1 if wl.N > 65536 else heads_per_call(wl)
@@ -388,7 +388,20 @@ def dense_comparator(g, wl, timed, ms_per_step):
     qf, kf, vf = [g[n][:, :heads].detach().clone().requires_grad_(True) for n in ("q", "k", "v")]
     do = g["do"][:, :heads].contiguous()
     dense_flop = 14.0 * wl.B * wl.H * wl.N * wl.N * wl.d
-    reps = 2 if wl.N > 65536 else 5
+    reps = 3 if wl.N > 65536 else 5
+
+    def fastest_of(fn, n):
+        # the comparator's best call (its time varies between calls and runs): the speedup quoted
+        # against it is the smallest one
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            flush_l2()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return min(a.elapsed_time(b) for a, b in ev)
+
     backends = {}
     for name, be in (("cudnn", SDPBackend.CUDNN_ATTENTION), ("flash", SDPBackend.FLASH_ATTENTION),
                      ("efficient", SDPBackend.EFFICIENT_ATTENTION)):
@@ -399,7 +412,7 @@ def dense_comparator(g, wl, timed, ms_per_step):
                     out.backward(do)
             dense_step()
             torch.cuda.synchronize()
-            ms = timed(dense_step, reps) * scale_to
+            ms = fastest_of(dense_step, reps) * scale_to
             backends[name] = {"ms": ms, "tflops": dense_flop / (ms / 1e3) / 1e12}
         except Exception as exc:  # a backend that does not run on this GPU / shape
             backends[name] = {"error": str(exc).splitlines()[0][:160]}
@@ -751,7 +764,7 @@ def dsv_arm(args):
     dense = None
     if side and not args.no_dense:
         try:
-            dense = dense_comparator(g, wl, timed, ms_per_step)
+            dense = dense_comparator(g, wl, flush_l2, ms_per_step)
         except Exception as exc:  # a comparator only
             dense = {"error": str(exc)[:200]}
 
