@@ -7,10 +7,12 @@
 //     O^T[d x 64 q]        += V_c^T . P^T         (tcgen05, M=d,   N=64, K=128)
 // so both products keep M = 128 although a block has 64 queries (for d = 64 the PV operand
 // carries an extra row of ones that yields the softmax row sums; see kOnesRow).
-// Roles (192 threads at d = 64, 288 at d = 128):
-//   warps 0-3  softmax: thread t owns key lane t of S^T in tensor memory (TMEM); it forms
-//              P = exp2(S scale log2e - m_q) and writes its P^T row (64 bf16, one 128-byte
-//              row) to shared memory as the B operand of the PV product;
+// Roles (192 threads at d = 64, 416 at d = 128):
+//   warps 0-3  softmax (with warps 9-12 at d = 128, each pair of warps on one TMEM lane
+//              quadrant taking 32 of the 64 query columns): a thread owns a key lane of S^T in
+//              tensor memory (TMEM); it forms P = exp2(S scale log2e - m_q) and writes its part
+//              of the key's P^T row (64 bf16, one 128-byte row) to shared memory as the B
+//              operand of the PV product;
 //   warp 4     producer (with warps 6-8 at d = 128, each taking 32 of a chunk's rows):
 //              gathers the chunk's K and V rows with cp.async (16 bytes per copy, into
 //              128-byte-swizzled tiles) into a ring of stages and lets the stage's mbarriers
@@ -46,9 +48,16 @@ constexpr int kChunk = 128;
 // each) one warp per CTA.  Producers are warp 4 and warps 6, 7, 8.
 template <int D>
 constexpr int kProducers = D == 128 ? 4 : 1;
+// Softmax warps: four (one per TMEM lane quadrant, 64 query columns each) at d = 64; eight at
+// d = 128 (two per quadrant, 32 query columns each: the softmax is the forward's critical path
+// there, and two warps per quadrant halve each thread's chain of dependent work).  Softmax warps
+// are 0-3 and, at d = 128, 9-12.
 template <int D>
-constexpr int kThreadsFor = 160 + 32 * kProducers<D>;
-DSV_DEVICE int producer_index(int warp) { return warp == 4 ? 0 : (warp >= 6 ? warp - 5 : -1); }
+constexpr int kSoftmaxWarps = D == 128 ? 8 : 4;
+template <int D>
+constexpr int kThreadsFor = 32 * (1 + kProducers<D> + kSoftmaxWarps<D>);  // + the MMA warp
+DSV_DEVICE int producer_index(int warp) { return warp == 4 ? 0 : (warp >= 6 && warp <= 8 ? warp - 5 : -1); }
+DSV_DEVICE int softmax_index(int warp) { return warp < 4 ? warp : (warp >= 9 ? warp - 5 : -1); }
 constexpr float kStaleLimit = 8.f;  // log2 units
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kPollLimit = 1u << 24;  // rounds of bounded waits before giving up
@@ -87,13 +96,16 @@ struct Bars {
   uint64_t drain;           // MMA commit at the end: every MMA the issuing thread started is done
 };
 
-DSV_DEVICE void named_sync_softmax() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
-// Barrier over the 128 softmax threads that also ORs a flag across them (uniform result).
+// Barrier over the NT softmax threads.
+template <int NT>
+DSV_DEVICE void named_sync_softmax() { asm volatile("bar.sync 1, %0;\n" ::"r"(NT) : "memory"); }
+// The same barrier, ORing a flag across the softmax threads (uniform result).
+template <int NT>
 DSV_DEVICE bool named_sync_or(bool v) {
   uint32_t r;
-  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
                : "=r"(r)
-               : "r"(static_cast<uint32_t>(v))
+               : "r"(static_cast<uint32_t>(v)), "r"(NT)
                : "memory");
   return r != 0;
 }
@@ -130,21 +142,23 @@ DSV_DEVICE void cp_async_arrive(uint32_t bar) {
 template <int D>
 constexpr bool kOnesRow = D == 64;
 
-// Column reduction over the 128 softmax threads of 64 per-thread values (v[c] is this
-// thread's value for column c).  Fixed order, so the result is deterministic.  Returns
-// through red[64] in shared memory (visible after the trailing barrier).
-template <bool MAX>
-DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* red, int warp, int lane) {
-  float cur[64];
+// Column reduction over the key lanes of the softmax threads: each thread holds C consecutive
+// query columns (v[c] for column c0 + c, c0 = C times its half); the four warps of a half cover
+// the 128 key lanes.  Fixed order, so the result is deterministic.  Returns through red[64] in
+// shared memory (visible after the trailing barrier).
+template <bool MAX, int C, int NSMW>
+DSV_DEVICE void column_reduce(float (&v)[C], float* red_w /*[NSMW][C]*/, float* red, int sw, int lane) {
+  constexpr int K = C / 32;  // columns per lane after the exchange
+  float cur[C];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) cur[i] = v[i];
-  int n = 64;
+  for (int i = 0; i < C; ++i) cur[i] = v[i];
+  int n = C;
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {  // after the step with mask m each lane keeps half its columns
     const bool upper = (lane & m) != 0;
     n >>= 1;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < C / 2; ++i) {
       if (i < n) {
         const float mine = upper ? cur[i + n] : cur[i];
         const float other = upper ? cur[i] : cur[i + n];
@@ -153,17 +167,17 @@ DSV_DEVICE void column_reduce(float (&v)[64], float* red_w /*[4][64]*/, float* r
       }
     }
   }
-  red_w[warp * 64 + 2 * lane] = cur[0];  // lane holds columns 2 lane and 2 lane + 1
-  red_w[warp * 64 + 2 * lane + 1] = cur[1];
-  named_sync_softmax();
-  if (warp * 32 + lane < 64) {
-    const int q = warp * 32 + lane;
-    float r = red_w[q];
 #pragma unroll
-    for (int w = 1; w < 4; ++w) r = MAX ? fmaxf(r, red_w[w * 64 + q]) : r + red_w[w * 64 + q];
-    red[q] = r;
+  for (int i = 0; i < K; ++i) red_w[sw * C + K * lane + i] = cur[i];  // lane holds columns K lane + i
+  named_sync_softmax<32 * NSMW>();
+  const int hq = sw >> 2, loc = (sw & 3) * 32 + lane;
+  if (loc < C) {
+    float r = red_w[(hq * 4) * C + loc];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) r = MAX ? fmaxf(r, red_w[(hq * 4 + w) * C + loc]) : r + red_w[(hq * 4 + w) * C + loc];
+    red[hq * C + loc] = r;
   }
-  named_sync_softmax();
+  named_sync_softmax<32 * NSMW>();
 }
 
 // CSR: per-block key counts from row offsets (and an optional launch order); otherwise k for
@@ -179,7 +193,11 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) Bars<NST> bars;
   __shared__ uint32_t tmem_base_s;
-  __shared__ float m_s[64], alpha_s[64], red_w[4 * 64], red_s[64];
+  // m_s is read as float4: every array here is 16-byte aligned explicitly
+  __shared__ __align__(16) float m_s[64];
+  __shared__ __align__(16) float alpha_s[64];
+  __shared__ __align__(16) float red_w[4 * 64];
+  __shared__ __align__(16) float red_s[64];
   __shared__ int flag_s[2];
   __shared__ int fail_s;
 
@@ -224,8 +242,8 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(bar(bars.s_full[b]), 1);
-      tc::mbar_init(bar(bars.s_empty[b]), 128);
-      tc::mbar_init(bar(bars.p_full[b]), 128);
+      tc::mbar_init(bar(bars.s_empty[b]), 32 * kSoftmaxWarps<D>);
+      tc::mbar_init(bar(bars.p_full[b]), 32 * kSoftmaxWarps<D>);
       tc::mbar_init(bar(bars.pv_done[b]), 1);
     }
     tc::mbar_init(bar(bars.o_full), 1);
@@ -380,11 +398,17 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       if (!tc::mbar_wait(bar(bars.drain), 0, kWaitLimit)) atomicOr(&fail_s, 1);
     }
   } else {
-    // ================================================================ softmax (threads 0..127)
+    // ================================================================ softmax
     // Every softmax thread runs every iteration and reaches every named barrier, also after
     // a timed-out wait (later waits are then skipped and the results are discarded).
-    const int t = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    constexpr int SMW = kSoftmaxWarps<D>, NSM = 32 * SMW;
+    constexpr int QC = 256 / SMW;  // query columns per thread: 64 or 32
+    constexpr int NH = QC / 16;    // 16-column TMEM loads per matrix row
+    const int sw = softmax_index(warp), hq = sw >> 2, quad = warp & 3;
+    const int t = quad * 32 + lane;  // key lane (TMEM lane) of this thread
+    const int sidx = sw * 32 + lane;  // 0 .. NSM - 1
+    const int c0 = hq * QC;           // this thread's first query column
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     bool ok_run = true;
     int32_t jnext = t < kk ? key_at(t) : -1;  // this lane's key index, one chunk ahead
     for (int c = 0; c < nchunks; ++c) {
@@ -396,19 +420,20 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       }
       ok_run = ok_run && tc::mbar_wait(bar(bars.s_full[b]), (c >> 1) & 1, kWaitLimit);
       tc::tc_fence_after();
-      // ---- one pass over the S^T row: probabilities against the stale max, and the vote on
-      // "some logit exceeds the stale max by more than 8" (the S buffer is released after it)
-      const uint32_t s_col = tmem + lane_base + (b ? kColS1 : kColS0);
+      // ---- one pass over this thread's part of the S^T row: probabilities against the stale
+      // max, and the vote on "some logit exceeds the stale max by more than 8" (the S buffer is
+      // released after it)
+      const uint32_t s_col = tmem + lane_base + (b ? kColS1 : kColS0) + c0;
       bool over = false;
-      float p[64];
+      float p[QC];
       {
-        uint32_t r[4][16];
+        uint32_t r[NH][16];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) tc::tmem_ld16(s_col + h * 16, r[h]);
+        for (int h = 0; h < NH; ++h) tc::tmem_ld16(s_col + h * 16, r[h]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i4 = 0; i4 < 16; ++i4) {
-          const float4 m4 = reinterpret_cast<const float4*>(m_s)[i4];
+        for (int i4 = 0; i4 < QC / 4; ++i4) {
+          const float4 m4 = reinterpret_cast<const float4*>(m_s + c0)[i4];
           const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -421,79 +446,80 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       }
       over &= valid;
       if (__any_sync(0xffffffffu, over) && lane == 0) atomicOr(&flag_s[c & 1], 1);
-      if (t == 0) flag_s[(c + 1) & 1] = 0;
-      named_sync_softmax();
+      if (sidx == 0) flag_s[(c + 1) & 1] = 0;
+      named_sync_softmax<NSM>();
       if (flag_s[c & 1]) {
         // ---- new running max for this chunk; rescale O and L; redo the probabilities
-        float x[64];
+        float x[QC];
         {
-          uint32_t r[4][16];
+          uint32_t r[NH][16];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) tc::tmem_ld16(s_col + h * 16, r[h]);
+          for (int h = 0; h < NH; ++h) tc::tmem_ld16(s_col + h * 16, r[h]);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = valid ? __uint_as_float(r[i >> 4][i & 15]) * scale_log2 : -CUDART_INF_F;
+          for (int i = 0; i < QC; ++i) x[i] = valid ? __uint_as_float(r[i >> 4][i & 15]) * scale_log2 : -CUDART_INF_F;
         }
-        column_reduce<true>(x, red_w, red_s, warp, lane);
-        if (t < 64) {
-          const float mo = m_s[t];
-          const float mn = fmaxf(mo, red_s[t]);
-          alpha_s[t] = mn == -CUDART_INF_F ? 1.f : fast_exp2(mo - mn);
-          m_s[t] = mn;
+        column_reduce<true, QC, SMW>(x, red_w, red_s, sw, lane);
+        if (sidx < 64) {
+          const float mo = m_s[sidx];
+          const float mn = fmaxf(mo, red_s[sidx]);
+          alpha_s[sidx] = mn == -CUDART_INF_F ? 1.f : fast_exp2(mo - mn);
+          m_s[sidx] = mn;
         }
-        named_sync_softmax();
+        named_sync_softmax<NSM>();
         if (c > 0) {
           ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[(c - 1) & 1]), ((c - 1) >> 1) & 1, kWaitLimit);
           tc::tc_fence_after();
 #pragma unroll
           for (int col = 0; col < (kOnesRow<D> ? 1 : 2); ++col) {  // O^T (and L with it), then L
-            const uint32_t base = tmem + lane_base + (col ? kColL : kColO);
+            const uint32_t base = tmem + lane_base + (col ? kColL : kColO) + c0;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
+            for (int h = 0; h < NH; ++h) {
               uint32_t r[16];
               tc::tmem_ld16(base + h * 16, r);
               tc::tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_s[h * 16 + i]);
+              for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_s[c0 + h * 16 + i]);
               tc::tmem_st16(base + h * 16, r);
             }
           }
           tc::tmem_wait_st();
         }
 #pragma unroll
-        for (int i = 0; i < 64; ++i) p[i] = x[i] == -CUDART_INF_F ? 0.f : fast_exp2(x[i] - m_s[i]);
+        for (int i = 0; i < QC; ++i) p[i] = x[i] == -CUDART_INF_F ? 0.f : fast_exp2(x[i] - m_s[c0 + i]);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty[b]));
-      // ---- P^T row of this key into the B tile (64 queries = one 128-byte row)
+      // ---- this thread's columns of the key's P^T row in the B tile (64 queries = one 128-byte
+      // row; 16-byte pieces XOR-swizzled by the row)
       if (c >= 2) ok_run = ok_run && tc::mbar_wait(bar(bars.pv_done[b]), ((c - 2) >> 1) & 1, kWaitLimit);
       const uint32_t prow = sP + b * S::P_BYTES + t * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t w0 = pack_bf16x2(p[ch * 8 + 0], p[ch * 8 + 1]), w1 = pack_bf16x2(p[ch * 8 + 2], p[ch * 8 + 3]);
-        const uint32_t w2 = pack_bf16x2(p[ch * 8 + 4], p[ch * 8 + 5]), w3 = pack_bf16x2(p[ch * 8 + 6], p[ch * 8 + 7]);
+      for (int cl = 0; cl < QC / 8; ++cl) {
+        const int ch = hq * (QC / 8) + cl;
+        const uint32_t w0 = pack_bf16x2(p[cl * 8 + 0], p[cl * 8 + 1]), w1 = pack_bf16x2(p[cl * 8 + 2], p[cl * 8 + 3]);
+        const uint32_t w2 = pack_bf16x2(p[cl * 8 + 4], p[cl * 8 + 5]), w3 = pack_bf16x2(p[cl * 8 + 6], p[cl * 8 + 7]);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + (((ch ^ t) & 7) << 4)), "r"(w0), "r"(w1),
                      "r"(w2), "r"(w3));
       }
       // ---- d = 128: row sums of this key lane, accumulated in TMEM
-#pragma unroll
-      for (int half = 0; half < (kOnesRow<D> ? 0 : 2); ++half) {
-        const uint32_t base = tmem + lane_base + kColL + half * 32;
-        uint32_t r[2][16];
+      if (!kOnesRow<D>) {
+        const uint32_t base = tmem + lane_base + kColL + c0;
+        uint32_t r[NH][16];
         if (c > 0) {
-          tc::tmem_ld16(base, r[0]);
-          tc::tmem_ld16(base + 16, r[1]);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) tc::tmem_ld16(base + h * 16, r[h]);
           tc::tmem_wait_ld();
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < NH; ++h) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            r[h][i] = __float_as_uint((c > 0 ? __uint_as_float(r[h][i]) : 0.f) + p[half * 32 + h * 16 + i]);
+            r[h][i] = __float_as_uint((c > 0 ? __uint_as_float(r[h][i]) : 0.f) + p[h * 16 + i]);
           tc::tmem_st16(base + h * 16, r[h]);
         }
+        tc::tmem_wait_st();
       }
-      if (!kOnesRow<D>) tc::tmem_wait_st();
       tc::fence_async_shared();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.p_full[b]));
@@ -502,7 +528,7 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     // LSE = (m + log2 l) ln 2
     ok_run = ok_run && tc::mbar_wait(bar(bars.o_full), 0, kWaitLimit);
     if (!ok_run) atomicOr(&fail_s, 1);
-    const bool failed = named_sync_or(!ok_run);
+    const bool failed = named_sync_or<NSM>(!ok_run);
     if (!failed) {
       tc::tc_fence_after();
       if (kOnesRow<D>) {
@@ -518,20 +544,20 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
               for (int i = 0; i < 16; ++i) red_s[h * 16 + i] = __uint_as_float(r[h][i]);
           }
         }
-        named_sync_softmax();
+        named_sync_softmax<NSM>();
       } else {
-        float lsum[64];
+        float lsum[QC];
         {
-          uint32_t r[4][16];
+          uint32_t r[NH][16];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) tc::tmem_ld16(tmem + lane_base + kColL + h * 16, r[h]);
+          for (int h = 0; h < NH; ++h) tc::tmem_ld16(tmem + lane_base + kColL + c0 + h * 16, r[h]);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
+          for (int h = 0; h < NH; ++h)
 #pragma unroll
             for (int i = 0; i < 16; ++i) lsum[h * 16 + i] = __uint_as_float(r[h][i]);
         }
-        column_reduce<false>(lsum, red_w, red_s, warp, lane);
+        column_reduce<false, QC, SMW>(lsum, red_w, red_s, sw, lane);
       }
       // O^T lane -> head dim (M = 128: lane = row; lanes 64.. of the d = 64 product are the
       // row sums and the zero rows of the ones tile)
@@ -539,26 +565,26 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       const int64_t qrow0 = bh * N + blk * 64;
       bf16* stage = reinterpret_cast<bf16*>(smem + S::OFF_K);  // [64 q][D]: K stage 0 is free now
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < NH; ++h) {
         uint32_t r[16];
-        tc::tmem_ld16(tmem + lane_base + kColO + h * 16, r);  // whole warp, converged
+        tc::tmem_ld16(tmem + lane_base + kColO + c0 + h * 16, r);  // whole warp, converged
         tc::tmem_wait_ld();
         if (dim >= 0) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int qq = h * 16 + i;
+            const int qq = c0 + h * 16 + i;
             const float l = red_s[qq];
             stage[qq * D + dim] = __float2bfloat16_rn(l > 0.f ? __uint_as_float(r[i]) / l : 0.f);
           }
         }
       }
-      named_sync_softmax();
+      named_sync_softmax<NSM>();
       bf16* ob = o + qrow0 * D;
-      for (int i = t; i < 64 * D / 8; i += 128)
+      for (int i = sidx; i < 64 * D / 8; i += NSM)
         reinterpret_cast<uint4*>(ob)[i] = reinterpret_cast<const uint4*>(stage)[i];
-      if (t < 64) {
-        const float l = red_s[t];
-        lse[qrow0 + t] = l > 0.f ? (m_s[t] + __log2f(l)) * kLn2 : -CUDART_INF_F;
+      if (sidx < 64) {
+        const float l = red_s[sidx];
+        lse[qrow0 + sidx] = l > 0.f ? (m_s[sidx] + __log2f(l)) * kLn2 : -CUDART_INF_F;
       }
     }
   }
