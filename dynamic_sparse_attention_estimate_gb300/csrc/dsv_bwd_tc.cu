@@ -16,8 +16,9 @@
 // Roles (512 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
 // on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
 // dK_c out of TMEM into shared-memory staging rows and write the key lists (and dQ at the
-// end); one thread of warp 13 issues the MMAs
-// in a fixed order, each group as soon as its inputs are there.  Partial rows leave shared
+// end); one thread of warp 13 issues the MMAs, each group as soon as its inputs are there
+// (dP^T before S^T, and S^T of the next chunk or the gradients of the current one, whichever
+// is ready first; the results do not depend on the order).  Partial rows leave shared
 // memory through the tensor memory accelerator (bulk copies, no load/store-unit work): at d = 64
 // one thread of warp 14 sends each chunk's staged rows as two copies (the dK half-rows and the
 // dV half-rows, 16 KB each: they go to two arrays) from two alternating staging buffers; at
@@ -117,6 +118,15 @@ DSV_DEVICE void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
 }
 DSV_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 DSV_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+DSV_DEVICE bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 DSV_DEVICE void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
@@ -250,8 +260,21 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       constexpr uint32_t idKV = tc::idesc_bf16(128, D, 0, 1);   // dV_c, dK_c: A K-major, B MN-major
       constexpr uint32_t idQ = tc::idesc_bf16(D, 64, 1, 1);     // dQ^T: A, B MN-major
       // S^T / dP^T of chunk c
-      auto issue_s = [&](int c) {
+      auto issue_dp = [&](int c) {  // dP^T of chunk c (frees its V stage)
         tc::fence_async_shared();  // the stage was written with cp.async (generic proxy)
+        tc::tc_fence_after();
+        const uint32_t aV = sV + (c % VST) * S::KV;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
+          const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
+          tc::mma_ss(tmem + kColDP, tc::smem_desc(aV + off_a, 16, 1024), tc::smem_desc(sDO + off_b, 16, 1024), idS,
+                     j > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(bar(bars.empty_v[c % VST]));
+      };
+      auto issue_sdp = [&](int c) {  // S^T and dP^T of chunk c together (d = 64)
+        tc::fence_async_shared();
         tc::tc_fence_after();
         const uint32_t aK = sK + (c % KST) * S::KV, aV = sV + (c % VST) * S::KV;
 #pragma unroll
@@ -265,6 +288,19 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         }
         tc::mma_commit(bar(bars.s_full));
         tc::mma_commit(bar(bars.empty_v[c % VST]));
+      };
+      auto issue_s = [&](int c) {  // S^T of chunk c; s_full then covers dP^T too
+        tc::fence_async_shared();
+        tc::tc_fence_after();
+        const uint32_t aK = sK + (c % KST) * S::KV;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+          const uint32_t off_a = (j >> 2) * (kChunk * 128) + (j & 3) * 32;
+          const uint32_t off_b = (j >> 2) * (64 * 128) + (j & 3) * 32;
+          tc::mma_ss(tmem + kColS, tc::smem_desc(aK + off_a, 16, 1024), tc::smem_desc(sQ + off_b, 16, 1024), idS,
+                     j > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(bar(bars.s_full));
       };
       // the dQ^T update of chunk c, then dV_c, dK_c (so the K stage frees first)
       auto issue_grads = [&](int c) {
@@ -290,21 +326,47 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         tc::mma_commit(bar(bars.pds_empty[c % NPDS]));
         if (c == nchunks - 1) tc::mma_commit(bar(bars.dq_full));
       };
-      // Fixed issue order S(0), then per chunk c: S(c+1), grads(c).  S(c+1) needs only the
-      // loaded stage and S^T(c) read out, both of which precede P(c); each wait blocks in the
-      // hardware (no polling), so an MMA group starts as soon as its inputs are there.
-      auto wait_kv = [&](int c) {
-        return tc::mbar_wait(bar(bars.full_k[c % KST]), (c / KST) & 1, kWaitLimit) &&
-               tc::mbar_wait(bar(bars.full_v[c % VST]), (c / VST) & 1, kWaitLimit);
-      };
-      bool ok_run = wait_kv(0);
-      if (ok_run) issue_s(0);
+      // Issue order per chunk c: dP^T(c+1) as soon as S^T/dP^T(c) have been read and V(c+1)
+      // has landed (the V rows are gathered two chunks ahead), then S^T(c+1) and the gradients
+      // of chunk c in whichever order their inputs arrive: S^T(c+1) waits for the K rows of
+      // chunk c+1, which can only be gathered once dQ of chunk c-1 has read their stage, and
+      // the gradients of chunk c free chunk c's K stage for chunk c+2.
+      auto wait_v = [&](int c) { return tc::mbar_wait(bar(bars.full_v[c % VST]), (c / VST) & 1, kWaitLimit); };
+      auto wait_k = [&](int c) { return tc::mbar_wait(bar(bars.full_k[c % KST]), (c / KST) & 1, kWaitLimit); };
+      // chunk 0: Q and dO land with the first K stage
+      bool ok_run = wait_v(0) && wait_k(0);
+      if (ok_run && D == 64) issue_sdp(0);
+      if (ok_run && D == 128) {
+        issue_dp(0);
+        issue_s(0);
+      }
       for (int c = 0; c < nchunks && ok_run; ++c) {
-        if (c + 1 < nchunks) {
-          ok_run = wait_kv(c + 1) &&
-                   tc::mbar_wait(bar(bars.s_empty), c & 1, kWaitLimit);
+        if (c + 1 < nchunks && D == 64) {  // four K stages: the K rows are never late
+          ok_run = wait_k(c + 1) && wait_v(c + 1) && tc::mbar_wait(bar(bars.s_empty), c & 1, kWaitLimit);
           if (!ok_run) break;
-          issue_s(c + 1);
+          issue_sdp(c + 1);
+        } else if (c + 1 < nchunks) {
+          ok_run = tc::mbar_wait(bar(bars.s_empty), c & 1, kWaitLimit) && wait_v(c + 1);
+          if (!ok_run) break;
+          issue_dp(c + 1);
+          // S^T(c + 1) waits for its K rows, the gradients of chunk c for P/dS(c): issue whichever
+          // is ready first (the gradients free chunk c's K stage for the rows of chunk c + 2)
+          bool s_done = false, g_done = false;
+          uint32_t spins = 0;
+          while (!(s_done && g_done)) {
+            if (!s_done && mbar_test(bar(bars.full_k[(c + 1) % KST]), ((c + 1) / KST) & 1)) {
+              issue_s(c + 1);
+              s_done = true;
+            } else if (!g_done && mbar_test(bar(bars.p_full[c % NPDS]), (c / NPDS) & 1) &&
+                       (DENSE || c < NDVK || mbar_test(bar(bars.dvk_empty[c % NDVK]), ((c / NDVK) - 1) & 1))) {
+              issue_grads(c);
+              g_done = true;
+            } else if (++spins > kWaitLimit) {
+              break;
+            }
+          }
+          ok_run = s_done && g_done;
+          continue;
         }
         ok_run = tc::mbar_wait(bar(bars.p_full[c % NPDS]), (c / NPDS) & 1, kWaitLimit) &&
                  (DENSE || c < NDVK || tc::mbar_wait(bar(bars.dvk_empty[c % NDVK]), ((c / NDVK) - 1) & 1, kWaitLimit));
