@@ -12,7 +12,7 @@
 //     dV_t += P^T . dO_b,  dK_t += dS^T . Q_b                     (M=128, N=d,   K=64)
 // Roles (416 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each on 32
 // of the 64 query columns; thread = key lane); warps 8, 10, 11 and 12 load the key tile once and
-// then each query block's Q, dO, LSE and D into a two-stage ring with cp.async (contiguous rows,
+// then each query block's Q, dO, LSE and D into a three-stage ring with cp.async (contiguous rows,
 // a quarter of every tile per warp: one warp alone cannot keep enough loads in flight); one
 // thread of warp 9 issues the MMAs (S / dP of block b + 1 ahead of the gradients of block b,
 // into two TMEM buffers).  At the end warps 0-3 move dK (times the scale) and dV out of tensor
@@ -38,15 +38,17 @@ struct DSm {
   static constexpr int T64 = BLK * 64 * 128;      // a [64 rows][D] tile (Q_b or dO_b)
   static constexpr int KV = BLK * kKeys * 128;    // a [128 rows][D] tile (K_t or V_t)
   static constexpr int P = kKeys * 128;           // [128 keys][64 q] bf16
-  static constexpr int OFF_K = 0, OFF_V = KV, OFF_Q = 2 * KV, OFF_DO = OFF_Q + 2 * T64, OFF_P = OFF_DO + 2 * T64,
+  static constexpr int QST = 3;                    // Q / dO stages
+  static constexpr int OFF_K = 0, OFF_V = KV, OFF_Q = 2 * KV, OFF_DO = OFF_Q + QST * T64,
+                       OFF_P = OFF_DO + QST * T64,
                        OFF_LD = OFF_P + 2 * P,  // per stage: LSE (64 floats), then D (64 floats)
-                       TOTAL = OFF_LD + 2 * 2 * 64 * 4;
+                       TOTAL = OFF_LD + QST * 2 * 64 * 4;
   static_assert(4 * T64 >= kKeys * 2 * D * 2, "the epilogue stages dK and dV in the Q / dO stages");
 };
 
 struct DBars {
   uint64_t kv_full;                  // K_t and V_t landed
-  uint64_t q_full[2], q_empty[2];    // per stage: Q_b, dO_b, LSE_b, D_b landed / no longer read
+  uint64_t q_full[3], q_empty[3];    // per stage: Q_b, dO_b, LSE_b, D_b landed / no longer read
   uint64_t s_full[2], s_empty[2];    // per TMEM buffer: S^T, dP^T ready / read
   uint64_t p_full, pds_empty;        // P, dS written / read by the gradient MMAs
   uint64_t acc_full;                 // last dV_t, dK_t update done
@@ -103,9 +105,11 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
   }
   if (tid == 0) {
     tc::mbar_init(bar(bars.kv_full), 32 * kProducers);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < S::QST; ++s) {
       tc::mbar_init(bar(bars.q_full[s]), 32 * kProducers);
       tc::mbar_init(bar(bars.q_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bar(bars.s_full[s]), 1);
       tc::mbar_init(bar(bars.s_empty[s]), kCompute);
     }
@@ -132,8 +136,8 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
     cp_async_arrive(bar(bars.kv_full));
     bool ok_run = true;
     for (int b = 0; b < NB && ok_run; ++b) {
-      const int st = b & 1;
-      if (b >= 2) ok_run = tc::mbar_wait(bar(bars.q_empty[st]), ((b >> 1) - 1) & 1, kWaitLimit);
+      const int st = b % S::QST;
+      if (b >= S::QST) ok_run = tc::mbar_wait(bar(bars.q_empty[st]), ((b / S::QST) - 1) & 1, kWaitLimit);
       ok_run = __all_sync(0xffffffffu, ok_run);
       if (!ok_run) break;
       copy_tile<D>(sQ + st * S::T64, 64, q + hrow * D, static_cast<int64_t>(b) * 64, qr0, qr0 + 64 / kProducers, N,
@@ -157,7 +161,7 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
       constexpr uint32_t idKV = tc::idesc_bf16(128, D, 0, 1);   // dV_t, dK_t: A K-major, B MN-major
       auto issue_s = [&](int b) {  // S^T and dP^T of block b into TMEM buffer b & 1
         tc::tc_fence_after();
-        const int st = b & 1;
+        const int st = b % S::QST;
         const uint32_t col = (b & 1) * 64;
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
@@ -168,10 +172,10 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
           tc::mma_ss(tmem + kColDP + col, tc::smem_desc(sV + off_a, 16, 1024),
                      tc::smem_desc(sDO + st * S::T64 + off_b, 16, 1024), idS, j > 0 ? 1u : 0u);
         }
-        tc::mma_commit(bar(bars.s_full[st]));
+        tc::mma_commit(bar(bars.s_full[b & 1]));
       };
       auto s_ready = [&](int b) {
-        return tc::mbar_wait(bar(bars.q_full[b & 1]), (b >> 1) & 1, kWaitLimit) &&
+        return tc::mbar_wait(bar(bars.q_full[b % S::QST]), (b / S::QST) & 1, kWaitLimit) &&
                (b < 2 || tc::mbar_wait(bar(bars.s_empty[b & 1]), ((b >> 1) - 1) & 1, kWaitLimit));
       };
       bool ok_run = tc::mbar_wait(bar(bars.kv_full), 0, kWaitLimit) && s_ready(0);
@@ -185,7 +189,7 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
         ok_run = tc::mbar_wait(bar(bars.p_full), b & 1, kWaitLimit);
         if (!ok_run) break;
         tc::tc_fence_after();
-        const int st = b & 1;
+        const int st = b % S::QST;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // K = 64 queries
           tc::mma_ss(tmem + kColDV, tc::smem_desc(sP + j * 32, 16, 1024),
@@ -221,7 +225,7 @@ dense_dkdv_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const 
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::mbar_arrive(bar(bars.s_empty[st]));
-      const float* lsb = ld_s + st * 128;
+      const float* lsb = ld_s + (b % S::QST) * 128;
       uint32_t pw[16], dw[16];  // packed bf16 pairs of P and dS
 #pragma unroll
       for (int i4 = 0; i4 < 8; ++i4) {
