@@ -135,10 +135,21 @@ bool plan_for(const dsv_dims* d, size_t budget, WavePlan* out) {
     }
     if (nh == 1) break;
   }
+  // blocks of one head per wave: the largest even split that fits, rounded down to whole waves of
+  // the main kernel's CTAs (one per SM), so that only a head's last wave ends in a partial one
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    sms = 0;
+    (void)cudaGetLastError();  // no device (a size query on a host without one): no rounding
+  }
   for (int64_t s = 2; s <= NB; s = (s < 64 ? s + 1 : s + s / 8)) {
-    const int64_t nblk = (NB + s - 1) / s;
+    int64_t nblk = (NB + s - 1) / s;
     WavePlan w{1, nblk, true};
-    if (plan_bytes(d, w) <= budget) { *out = w; return true; }
+    if (plan_bytes(d, w) <= budget) {
+      if (sms > 0 && nblk > sms) w.nblk = nblk / sms * sms;
+      *out = w;
+      return true;
+    }
   }
   WavePlan w{1, 1, NB > 1};
   if (plan_bytes(d, w) <= budget) { *out = w; return true; }
@@ -494,21 +505,20 @@ dsv_status bwd_impl(const dsv_dims* dims, const void* d_o, const void* q, const 
   p.order = order;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<dsv::BwdWave> waves;
   if (!plan.sub) {
-    for (int64_t bh0 = 0; bh0 < p.BH; bh0 += plan.nh) {
-      dsv::BwdWave w{bh0, plan.nh < p.BH - bh0 ? plan.nh : p.BH - bh0, 0, p.NB, true, true};
-      cudaError_t e = dsv::launch_bwd_wave(p, w, st, parts);
-      if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
-    }
+    for (int64_t bh0 = 0; bh0 < p.BH; bh0 += plan.nh)
+      waves.push_back(dsv::BwdWave{bh0, plan.nh < p.BH - bh0 ? plan.nh : p.BH - bh0, 0, p.NB, true, true});
   } else {
-    for (int64_t bh = 0; bh < p.BH; ++bh) {
+    for (int64_t bh = 0; bh < p.BH; ++bh)
       for (int64_t b0 = 0; b0 < p.NB; b0 += plan.nblk) {
         const int64_t n = plan.nblk < p.NB - b0 ? plan.nblk : p.NB - b0;
-        dsv::BwdWave w{bh, 1, b0, n, b0 == 0, b0 + n == p.NB};
-        cudaError_t e = dsv::launch_bwd_wave(p, w, st);
-        if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+        waves.push_back(dsv::BwdWave{bh, 1, b0, n, b0 == 0, b0 + n == p.NB});
       }
-    }
+  }
+  for (const dsv::BwdWave& w : waves) {
+    cudaError_t e = dsv::launch_bwd_wave(p, w, st, parts);
+    if (e != cudaSuccess) return fail(DSV_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   }
   return ok();
 }

@@ -229,7 +229,7 @@ def test_backward_is_deterministic_and_wave_independent():
     again = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx)
     dims = make_dims(1, 2, wl.N, wl.d, wl.r, wl.k)
     small = dsv_sparse_attn_bwd_workspace(dims, minimum=True)
-    for nbytes in (small, small * 3, small * 12):   # sub-head waves of one or a few blocks
+    for nbytes in (small, small * 2, small * 3, small * 5, small * 12, small * 40):  # sub-head waves of a few blocks
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         other = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws)
         for a, b in zip(ref, other):
@@ -256,3 +256,25 @@ def test_out_of_range_and_repeated_indices_set_the_device_status():
     o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
     dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, dup)
     assert dsv_last_device_status() == 5
+
+
+def test_multi_wave_backward_matches_one_wave_bitwise():
+    """The short clip's backward through workspaces that hold a whole head, part of a head, or a
+    few blocks per wave (waves whose rank structure is built on a second stream while the previous
+    wave is reduced, where the workspace has room for two copies of it): bitwise the one-wave
+    gradients."""
+    dev = need_gpu()
+    wl = WORKLOADS["short"].with_heads(3)
+    g = _to(dev, make_inputs(wl))
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+    ref = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx)
+    dims = make_dims(1, 3, wl.N, wl.d, wl.r, wl.k)
+    rec = dsv_sparse_attn_bwd_workspace(dims)
+    for frac in (0.6, 0.34, 0.2, 0.07, 0.03):
+        ws = torch.empty(int(rec * frac) // 256 * 256, dtype=torch.uint8, device=dev)
+        other = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws)
+        for a, b in zip(ref, other):
+            assert torch.equal(a, b), f"workspace fraction {frac}"
+    torch.cuda.synchronize()
+    assert dsv_last_device_status() == 0
