@@ -11,8 +11,10 @@
 // out as bf16 partial rows, block-major (this CTA's k rows are contiguous), and the list of
 // every key's rows in ascending block order is written alongside; a separate kernel sums
 // every key's rows in that fixed order (deterministic, no float atomics).
-// P and dS are written once to shared memory as bf16 128-byte rows (one per key); the same
-// bytes are the K-major A operand of dV_c / dK_c and the MN-major B operand of dQ^T.
+// P^T and dS^T go to tensor memory as bf16 pairs (a key's row in its own TMEM lane, where the
+// thread that computed it writes it): the A operands of dV_c and dK_c, read by the tensor core
+// without a trip through shared memory.  dS is also written to shared memory as bf16 128-byte
+// rows (one per key), the MN-major B operand of dQ^T.
 // Roles (512 threads): warps 0-7 compute P and dS (two warps per TMEM lane quadrant, each
 // on 32 of the 64 query columns; thread = key lane of S^T / dP^T); warps 8-11 read dV_c /
 // dK_c out of TMEM into shared-memory staging rows and write the key lists (and dQ at the
@@ -53,13 +55,16 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 // TMEM columns: S^T, dP^T, dQ^T (64 each), then dV_c, dK_c (d each) in one buffer (d = 128)
 // or two (d = 64: the MMAs of the next chunk fill one while the partial rows leave the other)
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kTmemCols = 512;
+// P^T and dS^T of the current chunk: 128 key lanes x 64 queries, two bf16 per column (the even
+// query in the low half), the A operands of dV_c and dK_c
+constexpr uint32_t kColP = 448, kColDS = 480;
 
 template <int D>
 struct Sm {
   static constexpr int KST = D == 64 ? 4 : 2;         // K stages (held until dQ)
   static constexpr int VST = 2;                       // V stages (held until dP, which is issued
                                                       // a chunk ahead of the gradients)
-  static constexpr int NPDS = 1;                      // P / dS tile pairs
+  static constexpr int NPDS = 1;                      // dS tiles (and P^T / dS^T TMEM sets)
   static constexpr int NST = D == 64 ? 2 : 1;         // staging buffers (d = 64: the store thread
                                                       // drains one while the other fills; d = 128:
                                                       // each readout warp sends its own rows)
@@ -73,9 +78,9 @@ struct Sm {
   static constexpr int BLK = D / 64;
   static constexpr int T64 = BLK * 64 * 128;          // a [64 rows][D] tile
   static constexpr int KV = BLK * kChunk * 128;       // a [128 rows][D] tile
-  static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16
+  static constexpr int P = kChunk * 128;              // [128 keys][64 q] bf16 (a dS tile)
   static constexpr int OFF_Q = 0, OFF_DO = OFF_Q + T64, OFF_K = OFF_DO + T64, OFF_V = OFF_K + KST * KV,
-                       OFF_P = OFF_V + VST * KV, OFF_ST = OFF_P + NPDS * 2 * P,  // pair b: P, then dS
+                       OFF_DS = OFF_V + VST * KV, OFF_ST = OFF_DS + NPDS * P,
                        TOTAL = OFF_ST + NST * STB;
 };
 
@@ -184,7 +189,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
   }
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + S::OFF_Q, sDO = sbase + S::OFF_DO, sK = sbase + S::OFF_K, sV = sbase + S::OFF_V;
-  const uint32_t sPDS = sbase + S::OFF_P;  // tile pair b: P at sPDS + b * 2 * S::P, dS after it
+  const uint32_t sDS0 = sbase + S::OFF_DS;  // dS tile b at sDS0 + b * S::P
   auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
   if (sbase & 1023u) {  // swizzled tiles need 1024-byte alignment
@@ -306,7 +311,7 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       auto issue_grads = [&](int c) {
         tc::tc_fence_after();
         const uint32_t cdv = S::COL_DV + (c % NDVK) * 2 * D;
-        const uint32_t sP = sPDS + (c % NPDS) * 2 * S::P, sDS = sP + S::P;
+        const uint32_t sDS = sDS0 + (c % NPDS) * S::P;
         const uint32_t aK = sK + (c % KST) * S::KV;
 #pragma unroll
         for (int j = 0; j < kChunk / 16; ++j)  // K = 128 keys
@@ -316,10 +321,10 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         if (!DENSE) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // K = 64 queries
-            tc::mma_ss(tmem + cdv, tc::smem_desc(sP + j * 32, 16, 1024), tc::smem_desc(sDO + j * 2048, 64 * 128, 1024),
-                       idKV, j > 0 ? 1u : 0u);
-            tc::mma_ss(tmem + cdv + D, tc::smem_desc(sDS + j * 32, 16, 1024),
-                       tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV, j > 0 ? 1u : 0u);
+            tc::mma_ts(tmem + cdv, tmem + kColP + j * 8, tc::smem_desc(sDO + j * 2048, 64 * 128, 1024), idKV,
+                       j > 0 ? 1u : 0u);
+            tc::mma_ts(tmem + cdv + D, tmem + kColDS + j * 8, tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV,
+                       j > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(bars.dvk_full[c % NDVK]));
         }
@@ -443,15 +448,18 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
       }
       const int pb = c % NPDS;
       if (c >= NPDS) ok_run = ok_run && tc::mbar_wait(bar(bars.pds_empty[pb]), ((c / NPDS) - 1) & 1, kWaitLimit);
-      const uint32_t prow = sPDS + pb * 2 * S::P + t * 128, drow = prow + S::P;
+      const uint32_t drow = sDS0 + pb * S::P + t * 128;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int ch = hq * 4 + cc;
         const uint32_t off = ((ch ^ t) & 7) << 4;
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + off), "r"(pw[cc * 4]), "r"(pw[cc * 4 + 1]),
-                     "r"(pw[cc * 4 + 2]), "r"(pw[cc * 4 + 3]));
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(drow + off), "r"(dw[cc * 4]), "r"(dw[cc * 4 + 1]),
                      "r"(dw[cc * 4 + 2]), "r"(dw[cc * 4 + 3]));
+      }
+      if (!DENSE) {  // this key lane's P^T and dS^T columns (query pairs 16 hq .. 16 hq + 15) in TMEM
+        tc::tmem_st16(tmem + lane_base + kColP + hq * 16, pw);
+        tc::tmem_st16(tmem + lane_base + kColDS + hq * 16, dw);
+        tc::tmem_wait_st();
       }
       tc::fence_async_shared();
       tc::tc_fence_before();
