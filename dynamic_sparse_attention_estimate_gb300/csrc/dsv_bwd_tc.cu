@@ -95,6 +95,15 @@ struct Bars {
   uint64_t drain;                  // MMA commit at the end: every MMA issued is done
 };
 
+// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A (M = 128) sits K-major in TMEM: row m
+// in lane m, two bf16 per 32-bit column (the even K element in the low half), K elements
+// 16 j .. 16 j + 15 in columns 8 j .. 8 j + 7 from a_tmem.
+DSV_DEVICE void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
 DSV_DEVICE void sync_group(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
 DSV_DEVICE bool sync_group_or(int id, bool v) {
   uint32_t r;
@@ -321,9 +330,9 @@ sparse_bwd_tc_kernel(BwdParams p, int64_t bh0, int64_t blk0, int64_t nblk, int64
         if (!DENSE) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // K = 64 queries
-            tc::mma_ts(tmem + cdv, tmem + kColP + j * 8, tc::smem_desc(sDO + j * 2048, 64 * 128, 1024), idKV,
+            mma_ts(tmem + cdv, tmem + kColP + j * 8, tc::smem_desc(sDO + j * 2048, 64 * 128, 1024), idKV,
                        j > 0 ? 1u : 0u);
-            tc::mma_ts(tmem + cdv + D, tmem + kColDS + j * 8, tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV,
+            mma_ts(tmem + cdv + D, tmem + kColDS + j * 8, tc::smem_desc(sQ + j * 2048, 64 * 128, 1024), idKV,
                        j > 0 ? 1u : 0u);
           }
           tc::mma_commit(bar(bars.dvk_full[c % NDVK]));
