@@ -50,6 +50,8 @@ class AdalnDims(ctypes.Structure):
 
 
 def library_path() -> str:
+    """The in-tree libdsv.so, or the file the DSV_LIBRARY variable names (another build of the same
+    sources, e.g. one made with different compiler flags)."""
     return os.environ.get("DSV_LIBRARY") or os.path.join(_HERE, _LIB_NAME)
 
 
