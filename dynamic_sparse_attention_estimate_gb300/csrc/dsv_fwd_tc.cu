@@ -21,10 +21,11 @@
 //              rows are gathered as soon as the S^T product two chunks back has read the
 //              stage's K, while its V rows wait for that chunk's PV product; keys past k or
 //              out of range are zero-filled;
-//   warp 5     one thread issues every MMA as soon as its inputs are ready: it waits in the
-//              hardware, for a short bounded time, on the barrier of the product that comes
-//              next in the usual order (the PV product of the oldest chunk with an S^T), and
-//              checks the other between waits, so neither order of readiness stalls it.
+//   warp 5     one thread issues every MMA as soon as its inputs are ready, an S^T product
+//              before a PV product when both are (the softmax waits for S^T, while a PV product
+//              has until the softmax writes P^T two chunks later): it checks the S^T product's
+//              barriers, then waits in the hardware, for a short bounded time, on the PV
+//              product's.
 // Dense blocks (every key selected, k = N): the DENSE instantiation reads no idx; chunk c holds
 // keys 128 c .. 128 c + 127 (contiguous rows, the same arithmetic otherwise).
 // The running max m_q is kept STALE: a chunk only triggers the cross-thread column max and
@@ -347,29 +348,14 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
       int cs = 0, cp = 0;
       uint32_t idle = 0;
       while (ok_run && cp < nchunks) {
-        // the usual next product is PV(cp) once S(cp) exists; otherwise S(cs)
+        // S(cs) whenever its K rows have landed and its TMEM buffer is free (a softmax that waits
+        // for S^T must not find it queued behind a PV product), otherwise PV(cp) once S(cp) exists,
+        // waiting for it in the hardware for a short bounded time
         const bool pv_next = cp < cs;
-        if (pv_next && mbar_try_wait_ns(bar(bars.p_full[cp & 1]), (cp >> 1) & 1, 64) &&
-            mbar_try_wait_ns(bar(bars.full_v[cp % NST]), (cp / NST) & 1, 64)) {
-          // PV(cp): O^T += V_c^T P^T
-          tc::tc_fence_after();
-          const uint32_t aV = sV + (cp % NST) * S::KV_BYTES, bP = sP + (cp & 1) * S::P_BYTES;
-#pragma unroll
-          for (int j = 0; j < kChunk / 16; ++j) {
-            // second 64-row block of A: the next 64 head dims (d = 128) or the ones tile
-            const uint32_t a = aV + j * 2048, lbo = kOnesRow<D> ? sOnes - a : kChunk * 128;
-            tc::mma_ss(tmem + kColO, tc::smem_desc(a, lbo, 1024), tc::smem_desc(bP + j * 2048, 8192, 1024), idO,
-                       (cp > 0 || j > 0) ? 1u : 0u);
-          }
-          tc::mma_commit(bar(bars.pv_done[cp & 1]));
-          tc::mma_commit(bar(bars.empty_v[cp % NST]));
-          if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
-          ++cp;
-          idle = 0;
-        } else if (cs < nchunks &&
-                   (pv_next ? mbar_test(bar(bars.full_k[cs % NST]), (cs / NST) & 1)
-                            : mbar_try_wait_ns(bar(bars.full_k[cs % NST]), (cs / NST) & 1, 64)) &&
-                   (cs < 2 || mbar_test(bar(bars.s_empty[cs & 1]), ((cs - 2) >> 1) & 1))) {
+        if (cs < nchunks &&
+            (pv_next ? mbar_test(bar(bars.full_k[cs % NST]), (cs / NST) & 1)
+                     : mbar_try_wait_ns(bar(bars.full_k[cs % NST]), (cs / NST) & 1, 64)) &&
+            (cs < 2 || mbar_test(bar(bars.s_empty[cs & 1]), ((cs - 2) >> 1) & 1))) {
           // S(cs): S^T = K_c Q^T.  The stage was written with cp.async (generic proxy):
           // order those writes before the tensor core's reads.
           tc::fence_async_shared();
@@ -385,6 +371,23 @@ sparse_fwd_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
           tc::mma_commit(bar(bars.s_full[cs & 1]));
           tc::mma_commit(bar(bars.empty_k[cs % NST]));
           ++cs;
+          idle = 0;
+        } else if (pv_next && mbar_try_wait_ns(bar(bars.p_full[cp & 1]), (cp >> 1) & 1, 64) &&
+                   mbar_try_wait_ns(bar(bars.full_v[cp % NST]), (cp / NST) & 1, 64)) {
+          // PV(cp): O^T += V_c^T P^T
+          tc::tc_fence_after();
+          const uint32_t aV = sV + (cp % NST) * S::KV_BYTES, bP = sP + (cp & 1) * S::P_BYTES;
+#pragma unroll
+          for (int j = 0; j < kChunk / 16; ++j) {
+            // second 64-row block of A: the next 64 head dims (d = 128) or the ones tile
+            const uint32_t a = aV + j * 2048, lbo = kOnesRow<D> ? sOnes - a : kChunk * 128;
+            tc::mma_ss(tmem + kColO, tc::smem_desc(a, lbo, 1024), tc::smem_desc(bP + j * 2048, 8192, 1024), idO,
+                       (cp > 0 || j > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(bar(bars.pv_done[cp & 1]));
+          tc::mma_commit(bar(bars.empty_v[cp % NST]));
+          if (cp == nchunks - 1) tc::mma_commit(bar(bars.o_full));
+          ++cp;
           idle = 0;
         } else if (++idle > kPollLimit) {
           ok_run = false;
