@@ -17,6 +17,8 @@
 //   5. reduce: dK_j, dV_j = sum of key j's rows in list order (fp32), written as bf16.
 // A head whose partial rows do not fit in the workspace is split into several waves
 // whose sums are chained through an fp32 accumulator.
+#include <climits>
+
 #include "dsv_common.cuh"
 #include "dsv_internal.h"
 
@@ -25,12 +27,15 @@ namespace {
 
 
 // ---------------------------------------------------------------- 1. column bitmaps
-// One CTA per (key tile, half of a 32-block word group, head slot).  The half's 16 blocks are
-// contiguous in idx (fixed k and CSR alike), so the CTA walks that range flat, ORs each key's
-// block bit into a shared-memory tile (16 bits per key, two keys per word) and then writes the
-// tile out as its half-words of colbits.  Every word of the wave is written (zeros included):
-// no clearing pass and no global atomics.  A key outside [0, N) or a key twice in one row sets
-// the bad-index status.
+// One CTA per (key tile, half of a 32-block word group, head slot) ORs each key's block bit into
+// a shared-memory tile (16 bits per key, two keys per word) and then writes the tile out as its
+// half-words of colbits.  Every word of the wave is written (zeros included): no clearing pass and
+// no global atomics.  With fixed k, a first kernel records for every row where its keys cross each
+// tile boundary (the selection writes rows strictly ascending), so a tile's CTA reads only its
+// rows' runs in that tile; a row that is not strictly ascending is marked there, and the CTA
+// filters all of that row's entries instead (the general method, which CSR rows always take: the
+// half's 16 blocks are contiguous in idx, so the CTA walks that range flat).  A key outside
+// [0, N) or a key twice in one row sets the bad-index status.
 constexpr int kBitsThreads = 1024;
 constexpr int64_t kBitsTile = 32768;  // keys per tile: 64 KB of shared memory
 
@@ -59,12 +64,48 @@ __device__ __forceinline__ void set_bit(uint32_t* tile, const int64_t* rp, int n
   if (old & bit) flag_status(status, kStatusBadIndex);  // duplicate key in one idx row
 }
 
+// Tile bounds of fixed-k rows: for row r of the wave (global row row0 + r) and tile t in [0, ntile],
+// b[t] = the position of the row's first entry whose key is at least kBitsTile t (entries before
+// b[0] have negative keys, entries from b[ntile] on keys past the last tile); b[ntile + 1] != 0
+// when the row is not strictly ascending (the bounds then mean nothing).  One thread per entry: a
+// boundary lies between two neighbouring entries, so every b[t] of an ascending row is written
+// once.  The bounds are zeroed before.  A CTA covers kBoundsSpan entries of one row.
+constexpr int kBoundsThreads = 256;
+constexpr int kBoundsPerThread = 8;
+constexpr int kBoundsSpan = kBoundsThreads * kBoundsPerThread;
+__global__ void __launch_bounds__(kBoundsThreads)
+tile_bounds_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ bounds, int64_t kk, int64_t row0,
+                   int64_t r0, int ntile) {
+  const int64_t r = r0 + blockIdx.y;
+  const int32_t* row = idx + (row0 + r) * kk;
+  int32_t* b = bounds + r * (ntile + 2);
+  auto tile_of = [&](int32_t key) -> int {
+    return key < 0 ? -1 : ((key >> 15) < ntile ? (key >> 15) : ntile);  // kBitsTile = 2^15
+  };
+#pragma unroll
+  for (int u = 0; u < kBoundsPerThread; ++u) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kBoundsSpan + u * kBoundsThreads + threadIdx.x;
+    if (i >= kk) break;
+    const int32_t key = __ldg(row + i);
+    const int32_t before = i > 0 ? __ldg(row + i - 1) : INT_MIN;
+    const int pk = tile_of(key), pb = i > 0 ? tile_of(before) : -1;
+    for (int t = pb + 1; t <= pk; ++t) b[t] = static_cast<int32_t>(i);
+    if (i == kk - 1)
+      for (int t = pk + 1; t <= ntile; ++t) b[t] = static_cast<int32_t>(kk);
+    if (i > 0 && key <= before) b[ntile + 1] = 1;
+  }
+}
+static_assert(kBitsTile == 32768, "tile_bounds_kernel divides keys by shifting");
+// Below this many key tiles the general method reads each row only a few times: no bounds.
+constexpr int kBoundsMinTiles = 8;
+
 __global__ void __launch_bounds__(kBitsThreads)
 set_bits_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ rowptr, uint32_t* __restrict__ colbits,
                 int64_t N, int64_t NB, int64_t kk, int64_t bh0, int64_t blk0, int64_t nblk, int64_t W32, int64_t hs0,
-                unsigned int* status) {
+                const int32_t* __restrict__ bounds, int ntile, unsigned int* status) {
   extern __shared__ uint32_t tile[];  // word i: key 2 i in bits 0-15, key 2 i + 1 in bits 16-31
   __shared__ int64_t rp[17];
+  __shared__ int32_t run0[16], runoff[17], irr[16];
   const int tid = threadIdx.x;
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kBitsTile;
   const int64_t tj = N - j0 < kBitsTile ? N - j0 : kBitsTile;
@@ -76,10 +117,56 @@ set_bits_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict__ row
   const int64_t g0 = (bh0 + hs) * NB + blk0 + lb0;  // global row of the half's first block
   for (int64_t i = tid; i < (tj + 1) / 2; i += kBitsThreads) tile[i] = 0;
   if (nrows > 0 && tid <= nrows) rp[tid] = rowptr ? rowptr[g0 + tid] : (g0 + tid) * kk;
+  const int tt = static_cast<int>(blockIdx.x);
+  if (bounds && tid < 16) {
+    int32_t lo = 0, hi = 0, ir = 0;
+    if (tid < nrows) {
+      const int32_t* b = bounds + (hs * nblk + lb0 + tid) * (ntile + 2);
+      lo = b[tt];
+      hi = b[tt + 1];
+      ir = b[ntile + 1];
+      if (!ir && ((tt == 0 && b[0] > 0) || (tt == ntile - 1 && b[ntile] < kk)))
+        flag_status(status, kStatusBadIndex);  // keys below 0 or past the last tile
+      if (ir || hi < lo) lo = hi = 0;
+    }
+    run0[tid] = lo;
+    runoff[tid] = hi - lo;  // length for now; the prefix below
+    irr[tid] = ir;
+  }
+  __syncthreads();
+  if (bounds && tid == 0) {
+    int32_t acc = 0;
+    for (int r = 0; r < 16; ++r) {
+      const int32_t len = runoff[r];
+      runoff[r] = acc;
+      acc += len;
+    }
+    runoff[16] = acc;
+  }
   __syncthreads();
   const bool csr = rowptr != nullptr;
   const bool report = blockIdx.x == 0;  // range errors are reported by the first key tile only
-  if (nrows > 0) {
+  if (bounds) {
+    // every ascending row's run in this tile, as one flat range
+    const int32_t total = runoff[16];
+    int r = 0;  // the row of entry e: e only grows, so r is carried from one entry to the next
+    for (int32_t e = tid; e < total; e += kBitsThreads) {
+      while (r < 15 && runoff[r + 1] <= e) ++r;
+      const int32_t key = __ldg(idx + rp[r] + run0[r] + (e - runoff[r]));
+      const int64_t jj = static_cast<int64_t>(key) - j0;
+      if (key >= N || jj < 0 || jj >= tj) {
+        flag_status(status, kStatusBadIndex);  // past N inside the last tile
+        continue;
+      }
+      const uint32_t bit = 1u << (r + 16 * static_cast<int>(jj & 1));
+      if (atomicOr(tile + (jj >> 1), bit) & bit) flag_status(status, kStatusBadIndex);
+    }
+    // rows not strictly ascending: the general method, their entries filtered
+    for (int r = 0; r < nrows; ++r)
+      if (irr[r])
+        for (int64_t i = rp[r] + tid; i < rp[r + 1]; i += kBitsThreads)
+          set_bit(tile, rp, nrows, rp[0], kk, false, i, __ldg(idx + i), j0, tj, N, report, status);
+  } else if (nrows > 0) {
     const int64_t first = rp[0], last = rp[nrows];
     // scalar head and tail, 16-byte loads in between
     const int64_t a0 = ((first + 3) & ~int64_t(3)) < last ? ((first + 3) & ~int64_t(3)) : last;
@@ -290,12 +377,30 @@ cudaError_t launch_wave_prep(const BwdParams& p, const BwdWave& w, cudaStream_t 
   cudaError_t e = cudaFuncSetAttribute(set_bits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(bits_smem));
   if (e != cudaSuccess) return e;
+  // fixed k over many key tiles: tile bounds of every row of the wave, in the offsets array (written
+  // only later, by the scan); with few tiles (each row then read only a few times), CSR rows, or
+  // bounds that would not fit there, the general method
+  const int nt = static_cast<int>(ntile);
+  const int64_t rows = w.nh * w.nblk;
+  const size_t bounds_bytes = sizeof(int32_t) * static_cast<size_t>(rows) * static_cast<size_t>(nt + 2);
+  const int32_t* bounds = nullptr;
+  if (nt >= kBoundsMinTiles && !p.rowptr && p.topk >= 1 && bounds_bytes <= sizeof(int64_t) * static_cast<size_t>(w.nh * N)) {
+    int32_t* bw = reinterpret_cast<int32_t*>(p.offsets);
+    if ((e = cudaMemsetAsync(bw, 0, bounds_bytes, stream)) != cudaSuccess) return e;
+    ProfScope prof("bwd_tile_bounds", stream);
+    for (int64_t r0 = 0; r0 < rows; r0 += 65535) {
+      const unsigned nr = static_cast<unsigned>(rows - r0 < 65535 ? rows - r0 : 65535);
+      tile_bounds_kernel<<<dim3(static_cast<unsigned>((p.topk + kBoundsSpan - 1) / kBoundsSpan), nr),
+                           kBoundsThreads, 0, stream>>>(p.idx, bw, p.topk, w.bh0 * p.NB + w.blk0, r0, nt);
+    }
+    bounds = bw;
+  }
   for (int64_t hs0 = 0; hs0 < w.nh; hs0 += 65535) {  // grid y / z limit
     const unsigned nh = static_cast<unsigned>(w.nh - hs0 < 65535 ? w.nh - hs0 : 65535);
     { ProfScope prof("bwd_set_bits", stream);
     set_bits_kernel<<<dim3(static_cast<unsigned>(ntile), static_cast<unsigned>(2 * W32), nh), kBitsThreads,
                       bits_smem, stream>>>(p.idx, p.rowptr, p.colbits, N, p.NB, p.topk, w.bh0, w.blk0, w.nblk, W32,
-                                           hs0, p.status); }
+                                           hs0, bounds, nt, p.status); }
     { ProfScope prof("bwd_colpre", stream);
     colpre_kernel<<<dim3(static_cast<unsigned>(nscan), nh), kScanThreads, 0, stream>>>(
         p.colbits, p.colpre, p.count, p.tsum, N, W32, hs0); }

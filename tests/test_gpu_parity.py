@@ -239,6 +239,49 @@ def test_backward_is_deterministic_and_wave_independent():
     assert dsv_last_device_status() == 0
 
 
+def test_backward_with_unordered_idx_rows_matches_ascending():
+    """The backward does not need ascending idx rows (only distinct keys): its bitmap kernel walks
+    ascending rows once and falls back to filtering every row per key tile when a row is out of
+    order.  Rows reversed or rotated give the same dK and dV bit for bit (each (block, key)
+    contribution is the same product and every key's contributions are summed in block order) and
+    dQ up to the order of its fp32 accumulation over chunks; also across sub-head waves."""
+    dev = need_gpu()
+    for wl in (WORKLOADS["tiny"].with_heads(2), Workload("ragged", 1, 2, (5, 16, 16), 128, 32, 100, None, lr_max=8)):
+        g = _to(dev, make_inputs(wl))
+        idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+        o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+        ref = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx)
+        small = dsv_sparse_attn_bwd_workspace(make_dims(1, wl.H, wl.N, wl.d, wl.r, wl.k), minimum=True)
+        for perm in (idx.flip(-1).contiguous(), torch.roll(idx, 37, dims=-1).contiguous()):
+            for ws in (None, torch.empty(small * 3, dtype=torch.uint8, device=dev)):
+                dq, dk, dv = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, perm, workspace=ws)
+                assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+                err = (dq.float() - ref[0].float()).abs().max().item()
+                assert err <= 1e-2 * ref[0].float().abs().max().item() + 1e-3, err
+        assert dsv_last_device_status() == 0
+
+
+def test_backward_tile_bounds_path_matches_the_general_path():
+    """Over many key tiles (here nine, the last one partial) the backward's bitmap kernel reads only
+    each ascending row's run per tile, from tile bounds found by a first pass; rows out of order take
+    the general method.  The same rows ascending and reversed must give the same dK and dV bit for
+    bit, in one wave and across sub-head waves (whose bounds start at a block offset)."""
+    dev = need_gpu()
+    wl = Workload("tiles", 1, 1, (17, 128, 128), 64, 16, 96, (4, 4, 4))
+    assert (wl.N + 32767) // 32768 == 9
+    g = _to(dev, make_inputs(wl))
+    idx = dsv_estimate_topk(g["q_lr"], g["k_lr"], wl.k)
+    o, lse = dsv_sparse_attn_fwd(g["q"], g["k"], g["v"], idx)
+    small = dsv_sparse_attn_bwd_workspace(make_dims(1, 1, wl.N, wl.d, wl.r, wl.k), minimum=True)
+    for ws in (None, torch.empty(small + 30_000_000, dtype=torch.uint8, device=dev)):  # waves of ~1,000 blocks
+        asc = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx, workspace=ws)
+        rev = dsv_sparse_attn_bwd(g["do"], g["q"], g["k"], g["v"], o, lse, idx.flip(-1).contiguous(), workspace=ws)
+        assert torch.equal(asc[1], rev[1]) and torch.equal(asc[2], rev[2])
+        err = (asc[0].float() - rev[0].float()).abs().max().item()
+        assert err <= 1e-2 * asc[0].float().abs().max().item() + 1e-3, err
+    assert dsv_last_device_status() == 0
+
+
 def test_out_of_range_and_repeated_indices_set_the_device_status():
     dev = need_gpu()
     wl = WORKLOADS["tiny"].with_heads(1)
