@@ -67,9 +67,10 @@ __device__ __forceinline__ void set_bit(uint32_t* tile, const int64_t* rp, int n
 // Tile bounds of fixed-k rows: for row r of the wave (global row row0 + r) and tile t in [0, ntile],
 // b[t] = the position of the row's first entry whose key is at least kBitsTile t (entries before
 // b[0] have negative keys, entries from b[ntile] on keys past the last tile); b[ntile + 1] != 0
-// when the row is not strictly ascending (the bounds then mean nothing).  One thread per entry: a
-// boundary lies between two neighbouring entries, so every b[t] of an ascending row is written
-// once.  The bounds are zeroed before.  A CTA covers kBoundsSpan entries of one row.
+// when the row is not strictly ascending (the bounds then mean nothing).  Each entry is compared
+// with the one before it: a boundary lies between two neighbouring entries, so every b[t] of an
+// ascending row is written once.  The bounds are zeroed before.  A CTA covers kBoundsSpan entries
+// of one row, a thread kBoundsPerThread of them.
 constexpr int kBoundsThreads = 256;
 constexpr int kBoundsPerThread = 8;
 constexpr int kBoundsSpan = kBoundsThreads * kBoundsPerThread;
